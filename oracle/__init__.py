@@ -1,0 +1,256 @@
+"""CPU oracles for pillar voxelization.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the
+benchmark's CPU-baseline leg may import this package; the product path must
+never route through it.  It shares no code with the CUDA library.
+
+Three independent restatements of one definition (the page "Voxelize",
+ethan-howes.github.io/projects/voxelize/, sections "Implementation > Binning
+a point", "Claiming a pillar and packing points", "Compaction", "The PyTorch
+side" and "Results"):
+
+* :func:`voxelize`            the sequential std::map pass in C++
+                              (``pv_oracle.cpp``), the primary oracle;
+* :func:`voxelize_numpy`      a vectorised NumPy restatement built on a stable
+                              sort (``np.unique`` + ``argsort(kind="stable")``);
+* :func:`voxelize_bruteforce` the O(N^2) definition in plain Python, for tiny
+                              clouds: rank(i) = number of distinct pillars whose
+                              first point precedes pillar(i)'s first point,
+                              pos(i) = number of earlier points in pillar(i).
+
+Canonical order (the page's hash-slot order is nondeterministic, "Results";
+the deterministic reading used here): pillars in ascending order of their
+lowest-index valid point, points inside a pillar in index order, the first
+``max_points`` points and the first ``max_voxels`` pillars kept, everything
+else zero.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+from typing import Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pv_oracle.cpp")
+_LIB = os.path.join(_HERE, "libpv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK = 0
+ERR_INVALID = -1
+ERR_UNSUPPORTED = -2
+
+GXX_FLAGS = ["-O2", "-std=c++17", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
+def build(src: str = _SRC, out: str = _LIB, extra: Sequence[str] = ()) -> str:
+    """Compile the C++ oracle into a shared library (plain g++)."""
+    cmd = ["g++", *GXX_FLAGS, *extra, src, "-o", out]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _bind(lib):
+    f = ctypes.POINTER(ctypes.c_float)
+    i64 = ctypes.POINTER(ctypes.c_int64)
+    i32 = ctypes.POINTER(ctypes.c_int32)
+    lib.pv_oracle_grid.argtypes = [f, f, i64]
+    lib.pv_oracle_grid.restype = ctypes.c_int
+    lib.pv_oracle_bin_point.argtypes = [f, f, f, i64, i64]
+    lib.pv_oracle_bin_point.restype = ctypes.c_int
+    lib.pv_oracle_voxelize.argtypes = [
+        f, ctypes.c_int64, f, f, ctypes.c_int, ctypes.c_int, f, i32, i32, i32,
+    ]
+    lib.pv_oracle_voxelize.restype = ctypes.c_int
+    return lib
+
+
+def load_path(path: str):
+    """Load an already compiled oracle library (e.g. a test's mutant)."""
+    return _bind(ctypes.CDLL(path))
+
+
+def load():
+    """Load the oracle library, compiling it first if it is missing or stale."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+                build()
+            _lib = load_path(_LIB)
+        return _lib
+
+
+def _fptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def _f32(seq) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(seq, dtype=np.float32))
+
+
+def grid(pc_range, voxel_size, lib=None) -> Tuple[int, Tuple[int, int, int]]:
+    """(status, (gx, gy, gz)) from the C++ oracle."""
+    lib = lib or load()
+    r, v = _f32(pc_range), _f32(voxel_size)
+    g = np.zeros(3, dtype=np.int64)
+    st = lib.pv_oracle_grid(_fptr(r), _fptr(v), g.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+    return st, tuple(int(x) for x in g)
+
+
+def bin_point(p, pc_range, voxel_size, lib=None):
+    """(cx, cy, cz) of one point, or None if it is dropped."""
+    lib = lib or load()
+    st, g = grid(pc_range, voxel_size, lib)
+    assert st == OK, st
+    pp, r, v = _f32(p), _f32(pc_range), _f32(voxel_size)
+    gg = np.array(g, dtype=np.int64)
+    cell = np.zeros(3, dtype=np.int64)
+    ok = lib.pv_oracle_bin_point(
+        _fptr(pp), _fptr(r), _fptr(v),
+        gg.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+        cell.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+    )
+    return tuple(int(c) for c in cell) if ok else None
+
+
+def voxelize(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int, lib=None):
+    """The C++ oracle.  Returns (status, voxels, coords, counts, V).
+
+    ``voxels`` is [max_voxels, max_points, 4] float32, ``coords`` [max_voxels, 3]
+    int32, ``counts`` [max_voxels] int32; all padded with zeros past V.
+    """
+    lib = lib or load()
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    r, v = _f32(pc_range), _f32(voxel_size)
+    vox = np.empty((max(max_voxels, 0), max(max_points, 0), 4), dtype=np.float32)
+    coords = np.empty((max(max_voxels, 0), 3), dtype=np.int32)
+    counts = np.empty((max(max_voxels, 0),), dtype=np.int32)
+    num = np.zeros(1, dtype=np.int32)
+    i32 = ctypes.POINTER(ctypes.c_int32)
+    st = lib.pv_oracle_voxelize(
+        _fptr(pts) if pts.size else None, pts.shape[0], _fptr(r), _fptr(v),
+        int(max_points), int(max_voxels), _fptr(vox),
+        coords.ctypes.data_as(i32), counts.ctypes.data_as(i32), num.ctypes.data_as(i32),
+    )
+    return st, vox, coords, counts, int(num[0])
+
+
+# --------------------------------------------------------------------------
+# NumPy restatement (stable sort), independent of the C++ pass.
+# --------------------------------------------------------------------------
+
+def grid_py(pc_range, voxel_size) -> Tuple[int, int, int]:
+    """Grid extents: (max - min) / size in double, rounded half away from zero."""
+    out = []
+    for a in range(3):
+        lo = float(np.float32(pc_range[a]))
+        hi = float(np.float32(pc_range[a + 3]))
+        v = float(np.float32(voxel_size[a]))
+        q = (hi - lo) / v
+        fl = math.floor(q)
+        out.append(int(fl + (1 if q - fl >= 0.5 else 0)))
+    return tuple(out)
+
+
+def bin_numpy(points: np.ndarray, pc_range, voxel_size):
+    """Per-point (valid mask, cx, cy) with float32 NumPy arithmetic."""
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    g = grid_py(pc_range, voxel_size)
+    lo = np.asarray(pc_range[:3], dtype=np.float32)
+    v = np.asarray(voxel_size, dtype=np.float32)
+    bits = pts.view(np.uint32)[:, :3]
+    finite = np.all((bits & np.uint32(0x7F800000)) != np.uint32(0x7F800000), axis=1)
+    with np.errstate(all="ignore"):
+        q = np.floor((pts[:, :3] - lo) / v)  # float32 subtract, divide, floor
+    gf = np.asarray(g, dtype=np.float32)
+    ok = finite & np.all(q >= np.float32(0), axis=1) & np.all(q < gf, axis=1)
+    cx = np.where(ok, q[:, 0], 0).astype(np.int64)
+    cy = np.where(ok, q[:, 1], 0).astype(np.int64)
+    return ok, cx, cy, g
+
+
+def voxelize_numpy(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int):
+    """Vectorised restatement.  Returns (voxels, coords, counts, V)."""
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    ok, cx, cy, g = bin_numpy(pts, pc_range, voxel_size)
+    vox = np.zeros((max_voxels, max_points, 4), dtype=np.float32)
+    coords = np.zeros((max_voxels, 3), dtype=np.int32)
+    counts = np.zeros((max_voxels,), dtype=np.int32)
+    idx = np.flatnonzero(ok)
+    if idx.size == 0:
+        return vox, coords, counts, 0
+    key = cy[idx] * g[0] + cx[idx]
+    uniq, first_pos, inverse = np.unique(key, return_index=True, return_inverse=True)
+    first_idx = idx[first_pos]
+    order = np.argsort(first_idx, kind="stable")       # pillars by first point
+    rank_of_uniq = np.empty_like(order)
+    rank_of_uniq[order] = np.arange(order.size)
+    rank = rank_of_uniq[inverse.reshape(-1)]            # per valid point
+    s = np.argsort(rank, kind="stable")                 # index order inside a pillar
+    r_sorted = rank[s]
+    start = np.searchsorted(r_sorted, r_sorted, side="left")
+    pos = np.empty_like(s)
+    pos[s] = np.arange(s.size) - start
+    keep = (rank < max_voxels) & (pos < max_points)
+    vox.view(np.uint32)[rank[keep], pos[keep]] = pts.view(np.uint32)[idx[keep]]
+    V = int(min(uniq.size, max_voxels))
+    counts[:V] = np.minimum(np.bincount(rank, minlength=uniq.size)[:V], max_points)
+    kept_keys = uniq[order[:V]]
+    coords[:V, 1] = kept_keys // g[0]
+    coords[:V, 2] = kept_keys % g[0]
+    return vox, coords, counts, V
+
+
+# --------------------------------------------------------------------------
+# O(N^2) brute force from the definition, plain Python loops (tiny N only).
+# --------------------------------------------------------------------------
+
+def voxelize_bruteforce(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int):
+    """Definition written out point by point.  Returns (voxels, coords, counts, V)."""
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    g = grid_py(pc_range, voxel_size)
+    lo = [np.float32(pc_range[a]) for a in range(3)]
+    vs = [np.float32(voxel_size[a]) for a in range(3)]
+    n = pts.shape[0]
+    keys = []
+    with np.errstate(all="ignore"):
+        for i in range(n):
+            p = pts[i]
+            key = None
+            if all(math.isfinite(float(p[a])) for a in range(3)):
+                cells = []
+                for a in range(3):
+                    q = np.floor(np.float32(p[a] - lo[a]) / vs[a])
+                    if q >= np.float32(0) and q < np.float32(g[a]):
+                        cells.append(int(q))
+                    else:
+                        break
+                if len(cells) == 3:
+                    key = cells[1] * g[0] + cells[0]
+            keys.append(key)
+    first = {}
+    for i, k in enumerate(keys):
+        if k is not None and k not in first:
+            first[k] = i
+    vox = np.zeros((max_voxels, max_points, 4), dtype=np.float32)
+    coords = np.zeros((max_voxels, 3), dtype=np.int32)
+    counts = np.zeros((max_voxels,), dtype=np.int32)
+    firsts = list(first.values())
+    for i, k in enumerate(keys):
+        if k is None:
+            continue
+        rank = sum(1 for f in firsts if f < first[k])
+        pos = sum(1 for j in range(i) if keys[j] == k)
+        if rank < max_voxels and pos < max_points:
+            vox.view(np.uint32)[rank, pos] = pts.view(np.uint32)[i]
+            counts[rank] += 1
+            coords[rank] = (0, k // g[0], k % g[0])
+    V = min(len(first), max_voxels)
+    return vox, coords, counts, V
