@@ -1,0 +1,355 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 pillar voxelizer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload kitti|dense|adversarial|tiny|uniform_<n>]
+
+One step = one voxelization of one synthetic frame (the whole hot path: bin,
+group, rank, emit, zero-fill) through the C ABI.  The default workload is the
+KITTI-shaped 122,880-return frame (432 x 496 grid, 32 points per pillar,
+16,000 pillars).  Inputs are resident in HBM before timing starts; the frame
+buffers (input + all outputs) rotate over a set larger than twice the L2, so
+every step reads and writes memory that is not in L2.  Times come from CUDA
+events on the launching stream; with torchrun (N > 1) every rank voxelizes
+its own frames (replicas, no collective on the data path) and the maximum
+time over ranks is reported.
+
+--impl reference times the CPU oracle (single-threaded C++) on the host on
+the same workload, one frame per step.
+
+Prints ONE JSON line (rank 0).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Mpoints/s voxelized per frame; achieved HBM GB/s vs GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="kitti")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample length")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def algorithmic_bytes(n, max_points, max_voxels):
+    # Input read once (16 B/point) + every output byte written once:
+    # voxels 16*K B, coords 12 B, counts 4 B per pillar row, plus V (4 B).
+    return 16 * n + max_voxels * (16 * max_points + 16) + 4
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha():
+    src = os.path.join(ROOT, "lidar_point_cloud_gb300", "csrc", "pv_voxelize.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    describes the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"pv_voxelize_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_sha():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+
+        fd, self.path = tempfile.mkstemp(prefix="pv_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        os.unlink(self.path)
+        busy = [r for r in rows if r[4].isdigit() and int(r[4]) > 0] or rows
+        sm = [float(r[1]) for r in busy if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in busy if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(busy)}
+
+
+def cpu_oracle_rate(pts, P, seconds):
+    """Single-threaded C++ oracle on the host: (Mpoints/s, frames, seconds)."""
+    import oracle
+
+    lib = oracle.load()
+    n = pts.shape[0]
+    oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib)  # warm
+    frames, t0 = 0, time.perf_counter()
+    while True:
+        oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib)
+        frames += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or frames >= 100000:
+            break
+    return n * frames / el / 1e6, frames, el
+
+
+def run_reference(args, rank, world):
+    from lidar_point_cloud_gb300 import synth
+
+    if rank != 0:
+        return
+    pts, P = synth.make(args.workload)
+    import oracle
+
+    lib = oracle.load()
+    for _ in range(args.warmup):
+        oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib)
+    el = time.perf_counter() - t0
+    n = pts.shape[0]
+    value = n * args.steps / el / 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "Mpoints/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {synth.WORKLOADS[args.workload]}", "N": n,
+                   "max_points": P.max_points, "max_voxels": P.max_voxels},
+        "cpu_baseline": {"value": round(value, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
+                         "sample": f"one full frame per step, {args.steps} steps, single-threaded C++ std::map oracle"},
+        "e2e": {"value": round(value, 3), "unit": "Mpoints/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gb300(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import lidar_point_cloud_gb300 as pv
+    from lidar_point_cloud_gb300 import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pts, P = synth.make(args.workload)
+    n, K, M = pts.shape[0], P.max_points, P.max_voxels
+    plan = pv.query_plan(n, P.point_cloud_range, P.voxel_size, K, M)
+    bytes_launch = algorithmic_bytes(n, K, M)
+    frame_bytes = 16 * n + M * (16 * K + 16) + 4
+    R = max(2, -(-2 * L2_BYTES // frame_bytes))
+    src = torch.from_numpy(pts).to(dev)
+    inputs = [src.clone() for _ in range(R)]
+    outs = [pv.alloc_outputs(K, M, dev) for _ in range(R)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(k):
+        pv.voxelize_into(inputs[k % R], P.point_cloud_range, P.voxel_size, K, M, outs[k % R], stream=stream)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize(dev)
+    # Correctness guard on the last warm-up output (cheap: V only).
+    v_dev = int(outs[(args.warmup - 1) % R][3].item()) if args.warmup else 0
+    if v_dev < 0:
+        raise RuntimeError(f"device status {v_dev}")
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    region0.record(stream)
+    for k in range(args.steps):
+        starts[k].record(stream)
+        step(args.warmup + k)
+        ends[k].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    region_ms = region0.elapsed_time(region1)
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # Keep the GPU busy (untimed) so the clock sampler sees at least ~1.5 s of load.
+    t_soak = time.perf_counter()
+    k = 0
+    while sampler and time.perf_counter() - t_soak < 1.5:
+        step(k)
+        k += 1
+        if k % 256 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+
+    if dist:
+        t = torch.tensor([region_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        region_ms = float(t.item())
+    # Result check after timing: the last timed output against the first.
+    last = outs[(args.warmup + args.steps - 1) % R]
+    V = int(last[3].item())
+
+    if rank != 0:
+        return
+    value = world * n * args.steps / (region_ms * 1e-3) / 1e6
+    avg_kernel_s = statistics.mean(kernel_ms) * 1e-3
+    peak, peak_src = measured_peak()
+    achieved = bytes_launch / avg_kernel_s / 1e9
+
+    # End to end through the C ABI with host buffers (pinned), rank 0 only.
+    pin_pts = torch.from_numpy(pts).pin_memory().numpy()
+    host_out = (torch.empty((M, K, 4), dtype=torch.float32).pin_memory().numpy(),
+                torch.empty((M, 3), dtype=torch.int32).pin_memory().numpy(),
+                torch.empty((M,), dtype=torch.int32).pin_memory().numpy(),
+                torch.empty((1,), dtype=torch.int32).pin_memory().numpy())
+    for _ in range(5):
+        pv.voxelize_host(pin_pts, P.point_cloud_range, P.voxel_size, K, M, out=host_out, stream=stream)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        pv.voxelize_host(pin_pts, P.point_cloud_range, P.voxel_size, K, M, out=host_out, stream=stream)
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": round(n * args.e2e_steps / e2e_s / 1e6, 3), "unit": "Mpoints/s",
+           "h2d_bytes_per_step": 16 * n, "d2h_bytes_per_step": M * (16 * K + 16) + 4,
+           "api": "pv_voxelize_host (C ABI, pinned host buffers, synchronous)", "steps": args.e2e_steps}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, frames, el = cpu_oracle_rate(pts, P, args.cpu_seconds)
+        cpu = {"value": round(rate, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
+               "sample": f"{frames} repetitions of the full frame ({el:.1f} s), single-threaded C++ std::map oracle"}
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "Mpoints/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(region_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: {synth.WORKLOADS[args.workload]}",
+            "N": n, "V": V, "grid": list(plan["grid"]), "max_points": K, "max_voxels": M,
+            "table": f"{plan['table_mode']}, {plan['table_slots']} slots",
+            "launch": f"1 cooperative kernel per step, {plan['ctas']} blocks x {plan['threads']} threads",
+            "l2": f"inputs+outputs rotate over {R} frame buffers ({R * frame_bytes / 2**20:.0f} MiB > 2x L2)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
+            "peak_source": f"{peak_src} (hbm_gbs)", "kernel": "pv_voxelize_kernel",
+            "bytes_per_launch": bytes_launch, "avg_launch_us": round(avg_kernel_s * 1e6, 3),
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_gb300(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * pv.h - C ABI of the GB300 pillar voxelizer (libpv.so).
+ *
+ * The operation is the one described on the page "Voxelize"
+ * (ethan-howes.github.io/projects/voxelize/): an unordered [N, 4] float32
+ * LiDAR cloud (x, y, z, intensity) becomes the three PointPillars tensors,
+ * a [V, max_points, 4] stack of per-pillar points, [V, 3] int32 pillar
+ * coordinates (z = 0, y, x) and [V] int32 per-pillar point counts.
+ *
+ * Semantics, section by section of that page:
+ *   "Implementation > Binning a point": a point is dropped if x, y or z is
+ *     NaN or +-Inf; its cell on each axis is floorf((c - c_min) / v_c), with
+ *     the subtraction and the division each one IEEE binary32 operation
+ *     rounded to nearest (no fast-math, no flush of subnormals); a point is
+ *     dropped unless 0 <= cell < grid on every axis (a strict < on the upper
+ *     bound, so a point exactly on x_max is excluded; z outside the slab is
+ *     dropped the same way).  The pillar id is cy * grid_x + cx.
+ *   "Claiming a pillar and packing points": one pillar per distinct id, with
+ *     coordinates (0, id / grid_x, id % grid_x); at most max_points points
+ *     per pillar ("keep the first K"); the intensity is copied bit for bit.
+ *   "Compaction" and "The PyTorch side": pillars are compacted into dense
+ *     outputs pre-allocated at max_voxels rows; V is the real pillar count.
+ *   Order (the page's hash-slot order varies from run to run, "Results";
+ *     this library fixes it): pillars in ascending order of their
+ *     lowest-index valid point, points inside a pillar in index order, the
+ *     first max_points points of each pillar and the first max_voxels pillars
+ *     kept.  Every output byte is written: rows past a pillar's count and
+ *     pillars past V are zero.  The result is therefore unique and
+ *     bit-reproducible.
+ *
+ * Grid extents: grid_c = round((max_c - min_c) / v_c), computed in double
+ * and rounded half away from zero (432 x 496 for the page's 0.16 m cells over
+ * [0, 69.12] x [-39.68, 39.68], "Fig. 2").  Only pillar grids (grid_z == 1)
+ * are supported; each of grid_x, grid_y must be <= 2^24 and
+ * grid_x * grid_y < 2^31.
+ *
+ * Errors: a status found on the host is returned and nothing is enqueued;
+ * *out_num_voxels is then left untouched.  A status found on the device is
+ * written, negative, into *out_num_voxels in place of V; the other outputs
+ * are then unspecified.
+ */
+#ifndef PV_H_
+#define PV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* pv_stream_t;
+
+typedef enum pv_status {
+  PV_OK = 0,
+  PV_ERR_INVALID = -1,     /* bad argument: null/misaligned pointer, host pointer where a
+                              device pointer is needed, non-finite or non-positive cell
+                              size, max <= min, size out of range */
+  PV_ERR_UNSUPPORTED = -2, /* grid_z != 1 (true 3-D voxels are not built) */
+  PV_ERR_ALLOC = -3,       /* the library's device workspace could not be allocated */
+  PV_ERR_CUDA = -4,        /* a CUDA runtime call failed (launch, copy, ...) */
+  PV_ERR_CAPACITY = -5,    /* device: the pillar table ran out of slots (only with a
+                              forced undersized table, see pv_options) */
+  PV_ERR_TIMEOUT = -6,     /* device: a bounded wait inside the kernel gave up (about
+                              one second); the workspace is then fully reset by the
+                              next call on the same stream */
+  PV_ERR_INTERNAL = -7     /* device: a consistency check failed (a point index read
+                              from the pillar table was out of range); the workspace is
+                              fully reset by the next call on the same stream */
+} pv_status;
+
+/* Largest max_points accepted. */
+#define PV_MAX_POINTS_LIMIT 1024
+
+/*
+ * pv_voxelize - voxelize one cloud, asynchronously on `stream`.
+ *
+ *   points          device, [num_points, 4] float32 row-major (x, y, z, intensity),
+ *                   16-byte aligned; may be NULL when num_points == 0.  Read only.
+ *   num_points      0 <= num_points < 2^31 - 1.
+ *   point_cloud_range  host, {x_min, y_min, z_min, x_max, y_max, z_max}.
+ *   voxel_size      host, {v_x, v_y, v_z}, finite and > 0.
+ *   max_points      points kept per pillar, 1..PV_MAX_POINTS_LIMIT (PointPillars: 32).
+ *   max_voxels      pillars kept, >= 1, max_voxels * max_points < 2^31.
+ *   out_voxels      device, [max_voxels, max_points, 4] float32, 16-byte aligned.
+ *   out_coords      device, [max_voxels, 3] int32, (z = 0, y, x).
+ *   out_counts      device, [max_voxels] int32.
+ *   out_num_voxels  device, one int32: V (>= 0) or a negative pv_status.
+ *   stream          CUDA stream the work is enqueued on.
+ *
+ * All pointers belong to the caller and must be device memory of one device;
+ * the call runs on that device.  Outputs are fully overwritten.  The call
+ * does not synchronize: V is read back by the caller when it needs it.
+ * The library keeps a grow-only workspace per (device, stream); calls on one
+ * stream run one after another, calls on different streams do not share
+ * state.  A call that grows the workspace synchronizes the stream once.
+ * Returns PV_OK or a negative pv_status found on the host.
+ */
+int pv_voxelize(const float* points, int64_t num_points, const float point_cloud_range[6],
+                const float voxel_size[3], int max_points, int max_voxels, float* out_voxels,
+                int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels,
+                pv_stream_t stream);
+
+/*
+ * Tuning and test knobs for pv_voxelize_ex.  Zero in any field means "use the
+ * library's choice".  The result never depends on these settings.
+ *   table_mode   0 auto, 1 direct (one slot per grid cell), 2 hashed (open
+ *                addressing, linear probing).
+ *   table_log2   hashed mode only: force 2^table_log2 slots.  A table smaller
+ *                than the number of distinct pillars makes the call fail with
+ *                PV_ERR_CAPACITY (used by the tests of that error path).
+ *   ctas_per_sm  resident blocks per SM of the single cooperative launch
+ *                (capped at what fits).
+ */
+typedef struct pv_options {
+  int table_mode;
+  int table_log2;
+  int ctas_per_sm;
+  int reserved[5];
+} pv_options;
+
+int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cloud_range[6],
+                   const float voxel_size[3], int max_points, int max_voxels, float* out_voxels,
+                   int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels,
+                   const pv_options* options, pv_stream_t stream);
+
+/*
+ * pv_voxelize_host - the same operation on HOST buffers, synchronous.
+ *
+ * Copies points_host to the device, runs pv_voxelize on `stream`, copies all
+ * four outputs back (the full padded [max_voxels, ...] buffers) and waits for
+ * the stream.  Host buffers may be pageable; pinned buffers copy faster.
+ * The device copies live in the library's per-(device, stream) workspace.
+ * Returns PV_OK, a host-side error, or the negative status the device wrote
+ * (then *out_num_voxels_host holds it too).
+ */
+int pv_voxelize_host(const float* points_host, int64_t num_points, const float point_cloud_range[6],
+                     const float voxel_size[3], int max_points, int max_voxels,
+                     float* out_voxels_host, int32_t* out_coords_host, int32_t* out_counts_host,
+                     int32_t* out_num_voxels_host, pv_stream_t stream);
+
+/* Grid extents for a range and a cell size: PV_OK, PV_ERR_INVALID or
+ * PV_ERR_UNSUPPORTED, with grid_out = {grid_x, grid_y, grid_z}. */
+int pv_grid_size(const float point_cloud_range[6], const float voxel_size[3], int64_t grid_out[3]);
+
+/* What pv_voxelize would launch for these sizes on the current device. */
+typedef struct pv_plan {
+  int64_t grid[3];          /* pillar grid extents */
+  int table_mode;           /* 1 direct, 2 hashed */
+  int64_t table_slots;      /* pillar slots in the table */
+  int list_stride;          /* uint32 entries per slot (max_points rounded up to 4) */
+  int ctas;                 /* blocks of the cooperative launch */
+  int threads;              /* threads per block */
+  int64_t points_per_cta;   /* contiguous points each block owns */
+  int64_t workspace_bytes;  /* device workspace the call needs */
+} pv_plan;
+
+int pv_query_plan(int64_t num_points, const float point_cloud_range[6], const float voxel_size[3],
+                  int max_points, int max_voxels, const pv_options* options, pv_plan* plan_out);
+
+/* Frees every cached workspace of every device and stream (waits for them
+ * to be idle first).  Returns PV_OK or PV_ERR_CUDA. */
+int pv_release_workspace(void);
+
+/* Static, human-readable name of a status. */
+const char* pv_status_string(int status);
+
+/* Library version, "major.minor.patch". */
+const char* pv_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* PV_H_ */

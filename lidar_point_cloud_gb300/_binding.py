@@ -1,0 +1,242 @@
+"""ctypes binding of libpv.so: argument marshalling only.
+
+Every step of the voxelization runs in the library's CUDA kernel; this file
+checks dtypes, devices and shapes the way the page "Voxelize" describes its
+C++ wrapper ("The PyTorch side": TORCH_CHECK of dtype, contiguity and device,
+then raw pointers), pre-allocates the outputs, and slices them to the real
+pillar count V.  There is no CPU fallback: without the compiled library, or
+without a GPU, the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+from . import _build
+
+STATUS = {
+    0: "PV_OK",
+    -1: "PV_ERR_INVALID",
+    -2: "PV_ERR_UNSUPPORTED",
+    -3: "PV_ERR_ALLOC",
+    -4: "PV_ERR_CUDA",
+    -5: "PV_ERR_CAPACITY",
+    -6: "PV_ERR_TIMEOUT",
+    -7: "PV_ERR_INTERNAL",
+}
+
+EXPORTS = (
+    "pv_voxelize", "pv_voxelize_ex", "pv_voxelize_host", "pv_grid_size", "pv_query_plan",
+    "pv_release_workspace", "pv_status_string", "pv_version",
+)
+
+
+class PVError(RuntimeError):
+    """A negative status returned by the library."""
+
+    def __init__(self, status: int, where: str = ""):
+        self.status = int(status)
+        name = STATUS.get(self.status, f"status {self.status}")
+        super().__init__(f"{where}: {name}" if where else name)
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("table_mode", ctypes.c_int), ("table_log2", ctypes.c_int),
+                ("ctas_per_sm", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int64 * 3), ("table_mode", ctypes.c_int),
+                ("table_slots", ctypes.c_int64), ("list_stride", ctypes.c_int),
+                ("ctas", ctypes.c_int), ("threads", ctypes.c_int),
+                ("points_per_cta", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None):
+    """Load libpv.so.  Raises if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"CUDA library {p} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"`")
+        lib = ctypes.CDLL(p)
+        f = ctypes.POINTER(ctypes.c_float)
+        vp = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        ci = ctypes.c_int
+        dev_args = [vp, i64, f, f, ci, ci, vp, vp, vp, vp]
+        lib.pv_voxelize.argtypes = dev_args + [vp]
+        lib.pv_voxelize.restype = ci
+        lib.pv_voxelize_ex.argtypes = dev_args + [ctypes.POINTER(Options), vp]
+        lib.pv_voxelize_ex.restype = ci
+        lib.pv_voxelize_host.argtypes = dev_args + [vp]
+        lib.pv_voxelize_host.restype = ci
+        lib.pv_grid_size.argtypes = [f, f, ctypes.POINTER(ctypes.c_int64)]
+        lib.pv_grid_size.restype = ci
+        lib.pv_query_plan.argtypes = [i64, f, f, ci, ci, ctypes.POINTER(Options), ctypes.POINTER(Plan)]
+        lib.pv_query_plan.restype = ci
+        lib.pv_release_workspace.argtypes = []
+        lib.pv_release_workspace.restype = ci
+        lib.pv_status_string.argtypes = [ci]
+        lib.pv_status_string.restype = ctypes.c_char_p
+        lib.pv_version.argtypes = []
+        lib.pv_version.restype = ctypes.c_char_p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _f6(seq: Sequence[float], n: int):
+    vals = [float(x) for x in seq]
+    if len(vals) != n:
+        raise ValueError(f"expected {n} values, got {len(vals)}")
+    return (ctypes.c_float * n)(*vals)
+
+
+def _options(table_mode=0, table_log2=0, ctas_per_sm=0) -> Options:
+    o = Options()
+    o.table_mode, o.table_log2, o.ctas_per_sm = int(table_mode), int(table_log2), int(ctas_per_sm)
+    return o
+
+
+def grid_size(point_cloud_range, voxel_size) -> Tuple[int, int, int]:
+    g = (ctypes.c_int64 * 3)()
+    st = load().pv_grid_size(_f6(point_cloud_range, 6), _f6(voxel_size, 3), g)
+    if st != 0:
+        raise PVError(st, "pv_grid_size")
+    return tuple(int(x) for x in g)
+
+
+def query_plan(num_points, point_cloud_range, voxel_size, max_points=32, max_voxels=16000, **opts) -> dict:
+    p = Plan()
+    o = _options(**opts)
+    st = load().pv_query_plan(int(num_points), _f6(point_cloud_range, 6), _f6(voxel_size, 3),
+                              int(max_points), int(max_voxels), ctypes.byref(o), ctypes.byref(p))
+    if st != 0:
+        raise PVError(st, "pv_query_plan")
+    return {"grid": tuple(p.grid), "table_mode": {1: "direct", 2: "hashed"}[p.table_mode],
+            "table_slots": p.table_slots, "list_stride": p.list_stride, "ctas": p.ctas,
+            "threads": p.threads, "points_per_cta": p.points_per_cta,
+            "workspace_bytes": p.workspace_bytes}
+
+
+def release_workspace() -> None:
+    st = load().pv_release_workspace()
+    if st != 0:
+        raise PVError(st, "pv_release_workspace")
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def alloc_outputs(max_points: int, max_voxels: int, device):
+    torch = _torch()
+    vox = torch.empty((max_voxels, max_points, 4), dtype=torch.float32, device=device)
+    coords = torch.empty((max_voxels, 3), dtype=torch.int32, device=device)
+    counts = torch.empty((max_voxels,), dtype=torch.int32, device=device)
+    num = torch.empty((1,), dtype=torch.int32, device=device)
+    return vox, coords, counts, num
+
+
+def voxelize_into(points, point_cloud_range, voxel_size, max_points: int, max_voxels: int,
+                  out, stream=None, table_mode: int = 0, table_log2: int = 0, ctas_per_sm: int = 0) -> None:
+    """Enqueue one voxelization into pre-allocated outputs (no synchronization).
+
+    ``out`` = (voxels [M, K, 4] f32, coords [M, 3] i32, counts [M] i32, num [1] i32),
+    all CUDA tensors on the points' device.  ``num`` receives V or a negative
+    status once the stream reaches the kernel.
+    """
+    torch = _torch()
+    vox, coords, counts, num = out
+    if not isinstance(points, torch.Tensor) or points.dtype != torch.float32:
+        raise TypeError("points must be a float32 torch.Tensor")
+    if points.dim() != 2 or points.shape[1] != 4:
+        raise ValueError("points must have shape [N, 4]")
+    if not points.is_cuda:
+        raise ValueError("points must be a CUDA tensor (use voxelize_host for host arrays)")
+    if not points.is_contiguous():
+        raise ValueError("points must be contiguous")
+    for t, dt, shape in ((vox, torch.float32, (max_voxels, max_points, 4)),
+                         (coords, torch.int32, (max_voxels, 3)),
+                         (counts, torch.int32, (max_voxels,)), (num, torch.int32, (1,))):
+        if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous() or t.device != points.device:
+            raise ValueError("output tensor has the wrong dtype, shape, layout or device")
+    if stream is None:
+        stream = torch.cuda.current_stream(points.device)
+    handle = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    lib = load()
+    args = (ctypes.c_void_p(points.data_ptr() if points.shape[0] else 0), int(points.shape[0]),
+            _f6(point_cloud_range, 6), _f6(voxel_size, 3), int(max_points), int(max_voxels),
+            ctypes.c_void_p(vox.data_ptr()), ctypes.c_void_p(coords.data_ptr()),
+            ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(num.data_ptr()))
+    if table_mode or table_log2 or ctas_per_sm:
+        o = _options(table_mode, table_log2, ctas_per_sm)
+        st = lib.pv_voxelize_ex(*args, ctypes.byref(o), handle)
+    else:
+        st = lib.pv_voxelize(*args, handle)
+    if st != 0:
+        raise PVError(st, "pv_voxelize")
+
+
+def voxelize(points, point_cloud_range, voxel_size, max_points: int = 32, max_voxels: int = 16000,
+             stream=None, **opts):
+    """Voxelize one cloud on its GPU.  Returns (voxels [V,K,4], coords [V,3], counts [V]).
+
+    Mirrors the page's Python entry point: outputs are pre-allocated at
+    max_voxels rows, the call runs without autograd, and the results are
+    sliced to the real pillar count (which costs one 4-byte device read).
+    """
+    torch = _torch()
+    with torch.no_grad():
+        out = alloc_outputs(max_points, max_voxels, points.device)
+        voxelize_into(points, point_cloud_range, voxel_size, max_points, max_voxels, out, stream, **opts)
+        V = int(out[3].item())
+        if V < 0:
+            raise PVError(V, "pv_voxelize (device)")
+        return out[0][:V], out[1][:V], out[2][:V]
+
+
+def voxelize_host(points, point_cloud_range, voxel_size, max_points: int = 32, max_voxels: int = 16000,
+                  out=None, stream=None):
+    """Voxelize a host (NumPy or CPU torch) cloud through pv_voxelize_host.
+
+    Copies in, runs on the current CUDA device, copies the padded outputs
+    back into ``out`` (NumPy arrays; allocated if None) and returns
+    (voxels [M,K,4], coords [M,3], counts [M], V).
+    """
+    import numpy as np
+
+    pts = np.ascontiguousarray(np.asarray(points, dtype=np.float32)).reshape(-1, 4)
+    if out is None:
+        out = (np.empty((max_voxels, max_points, 4), np.float32), np.empty((max_voxels, 3), np.int32),
+               np.empty((max_voxels,), np.int32), np.empty((1,), np.int32))
+    vox, coords, counts, num = out
+    for a in out:
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("output arrays must be C-contiguous")
+    handle = ctypes.c_void_p(0 if stream is None else (stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)))
+    st = load().pv_voxelize_host(
+        ctypes.c_void_p(pts.ctypes.data if pts.shape[0] else 0), int(pts.shape[0]),
+        _f6(point_cloud_range, 6), _f6(voxel_size, 3), int(max_points), int(max_voxels),
+        ctypes.c_void_p(vox.ctypes.data), ctypes.c_void_p(coords.ctypes.data),
+        ctypes.c_void_p(counts.ctypes.data), ctypes.c_void_p(num.ctypes.data), handle)
+    if st != 0:
+        raise PVError(st, "pv_voxelize_host")
+    return vox, coords, counts, int(num[0])

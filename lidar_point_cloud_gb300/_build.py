@@ -1,0 +1,56 @@
+"""Compile libpv.so (the CUDA library) in-tree with nvcc for sm_103a."""
+
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+SRC = os.path.join(PKG, "csrc", "pv_voxelize.cu")
+INCLUDE = os.path.join(ROOT, "include")
+LIB = os.path.join(PKG, "libpv.so")
+
+# IEEE binary32 semantics are part of the contract: no fast-math, no flush of
+# subnormals, correctly rounded division, no multiply-add contraction.
+NVCC_FLAGS = [
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-O3", "-lineinfo", "-std=c++17",
+    "-ftz=false", "-prec-div=true", "-prec-sqrt=true", "-fmad=false",
+    "-Xcompiler", "-fPIC", "-shared",
+]
+
+
+def nvcc_path() -> str:
+    for cand in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if cand and os.path.exists(os.path.join(cand, "bin", "nvcc")):
+            return os.path.join(cand, "bin", "nvcc")
+    found = shutil.which("nvcc")
+    if not found:
+        raise RuntimeError("nvcc not found: set CUDA_HOME")
+    return found
+
+
+def sources():
+    return [SRC, os.path.join(INCLUDE, "pv.h")]
+
+
+def is_stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
+        return True
+    t = os.path.getmtime(lib)
+    return any(os.path.getmtime(s) > t for s in sources())
+
+
+def build(out: str = LIB, extra=(), verbose: bool = False) -> str:
+    """Compile the library; returns its path."""
+    tmp = out + ".tmp"
+    cmd = [nvcc_path(), *NVCC_FLAGS, *extra, "-I", INCLUDE, SRC, "-o", tmp]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
+    if verbose:
+        print(res.stdout + res.stderr)
+    os.replace(tmp, out)
+    return out

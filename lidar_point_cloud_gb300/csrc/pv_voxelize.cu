@@ -1,0 +1,1222 @@
+// GB300 (sm_103a) pillar voxelizer: kernels and the C ABI declared in pv.h.
+//
+// What is computed is the page "Voxelize" (ethan-howes.github.io/projects/
+// voxelize/): bin every point into a pillar ("Implementation > Binning a
+// point"), group points that share a pillar ("Claiming a pillar and packing
+// points"), compact the pillars into dense outputs ("Compaction"), with the
+// canonical order stated in pv.h.  How it is computed differs from the
+// page's one-thread-per-point kernel + Thrust copy_if + gather:
+//
+//   * one cooperative launch, one 1024-thread block per SM, all resident,
+//     and two grid-wide barriers;
+//   * phase 1 (before the first barrier): blocks sweep the cloud in tiles of
+//     1024 consecutive points, in index order across the grid.  Each point is
+//     read with one 16-byte load and binned with IEEE round-to-nearest
+//     subtract/divide and floorf.  In shared memory the tile is grouped by
+//     pillar (warp match + a small open-addressing map), which gives every
+//     point its rank among the tile's points of its pillar and lays the tile
+//     out group by group in a per-tile buffer.  Only each group's first point
+//     (its leader) touches the pillar's slot in an L2-resident table: the
+//     slot keeps the max_points smallest leader indices with atomicMin (entry
+//     k keeps the minimum of what reaches it and passes the larger value on,
+//     so it ends as the (k+1)-th smallest whatever order the inserts came
+//     in).  Entry 0 is the pillar's first point (the page's atomicCAS claim
+//     plus an atomicMin of the first index), and the pillar's points in index
+//     order are its groups concatenated in entry order.  The table is
+//     direct-mapped (one slot per grid cell) when the grid is small enough,
+//     else open addressing with linear probing (the page's hash table, "A
+//     hash table instead of a sort"), probes bounded by the table size;
+//   * phase 2: each block owns a contiguous range of point indices.  A point
+//     is the first of its pillar iff its index sits in entry 0 of its slot.
+//     Blocks compact their first points in index order and publish the
+//     count; after the second barrier every block scans all counts into
+//     shared memory, so every pillar's rank (its order of first appearance)
+//     is known everywhere.  All warps share the output rows: rank r finds
+//     its owner block by binary search in the prefix, reads its groups,
+//     gathers the first max_points points (16-byte rows) and writes the row
+//     stack, coordinates and count; the slots of pillars past the budget are
+//     emptied; rows past V are zero-filled.
+//
+// The table cleans itself: every slot a call fills is emptied by the same
+// call, so no memset runs per call.  A launch that fails on the device marks
+// the table dirty and the next launch resets it whole first.  Every wait is
+// bounded by the global timer (about 1 s), after which the kernel records
+// PV_ERR_TIMEOUT and returns.
+
+#include "pv.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <utility>
+
+namespace {
+
+constexpr uint32_t kEmpty = 0xFFFFFFFFu;   // empty list entry (also an all-0xFF memset)
+constexpr int32_t kNoKey = -1;             // empty hashed slot
+constexpr int kThreads = 1024;             // one block per SM
+constexpr int kWarps = kThreads / 32;
+constexpr int kMinBlocksPerSM = 1;
+constexpr int kMaxCtas = 1024;             // blocks per launch (prefix lives in shared memory)
+constexpr int kFlagUnroll = 2;             // block-wide tiles in flight when flagging
+constexpr int kEmitUnroll = 4;             // pillars in flight per warp when emitting
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded spins: 1 s
+constexpr int64_t kMaxAxisCells = int64_t(1) << 24;
+
+// Control block of one workspace (device memory, zero at creation, epoch 1).
+struct Control {
+  unsigned int bar;     // grid-barrier arrivals in the running launch
+  unsigned int done;    // blocks finished in the running launch
+  int err;              // most negative status recorded in the running launch
+  unsigned int dirty;   // 1: the table may hold stale entries
+  unsigned int epoch;   // launch number
+  unsigned int pad[3];
+};
+
+struct KParams {
+  const float4* points;
+  long long n;
+  long long chunk;   // points owned by each block in phase 2
+  float lo_x, lo_y, lo_z;
+  float v_x, v_y, v_z;
+  float g_xf, g_yf, g_zf;
+  int g_x;
+  int K;             // max_points
+  int KS;            // list stride in uint32 entries (K rounded up to 4)
+  int max_voxels;
+  int hash_mode;
+  unsigned int table_mask;
+  uint32_t* lists;
+  int32_t* keys;
+  int32_t* slot_of_point;
+  int32_t* firsts;
+  int32_t* tile_buf;     // [N] each tile's point indices, grouped by pillar
+  int32_t* grp_info;     // [N] at a group leader's index: (offset in tile << 11) | size
+  unsigned int* counts;  // [kMaxCtas] first points per block
+  Control* ctl;
+  size_t list_words_cap;  // whole allocation, for the dirty reset
+  size_t key_words_cap;
+  float4* out_voxels;
+  int32_t* out_coords;
+  int32_t* out_counts;
+  int32_t* out_num;
+};
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned int ld_relaxed(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ long long lmin(long long a, long long b) { return a < b ? a : b; }
+
+__device__ __forceinline__ unsigned int lanemask_lt() {
+  unsigned int m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// ------------------------------------------------------------ instrumentation
+
+// A PV_INSTRUMENT build stamps the global timer per block at each phase
+// boundary (read back with pv_debug_phase_times); the normal build has none.
+#ifdef PV_INSTRUMENT
+constexpr int kStampCtas = 4096;
+constexpr int kStamps = 8;
+__device__ unsigned long long g_phase_ns[kStampCtas][kStamps];
+#define PV_STAMP(k)                                                          \
+  do {                                                                       \
+    __syncthreads();                                                         \
+    if (threadIdx.x == 0 && blockIdx.x < kStampCtas)                         \
+      g_phase_ns[blockIdx.x][k] = global_timer_ns();                         \
+  } while (0)
+#else
+#define PV_STAMP(k) \
+  do {              \
+  } while (0)
+#endif
+
+// ------------------------------------------------------------ block-wide helpers
+
+// Thread 0 waits (bounded) until *flag reaches `target` (>=) or equals it
+// (exact); returns false after the time limit, recording PV_ERR_TIMEOUT.
+__device__ bool wait_flag(Control* ctl, const unsigned int* flag, unsigned int target, bool exact,
+                          int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    unsigned int v = ld_acquire(flag);
+    if (exact ? v != target : v < target) {
+      const unsigned long long t0 = global_timer_ns();
+      do {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          atomicMin(&ctl->err, PV_ERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        v = ld_acquire(flag);
+      } while (exact ? v != target : v < target);
+    }
+    __threadfence();
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+// All blocks of the cooperative launch arrive; `target` counts arrivals
+// since the launch began (P for the first barrier, 2P for the next).
+__device__ bool grid_sync(Control* ctl, unsigned int target, int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&ctl->bar, 1u);
+  }
+  return wait_flag(ctl, &ctl->bar, target, false, s_flag);
+}
+
+// Exclusive prefix sum over the block; *total receives the block sum.
+__device__ unsigned int block_exclusive_scan(unsigned int x, unsigned int* s_tmp, unsigned int* total) {
+  const unsigned int lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  unsigned int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= static_cast<unsigned int>(o)) incl += y;
+  }
+  if (lane == 31) s_tmp[warp] = incl;
+  __syncthreads();
+  unsigned int before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const unsigned int c = s_tmp[w];
+    before += (w < static_cast<int>(warp)) ? c : 0u;
+    tot += c;
+  }
+  __syncthreads();
+  *total = tot;
+  return before + incl - x;
+}
+
+// ------------------------------------------------------------ binning
+
+__device__ __forceinline__ bool finite_bits(float f) {
+  return (__float_as_uint(f) & 0x7f800000u) != 0x7f800000u;
+}
+
+// floorf of the IEEE round-to-nearest quotient; bounds tested on the float
+// cell, so a huge or infinite quotient never reaches the integer cast.
+__device__ __forceinline__ bool bin_axis(float c, float lo, float v, float g, int* cell) {
+  const float q = floorf(__fdiv_rn(__fsub_rn(c, lo), v));
+  const bool ok = (q >= 0.0f) && (q < g);
+  *cell = ok ? static_cast<int>(q) : 0;
+  return ok;
+}
+
+__device__ __forceinline__ bool bin_point(const float4& q, const KParams& p, int* key) {
+  if (!(finite_bits(q.x) && finite_bits(q.y) && finite_bits(q.z))) return false;
+  int cx, cy, cz;
+  if (!bin_axis(q.x, p.lo_x, p.v_x, p.g_xf, &cx)) return false;
+  if (!bin_axis(q.y, p.lo_y, p.v_y, p.g_yf, &cy)) return false;
+  if (!bin_axis(q.z, p.lo_z, p.v_z, p.g_zf, &cz)) return false;
+  *key = cy * p.g_x + cx;
+  return true;
+}
+
+// ------------------------------------------------------------ pillar table
+
+__device__ __forceinline__ unsigned int mix32(unsigned int h) {
+  // Murmur3 finaliser: spreads ids that differ by large strides.
+  h ^= h >> 16;
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  h ^= h >> 16;
+  return h;
+}
+
+// Find or claim the hashed slot of `key`.  At most table-size probes; -1 if
+// the table is full.
+__device__ __forceinline__ int claim_slot(int32_t* keys, unsigned int mask, int key) {
+  unsigned int h = mix32(static_cast<unsigned int>(key)) & mask;
+  for (unsigned int probe = 0; probe <= mask; ++probe) {
+    const int cur = __ldcg(keys + h);
+    if (cur == key) return static_cast<int>(h);
+    if (cur == kNoKey) {
+      const int old = atomicCAS(keys + h, kNoKey, key);
+      if (old == kNoKey || old == key) return static_cast<int>(h);
+    }
+    h = (h + 1) & mask;
+  }
+  return -1;
+}
+
+// Insert the group-leader index x into list L, which keeps the K smallest
+// leader indices of a pillar in ascending order (atomicMin cascade: each
+// entry keeps the minimum of what reaches it and passes the larger value on,
+// so entry k ends as the (k+1)-th smallest whatever order inserts arrive in).
+// Values in a list only ever decrease, so an entry read below x stays below
+// x: the cascade may start at the length of the strictly increasing run of
+// entries read below x (distinct leaders, all smaller than x), and an entry
+// K-1 read below x keeps x out altogether.
+__device__ __forceinline__ void list_insert(uint32_t* L, int K, int KS, uint32_t x) {
+  const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+  const uint32_t last = __ldcg(L + (K - 1));
+  uint4 q[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) q[t] = (4 * t < KS) ? __ldcg(reinterpret_cast<const uint4*>(L + 4 * t)) : e4;
+  if (last < x) return;
+  int a = 0;
+  uint32_t prev = 0;
+  bool run = true;
+  auto step = [&](uint32_t y) {
+    if (run && y < x && (a == 0 || y > prev)) {
+      prev = y;
+      ++a;
+    } else {
+      run = false;
+    }
+  };
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    step(q[t].x); step(q[t].y); step(q[t].z); step(q[t].w);
+  }
+  for (int e = 16; run && e < K; e += 16) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      q[t] = (e + 4 * t < KS) ? __ldcg(reinterpret_cast<const uint4*>(L + e + 4 * t)) : e4;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      step(q[t].x); step(q[t].y); step(q[t].z); step(q[t].w);
+    }
+  }
+  // Stride padding past K reads empty, so a >= K only if K entries are below x.
+  for (int k = a; k < K; ++k) {
+    const uint32_t old = atomicMin(L + k, x);
+    if (old == kEmpty) return;
+    x = old > x ? old : x;
+  }
+}
+
+// ------------------------------------------------------------ block tiles
+
+// Shared-memory grouping of one block tile (kThreads consecutive points):
+// an open-addressing map slot -> map position, per (position, warp) the
+// number of the warp's points in that slot, and per position the group's
+// offset in the tile's grouped layout.  A point's rank among the tile's
+// points of its pillar is the sum over earlier warps plus its rank in its
+// own warp (lanes hold consecutive indices).
+constexpr int kTileHash = 2 * kThreads;
+
+// Dynamic shared memory of the kernel: the tile map.
+constexpr int kDynSmem = kTileHash * kWarps + kTileHash * 4 + kTileHash * 2 + kThreads * 2;
+
+struct TileMap {
+  unsigned int* cnt;         // [kTileHash][kWarps / 4] packed byte counters
+  int* key;                  // [kTileHash], -1 = free
+  unsigned short* off;       // [kTileHash] group offset in the tile layout
+  unsigned short* used;      // [kThreads] map positions claimed in this tile
+  unsigned int* nused;
+};
+
+// The warp-group leader claims (or finds) the map position of `slot`.
+__device__ __forceinline__ int tile_claim(const TileMap& m, int slot) {
+  unsigned int h = mix32(static_cast<unsigned int>(slot)) & (kTileHash - 1);
+  for (int probe = 0; probe < kTileHash; ++probe) {  // at most kThreads keys: never full
+    const int cur = atomicCAS(m.key + h, -1, slot);
+    if (cur == -1) {
+      m.used[atomicAdd(m.nused, 1u)] = static_cast<unsigned short>(h);
+      return static_cast<int>(h);
+    }
+    if (cur == slot) return static_cast<int>(h);
+    h = (h + 1) & (kTileHash - 1);
+  }
+  return -1;
+}
+
+// Byte counters at map position h: *before = warps 0 .. warp-1, *total = all.
+__device__ __forceinline__ void tile_counts(const TileMap& m, int h, unsigned int warp, unsigned int* before,
+                                            unsigned int* total) {
+  const uint4* row = reinterpret_cast<const uint4*>(m.cnt + static_cast<size_t>(h) * (kWarps / 4));
+  unsigned int b = 0, t = 0;
+#pragma unroll
+  for (int r = 0; r < kWarps / 16; ++r) {
+    const uint4 q = row[r];
+    const unsigned int w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int lo = 16 * r + 4 * c;  // warp of the word's lowest byte
+      const unsigned int all = (w[c] * 0x01010101u) >> 24;  // byte sum (bytes <= 32)
+      t += all;
+      const int keep = static_cast<int>(warp) - lo;
+      if (keep >= 4) {
+        b += all;
+      } else if (keep > 0) {
+        b += ((w[c] & ((1u << (8 * keep)) - 1u)) * 0x01010101u) >> 24;
+      }
+    }
+  }
+  *before = b;
+  *total = t;
+}
+
+// Slot of the pillar with rank r: binary search of the owner block in the
+// exclusive prefix (s_prefix[0..P], s_prefix[P] = total), then its
+// compacted first-point list.
+__device__ __forceinline__ int slot_of_rank(const KParams& p, const unsigned int* s_prefix, unsigned int P,
+                                            unsigned int r) {
+  unsigned int lo = 0, hi = P;  // invariant: s_prefix[lo] <= r < s_prefix[hi]
+  while (hi - lo > 1) {
+    const unsigned int mid = (lo + hi) >> 1;
+    if (s_prefix[mid] <= r) lo = mid; else hi = mid;
+  }
+  return __ldcg(p.firsts + static_cast<long long>(lo) * p.chunk + (r - s_prefix[lo]));
+}
+
+// ------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(const KParams p) {
+  extern __shared__ __align__(16) unsigned char s_dyn[];
+  __shared__ unsigned int s_prefix[kMaxCtas + 1];
+  __shared__ unsigned int s_tile[kFlagUnroll][kWarps];
+  __shared__ unsigned int s_tmp[kWarps];
+  __shared__ int s_flag;
+  __shared__ unsigned int s_nused;
+
+  const unsigned int P = gridDim.x;
+  const unsigned int cta = blockIdx.x;
+  const unsigned int tid = threadIdx.x;
+  const unsigned int lane = tid & 31u;
+  const unsigned int warp = tid >> 5;
+  const size_t gtid = static_cast<size_t>(cta) * kThreads + tid;
+  const size_t gthreads = static_cast<size_t>(P) * kThreads;
+  const long long gwarp = static_cast<long long>(cta) * kWarps + warp;
+  const long long nwarps = static_cast<long long>(P) * kWarps;
+  const int K = p.K;
+
+  const unsigned int epoch = ld_relaxed(&p.ctl->epoch);
+  const unsigned int dirty = ld_relaxed(&p.ctl->dirty);
+  unsigned int bar_target = P;
+  bool alive = true;
+  (void)epoch;
+  PV_STAMP(0);
+
+  // Recovery after a failed launch: empty the whole table first.
+  if (dirty) {
+    const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+    uint4* l4 = reinterpret_cast<uint4*>(p.lists);
+    for (size_t q = gtid; q < p.list_words_cap / 4; q += gthreads) l4[q] = e4;
+    for (size_t q = gtid; q < p.key_words_cap; q += gthreads) p.keys[q] = kNoKey;
+    alive = grid_sync(p.ctl, bar_target, &s_flag);
+    bar_target += P;
+  }
+
+  // ---- phase 1: bin every point; lay each block tile out grouped by pillar
+  // (first-appearance order inside the tile), and insert one entry per
+  // (pillar, tile) group, the group's first point, into the pillar's list.
+  if (alive) {
+    TileMap tm;
+    tm.cnt = reinterpret_cast<unsigned int*>(s_dyn);
+    tm.key = reinterpret_cast<int*>(s_dyn + kTileHash * kWarps);
+    tm.off = reinterpret_cast<unsigned short*>(s_dyn + kTileHash * kWarps + kTileHash * 4);
+    tm.used = reinterpret_cast<unsigned short*>(s_dyn + kTileHash * kWarps + kTileHash * 6);
+    tm.nused = &s_nused;
+    for (int h = static_cast<int>(tid); h < kTileHash; h += kThreads) {
+      tm.key[h] = -1;
+#pragma unroll
+      for (int w4 = 0; w4 < kWarps / 4; ++w4) tm.cnt[h * (kWarps / 4) + w4] = 0u;
+    }
+    if (tid == 0) s_nused = 0;
+
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const long long stride = static_cast<long long>(P) * kThreads;
+    long long tb = static_cast<long long>(cta) * kThreads;
+    float4 q = (tb + tid < p.n) ? __ldg(p.points + tb + tid) : z4;
+    for (; tb < p.n; tb += stride) {
+      const long long i = tb + tid;
+      const long long inext = i + stride;
+      const float4 qn = inext < p.n ? __ldg(p.points + inext) : z4;  // next tile, in flight early
+      int slot = -1;
+      if (i < p.n) {
+        int key;
+        if (bin_point(q, p, &key)) {
+          slot = p.hash_mode ? claim_slot(p.keys, p.table_mask, key) : key;
+          if (slot < 0) atomicMin(&p.ctl->err, PV_ERR_CAPACITY);
+        }
+      }
+      const unsigned int peers = __match_any_sync(0xffffffffu, slot);
+      const int leader = __ffs(peers) - 1;
+      __syncthreads();  // the previous tile's map is clear
+      int h = -1;
+      if (slot >= 0 && static_cast<int>(lane) == leader) {
+        h = tile_claim(tm, slot);
+        if (h >= 0) {
+          reinterpret_cast<unsigned char*>(tm.cnt + h * (kWarps / 4))[warp] =
+              static_cast<unsigned char>(__popc(peers));
+        } else {  // cannot happen: at most kThreads keys in 2 * kThreads positions
+          atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
+        }
+      }
+      h = __shfl_sync(0xffffffffu, h, leader);
+      if (h < 0) slot = -1;
+      if (i < p.n) p.slot_of_point[i] = slot;
+      __syncthreads();  // every warp group registered
+      unsigned int trank = 0, tot = 0;
+      if (slot >= 0) {
+        tile_counts(tm, h, warp, &trank, &tot);
+        trank += __popc(peers & lanemask_lt());
+      }
+      // Group offsets in the tile layout: groups in order of their first point.
+      unsigned int tile_valid;
+      const unsigned int goff = block_exclusive_scan((slot >= 0 && trank == 0) ? tot : 0u, s_tmp, &tile_valid);
+      (void)tile_valid;
+      if (slot >= 0 && trank == 0) tm.off[h] = static_cast<unsigned short>(goff);
+      const unsigned int nu = s_nused;
+      __syncthreads();  // offsets published
+      unsigned int off = 0;
+      if (slot >= 0) off = tm.off[h];
+      __syncthreads();  // every map read done: empty the map for the next tile
+      if (tid == 0) s_nused = 0;
+      for (unsigned int j = tid; j < nu; j += kThreads) {
+        const int hh = tm.used[j];
+        tm.key[hh] = -1;
+#pragma unroll
+        for (int w4 = 0; w4 < kWarps / 4; ++w4) tm.cnt[hh * (kWarps / 4) + w4] = 0u;
+      }
+      if (slot >= 0) {
+        p.tile_buf[tb + off + trank] = static_cast<int32_t>(i);
+        if (trank == 0) {
+          p.grp_info[i] = static_cast<int32_t>((off << 11) | tot);
+          list_insert(p.lists + static_cast<size_t>(slot) * p.KS, K, p.KS, static_cast<uint32_t>(i));
+        }
+      }
+      q = qn;
+    }
+    PV_STAMP(1);
+    alive = grid_sync(p.ctl, bar_target, &s_flag);
+  }
+  PV_STAMP(2);
+
+  const long long begin = lmin(p.n, static_cast<long long>(cta) * p.chunk);
+  const long long end = lmin(p.n, begin + p.chunk);
+  const unsigned int M = static_cast<unsigned int>(p.max_voxels);
+  unsigned int V = 0;
+
+  if (alive) {
+    // ---- phase 2a: first points of this block's range, compacted in index order.
+    unsigned int local = 0;
+    for (long long base = begin; base < end; base += static_cast<long long>(kFlagUnroll) * kThreads) {
+      int s[kFlagUnroll];
+      uint32_t head[kFlagUnroll];
+#pragma unroll
+      for (int u = 0; u < kFlagUnroll; ++u) {
+        const long long i = base + u * kThreads + tid;
+        s[u] = i < end ? __ldcg(p.slot_of_point + i) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kFlagUnroll; ++u)
+        head[u] = s[u] >= 0 ? __ldcg(p.lists + static_cast<size_t>(s[u]) * p.KS) : kEmpty;
+      unsigned int ball[kFlagUnroll];
+#pragma unroll
+      for (int u = 0; u < kFlagUnroll; ++u) {
+        const long long i = base + u * kThreads + tid;
+        ball[u] = __ballot_sync(0xffffffffu, s[u] >= 0 && head[u] == static_cast<uint32_t>(i));
+        if (lane == 0) s_tile[u][warp] = __popc(ball[u]);
+      }
+      __syncthreads();
+      unsigned int run = local;
+#pragma unroll
+      for (int u = 0; u < kFlagUnroll; ++u) {
+        unsigned int before = 0, tile = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const unsigned int c = s_tile[u][w];
+          before += (w < static_cast<int>(warp)) ? c : 0u;
+          tile += c;
+        }
+        if ((ball[u] >> lane) & 1u) p.firsts[begin + run + before + __popc(ball[u] & lanemask_lt())] = s[u];
+        run += tile;
+      }
+      local = run;
+      __syncthreads();
+    }
+    PV_STAMP(3);
+
+    // ---- phase 2b: publish the count; after a second barrier every block
+    // scans all counts itself (one count per thread) into shared memory.
+    if (tid == 0) p.counts[cta] = local;
+    alive = grid_sync(p.ctl, bar_target + P, &s_flag);
+  }
+
+  unsigned int total = 0;
+  if (alive) {
+    const unsigned int c = tid < P ? __ldcg(p.counts + tid) : 0u;
+    const unsigned int excl = block_exclusive_scan(c, s_tmp, &total);
+    if (tid < P) s_prefix[tid] = excl;
+    if (tid == 0) s_prefix[P] = total;
+    __syncthreads();
+    V = total < M ? total : M;
+    PV_STAMP(4);
+
+    // ---- phase 2c: output rows, ranks spread over every warp of the grid.
+    // A pillar's points are its groups, concatenated in list order: lane g
+    // holds group g (leader index, tile offset, size); output position e
+    // belongs to the last group whose running start is <= e.
+    bool stale = false;
+    for (long long r0 = gwarp; r0 < V; r0 += kEmitUnroll * nwarps) {
+      int slot[kEmitUnroll];
+      bool ok[kEmitUnroll];
+#pragma unroll
+      for (int u = 0; u < kEmitUnroll; ++u) {
+        const long long r = r0 + u * nwarps;
+        ok[u] = r < V;
+        slot[u] = ok[u] ? slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r)) : 0;
+      }
+      // Group descriptors: leader (list entry), then its (offset, size).
+      uint32_t lead[kEmitUnroll];
+#pragma unroll
+      for (int u = 0; u < kEmitUnroll; ++u)
+        lead[u] = (ok[u] && static_cast<int>(lane) < K) ? __ldcg(p.lists + static_cast<size_t>(slot[u]) * p.KS + lane)
+                                                        : kEmpty;
+      uint32_t ginfo[kEmitUnroll];
+#pragma unroll
+      for (int u = 0; u < kEmitUnroll; ++u) {
+        if (lead[u] != kEmpty && static_cast<long long>(lead[u]) >= p.n) {  // never in a clean table
+          lead[u] = kEmpty;
+          stale = true;
+        }
+        ginfo[u] = lead[u] != kEmpty ? static_cast<uint32_t>(__ldcg(p.grp_info + lead[u])) : 0u;
+      }
+      unsigned int cnt[kEmitUnroll];
+      int gstart[kEmitUnroll];
+#pragma unroll
+      for (int u = 0; u < kEmitUnroll; ++u) {
+        // Inclusive scan of group sizes over the lanes (groups), capped at K.
+        const unsigned int size = ginfo[u] & 2047u;
+        unsigned int incl = size;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= static_cast<unsigned int>(o)) incl += y;
+        }
+        gstart[u] = static_cast<int>(incl - size);
+        const unsigned int all = __shfl_sync(0xffffffffu, incl, 31);
+        cnt[u] = all < static_cast<unsigned int>(K) ? all : static_cast<unsigned int>(K);
+      }
+      for (int e0 = 0; e0 < K; e0 += 32) {
+        const int e = e0 + static_cast<int>(lane);
+        int32_t idx[kEmitUnroll];
+#pragma unroll
+        for (int u = 0; u < kEmitUnroll; ++u) {
+          idx[u] = -1;
+          // Group of position e: the last valid group whose start is <= e
+          // (valid groups fill lanes 0 .. G-1 with strictly increasing starts).
+          const int G = __popc(__ballot_sync(0xffffffffu, lead[u] != kEmpty));
+          int g = G > 0 ? 0 : -1;
+#pragma unroll
+          for (int step = 16; step >= 1; step >>= 1) {
+            const int j = g + step;
+            const int st = __shfl_sync(0xffffffffu, gstart[u], j < 32 ? j : 31);
+            if (g >= 0 && j < G && st <= e) g = j;
+          }
+          const int gsafe = g < 0 ? 0 : g;
+          const uint32_t gl_lead = __shfl_sync(0xffffffffu, lead[u], gsafe);
+          const uint32_t gl_info = __shfl_sync(0xffffffffu, ginfo[u], gsafe);
+          const int gl_start = __shfl_sync(0xffffffffu, gstart[u], gsafe);
+          if (ok[u] && e < K && g >= 0 && static_cast<unsigned int>(e) < cnt[u]) {
+            const long long tbase = static_cast<long long>(gl_lead) & ~static_cast<long long>(kThreads - 1);
+            idx[u] = __ldcg(p.tile_buf + tbase + (gl_info >> 11) + (e - gl_start));
+          }
+        }
+        float4 row[kEmitUnroll];
+#pragma unroll
+        for (int u = 0; u < kEmitUnroll; ++u) {
+          bool has = idx[u] >= 0;
+          if (has && static_cast<long long>(idx[u]) >= p.n) {
+            has = false;
+            stale = true;
+          }
+          row[u] = has ? __ldg(p.points + idx[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kEmitUnroll; ++u) {
+          if (ok[u] && e < K) {
+            const long long r = r0 + u * nwarps;
+            p.out_voxels[static_cast<size_t>(r) * K + e] = row[u];
+            p.lists[static_cast<size_t>(slot[u]) * p.KS + e] = kEmpty;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kEmitUnroll; ++u) {
+        if (ok[u] && lane == 0) {
+          const size_t r = static_cast<size_t>(r0 + u * nwarps);
+          const int key = p.hash_mode ? __ldcg(p.keys + slot[u]) : slot[u];
+          p.out_coords[3 * r + 0] = 0;
+          p.out_coords[3 * r + 1] = key / p.g_x;
+          p.out_coords[3 * r + 2] = key % p.g_x;
+          p.out_counts[r] = static_cast<int32_t>(cnt[u]);
+          if (p.hash_mode) p.keys[slot[u]] = kNoKey;
+        }
+      }
+    }
+    if (stale) atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
+    PV_STAMP(5);
+
+    // ---- phase 2d: empty the slots of pillars past the budget (ranks M..total-1).
+    for (long long r0 = static_cast<long long>(M) + gwarp * 32; r0 < total; r0 += nwarps * 32) {
+      const long long r = r0 + lane;
+      const int mine = r < total ? slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r)) : -1;
+      for (int t = 0; t < 32; ++t) {
+        const int s = __shfl_sync(0xffffffffu, mine, t);
+        if (s < 0) break;  // ranks ascend with t, so the rest are past the end too
+        uint32_t* L = p.lists + static_cast<size_t>(s) * p.KS;
+        for (int e = static_cast<int>(lane); e < K; e += 32) L[e] = kEmpty;
+        if (p.hash_mode && lane == 0) p.keys[s] = kNoKey;
+      }
+    }
+    PV_STAMP(6);
+
+    // ---- phase 2e: zero rows V .. max_voxels-1 (all blocks share it).
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const size_t Kz = static_cast<size_t>(K);
+    for (size_t q = static_cast<size_t>(V) * Kz + gtid; q < static_cast<size_t>(M) * Kz; q += gthreads)
+      p.out_voxels[q] = z4;
+    for (size_t q = 3 * static_cast<size_t>(V) + gtid; q < 3 * static_cast<size_t>(M); q += gthreads)
+      p.out_coords[q] = 0;
+    for (size_t q = static_cast<size_t>(V) + gtid; q < static_cast<size_t>(M); q += gthreads)
+      p.out_counts[q] = 0;
+  }
+
+  // ---- the last block to finish publishes the status and rearms the control block.
+  PV_STAMP(7);
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned int prev = atomicAdd(&p.ctl->done, 1u);
+    if (prev == P - 1) {
+      __threadfence();
+      const int err = *reinterpret_cast<volatile int*>(&p.ctl->err);
+      *p.out_num = err != 0 ? err : static_cast<int32_t>(V);
+      p.ctl->dirty = err != 0 ? 1u : 0u;
+      p.ctl->err = 0;
+      p.ctl->bar = 0;
+      p.ctl->done = 0;
+      const unsigned int next = epoch + 1;
+      p.ctl->epoch = next == 0 ? 1u : next;
+      __threadfence();
+    }
+  }
+}
+
+// ------------------------------------------------------------ host side
+
+struct DeviceInfo {
+  int sms = 0;
+  int blocks_per_sm = 0;
+  bool cooperative = false;
+};
+
+struct Workspace {
+  std::mutex mu;
+  int device = 0;
+  Control* ctl = nullptr;
+  unsigned int* counts = nullptr;  // [kMaxCtas]
+  int32_t* slot_of_point = nullptr;
+  int32_t* firsts = nullptr;
+  int32_t* tile_buf = nullptr;
+  int32_t* grp_info = nullptr;
+  size_t points_cap = 0;
+  uint32_t* lists = nullptr;
+  size_t list_words_cap = 0;
+  int32_t* keys = nullptr;
+  size_t key_words_cap = 0;
+  // Device copies used by pv_voxelize_host.
+  unsigned char* staging = nullptr;
+  size_t staging_cap = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::pair<int, pv_stream_t>, Workspace*> g_ws;
+
+struct Plan {
+  int64_t g[3];
+  int mode;
+  int64_t T;
+  int KS;
+  int ctas;
+  int64_t chunk;
+  unsigned int mask;
+  size_t list_words;
+  size_t key_words;
+  size_t bytes;
+};
+
+int64_t next_pow2(int64_t v) {
+  int64_t p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+int grid_extents(const float r[6], const float v[3], int64_t g[3]) {
+  if (!r || !v) return PV_ERR_INVALID;
+  for (int a = 0; a < 3; ++a) {
+    const float lo = r[a], hi = r[a + 3], s = v[a];
+    if (!std::isfinite(lo) || !std::isfinite(hi) || !std::isfinite(s)) return PV_ERR_INVALID;
+    if (!(s > 0.0f) || !(hi > lo)) return PV_ERR_INVALID;
+    const double q = (static_cast<double>(hi) - static_cast<double>(lo)) / static_cast<double>(s);
+    if (!(q < 2.0 * static_cast<double>(kMaxAxisCells))) return PV_ERR_INVALID;
+    const int64_t cells = static_cast<int64_t>(std::llround(q));  // half away from zero
+    if (cells < 1 || cells > kMaxAxisCells) return PV_ERR_INVALID;
+    g[a] = cells;
+  }
+  if (g[0] * g[1] >= (int64_t(1) << 31)) return PV_ERR_INVALID;
+  if (g[2] != 1) return PV_ERR_UNSUPPORTED;
+  return PV_OK;
+}
+
+int device_info(int dev, DeviceInfo* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_devices.find(dev);
+  if (it != g_devices.end()) {
+    *out = it->second;
+    return PV_OK;
+  }
+  DeviceInfo d;
+  int coop = 0;
+  if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) return PV_ERR_CUDA;
+  if (cudaFuncSetAttribute(pv_voxelize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
+      cudaSuccess)
+    return PV_ERR_CUDA;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.blocks_per_sm, pv_voxelize_kernel, kThreads, kDynSmem) !=
+      cudaSuccess)
+    return PV_ERR_CUDA;
+  d.cooperative = coop != 0;
+  if (d.blocks_per_sm < 1 || !d.cooperative) return PV_ERR_CUDA;
+  g_devices[dev] = d;
+  *out = d;
+  return PV_OK;
+}
+
+int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int M, const pv_options* opt,
+              const DeviceInfo& dev, Plan* pl) {
+  if (N < 0 || N >= (int64_t(1) << 31) - 1) return PV_ERR_INVALID;
+  if (K < 1 || K > PV_MAX_POINTS_LIMIT || M < 1) return PV_ERR_INVALID;
+  if (static_cast<int64_t>(K) * M >= (int64_t(1) << 31)) return PV_ERR_INVALID;
+  int st = grid_extents(range, vsize, pl->g);
+  if (st != PV_OK) return st;
+  pv_options o{};
+  if (opt) o = *opt;
+  if (o.table_mode < 0 || o.table_mode > 2 || o.table_log2 < 0 || o.table_log2 > 31 || o.ctas_per_sm < 0)
+    return PV_ERR_INVALID;
+  const int64_t cells = pl->g[0] * pl->g[1];
+  const int64_t distinct_bound = std::max<int64_t>(1, std::min(N, cells));
+  const int64_t hashed_T = next_pow2(std::max<int64_t>(2 * distinct_bound, 1024));
+  pl->KS = (K + 3) & ~3;
+  const int64_t direct_bytes = cells * pl->KS * 4;
+  int mode = o.table_mode;
+  if (mode == 0) mode = (cells <= 2 * hashed_T && direct_bytes <= (int64_t(1) << 31)) ? 1 : 2;
+  pl->mode = mode;
+  if (mode == 1) {
+    pl->T = cells;
+    pl->mask = 0;
+  } else {
+    pl->T = o.table_log2 ? (int64_t(1) << std::max(2, o.table_log2)) : hashed_T;
+    if (pl->T > (int64_t(1) << 31)) return PV_ERR_INVALID;
+    pl->mask = static_cast<unsigned int>(pl->T - 1);
+  }
+  pl->list_words = static_cast<size_t>(pl->T) * pl->KS;
+  pl->key_words = mode == 2 ? static_cast<size_t>(pl->T) : 0;
+  const int per_sm = o.ctas_per_sm ? std::min(o.ctas_per_sm, dev.blocks_per_sm) : dev.blocks_per_sm;
+  pl->ctas = std::min(kMaxCtas, std::max(1, dev.sms * per_sm));
+  pl->chunk = (N + pl->ctas - 1) / pl->ctas;
+  pl->bytes = sizeof(Control) + 4 * static_cast<size_t>(kMaxCtas) + 16 * static_cast<size_t>(N) +
+              4 * (pl->list_words + pl->key_words);
+  return PV_OK;
+}
+
+// Grows one workspace region.  New memory is set to `fill` on `stream`.
+template <typename T>
+int grow(T** ptr, size_t* cap, size_t need, int fill, pv_stream_t stream, bool* synced) {
+  if (*cap >= need) return PV_OK;
+  if (!*synced) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PV_ERR_CUDA;
+    *synced = true;
+  }
+  if (*ptr) cudaFree(*ptr);
+  *ptr = nullptr;
+  *cap = 0;
+  void* mem = nullptr;
+  if (cudaMalloc(&mem, need * sizeof(T)) != cudaSuccess) {
+    cudaGetLastError();
+    return PV_ERR_ALLOC;
+  }
+  if (cudaMemsetAsync(mem, fill, need * sizeof(T), stream) != cudaSuccess) {
+    cudaFree(mem);
+    return PV_ERR_CUDA;
+  }
+  *ptr = static_cast<T*>(mem);
+  *cap = need;
+  return PV_OK;
+}
+
+int get_workspace(int dev, pv_stream_t stream, Workspace** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_pair(dev, stream);
+  auto it = g_ws.find(key);
+  if (it != g_ws.end()) {
+    *out = it->second;
+    return PV_OK;
+  }
+  Workspace* ws = new (std::nothrow) Workspace();
+  if (!ws) return PV_ERR_ALLOC;
+  ws->device = dev;
+  void* ctl = nullptr;
+  if (cudaMalloc(&ctl, sizeof(Control)) != cudaSuccess) {
+    cudaGetLastError();
+    delete ws;
+    return PV_ERR_ALLOC;
+  }
+  Control init{};
+  init.epoch = 1;
+  if (cudaMemcpy(ctl, &init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(ctl);
+    delete ws;
+    return PV_ERR_CUDA;
+  }
+  ws->ctl = static_cast<Control*>(ctl);
+  void* cnt = nullptr;
+  if (cudaMalloc(&cnt, sizeof(unsigned int) * kMaxCtas) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(ctl);
+    delete ws;
+    return PV_ERR_ALLOC;
+  }
+  ws->counts = static_cast<unsigned int*>(cnt);
+  g_ws[key] = ws;
+  *out = ws;
+  return PV_OK;
+}
+
+size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
+
+// Makes every region big enough for `pl` (caller holds ws->mu).
+int reserve(Workspace* ws, const Plan& pl, int64_t N, pv_stream_t stream) {
+  bool synced = false;
+  int st;
+  const size_t np = round_up(static_cast<size_t>(std::max<int64_t>(N, 1)), 65536);
+  if (ws->points_cap < np) {
+    const size_t want = std::max(np, ws->points_cap + ws->points_cap / 2);
+    size_t cap_a = ws->points_cap, cap_b = ws->points_cap, cap_c = ws->points_cap, cap_d = ws->points_cap;
+    if ((st = grow(&ws->slot_of_point, &cap_a, want, 0, stream, &synced)) != PV_OK) return st;
+    if ((st = grow(&ws->firsts, &cap_b, want, 0, stream, &synced)) != PV_OK) return st;
+    if ((st = grow(&ws->tile_buf, &cap_c, want, 0, stream, &synced)) != PV_OK) return st;
+    if ((st = grow(&ws->grp_info, &cap_d, want, 0, stream, &synced)) != PV_OK) return st;
+    ws->points_cap = want;
+  }
+  if ((st = grow(&ws->lists, &ws->list_words_cap, round_up(pl.list_words, 4), 0xFF, stream, &synced)) != PV_OK)
+    return st;
+  if (pl.key_words &&
+      (st = grow(&ws->keys, &ws->key_words_cap, pl.key_words, 0xFF, stream, &synced)) != PV_OK)
+    return st;
+  return PV_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device that owns a pointer, or -1 if it is not device (or managed) memory.
+int device_of(const void* ptr) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return -1;
+  return at.device;
+}
+
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev_);
+    if (prev_ != dev) {
+      ok_ = cudaSetDevice(dev) == cudaSuccess;
+      changed_ = true;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed_) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = 0;
+  bool changed_ = false;
+  bool ok_ = true;
+};
+
+int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const float range[6],
+           const float vsize[3], int K, int M, float* out_voxels, int32_t* out_coords, int32_t* out_counts,
+           int32_t* out_num, pv_stream_t stream) {
+  KParams kp;
+  kp.points = reinterpret_cast<const float4*>(points);
+  kp.n = N;
+  kp.chunk = pl.chunk;
+  kp.lo_x = range[0];
+  kp.lo_y = range[1];
+  kp.lo_z = range[2];
+  kp.v_x = vsize[0];
+  kp.v_y = vsize[1];
+  kp.v_z = vsize[2];
+  kp.g_xf = static_cast<float>(pl.g[0]);
+  kp.g_yf = static_cast<float>(pl.g[1]);
+  kp.g_zf = static_cast<float>(pl.g[2]);
+  kp.g_x = static_cast<int>(pl.g[0]);
+  kp.K = K;
+  kp.KS = pl.KS;
+  kp.max_voxels = M;
+  kp.hash_mode = pl.mode == 2 ? 1 : 0;
+  kp.table_mask = pl.mask;
+  kp.lists = ws->lists;
+  kp.keys = ws->keys;
+  kp.slot_of_point = ws->slot_of_point;
+  kp.firsts = ws->firsts;
+  kp.tile_buf = ws->tile_buf;
+  kp.grp_info = ws->grp_info;
+  kp.counts = ws->counts;
+  kp.ctl = ws->ctl;
+  kp.list_words_cap = ws->list_words_cap;
+  kp.key_words_cap = ws->key_words_cap;
+  kp.out_voxels = reinterpret_cast<float4*>(out_voxels);
+  kp.out_coords = out_coords;
+  kp.out_counts = out_counts;
+  kp.out_num = out_num;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned int>(pl.ctas));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kDynSmem;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, pv_voxelize_kernel, kp) != cudaSuccess) {
+    cudaGetLastError();
+    return PV_ERR_CUDA;
+  }
+  return PV_OK;
+}
+
+int voxelize_impl(const float* points, int64_t N, const float range[6], const float vsize[3], int K, int M,
+                  float* out_voxels, int32_t* out_coords, int32_t* out_counts, int32_t* out_num,
+                  const pv_options* opt, pv_stream_t stream) {
+  if (!range || !vsize) return PV_ERR_INVALID;
+  if (!out_voxels || !out_coords || !out_counts || !out_num) return PV_ERR_INVALID;
+  if (N > 0 && !points) return PV_ERR_INVALID;
+  if (!aligned(out_voxels, 16) || !aligned(out_coords, 4) || !aligned(out_counts, 4) || !aligned(out_num, 4))
+    return PV_ERR_INVALID;
+  if (N > 0 && !aligned(points, 16)) return PV_ERR_INVALID;
+  const int dev = device_of(out_voxels);
+  if (dev < 0) return PV_ERR_INVALID;
+  if (device_of(out_coords) != dev || device_of(out_counts) != dev || device_of(out_num) != dev)
+    return PV_ERR_INVALID;
+  if (N > 0 && device_of(points) != dev) return PV_ERR_INVALID;
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return PV_ERR_CUDA;
+  DeviceInfo di;
+  int st = device_info(dev, &di);
+  if (st != PV_OK) return st;
+  Plan pl;
+  if ((st = make_plan(N, range, vsize, K, M, opt, di, &pl)) != PV_OK) return st;
+  Workspace* ws = nullptr;
+  if ((st = get_workspace(dev, stream, &ws)) != PV_OK) return st;
+  std::lock_guard<std::mutex> lk(ws->mu);
+  if ((st = reserve(ws, pl, N, stream)) != PV_OK) return st;
+  return launch(ws, pl, points, N, range, vsize, K, M, out_voxels, out_coords, out_counts, out_num, stream);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ C ABI
+
+extern "C" {
+
+int pv_voxelize(const float* points, int64_t num_points, const float point_cloud_range[6],
+                const float voxel_size[3], int max_points, int max_voxels, float* out_voxels,
+                int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels, pv_stream_t stream) {
+  return voxelize_impl(points, num_points, point_cloud_range, voxel_size, max_points, max_voxels, out_voxels,
+                       out_coords, out_counts, out_num_voxels, nullptr, stream);
+}
+
+int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cloud_range[6],
+                   const float voxel_size[3], int max_points, int max_voxels, float* out_voxels,
+                   int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels, const pv_options* options,
+                   pv_stream_t stream) {
+  return voxelize_impl(points, num_points, point_cloud_range, voxel_size, max_points, max_voxels, out_voxels,
+                       out_coords, out_counts, out_num_voxels, options, stream);
+}
+
+int pv_voxelize_host(const float* points_host, int64_t num_points, const float point_cloud_range[6],
+                     const float voxel_size[3], int max_points, int max_voxels, float* out_voxels_host,
+                     int32_t* out_coords_host, int32_t* out_counts_host, int32_t* out_num_voxels_host,
+                     pv_stream_t stream) {
+  if (!point_cloud_range || !voxel_size) return PV_ERR_INVALID;
+  if (!out_voxels_host || !out_coords_host || !out_counts_host || !out_num_voxels_host) return PV_ERR_INVALID;
+  if (num_points > 0 && !points_host) return PV_ERR_INVALID;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PV_ERR_CUDA;
+  DeviceInfo di;
+  int st = device_info(dev, &di);
+  if (st != PV_OK) return st;
+  Plan pl;
+  if ((st = make_plan(num_points, point_cloud_range, voxel_size, max_points, max_voxels, nullptr, di, &pl)) !=
+      PV_OK)
+    return st;
+  Workspace* ws = nullptr;
+  if ((st = get_workspace(dev, stream, &ws)) != PV_OK) return st;
+  std::lock_guard<std::mutex> lk(ws->mu);
+  if ((st = reserve(ws, pl, num_points, stream)) != PV_OK) return st;
+  // Staging layout: points | voxels | coords | counts | num, each 256-byte aligned.
+  const size_t b_pts = round_up(16 * static_cast<size_t>(num_points), 256);
+  const size_t b_vox = round_up(16 * static_cast<size_t>(max_voxels) * max_points, 256);
+  const size_t b_crd = round_up(12 * static_cast<size_t>(max_voxels), 256);
+  const size_t b_cnt = round_up(4 * static_cast<size_t>(max_voxels), 256);
+  const size_t need = b_pts + b_vox + b_crd + b_cnt + 256;
+  bool synced = false;
+  if ((st = grow(&ws->staging, &ws->staging_cap, need, 0, stream, &synced)) !=
+      PV_OK)
+    return st;
+  unsigned char* base = ws->staging;
+  float* d_pts = reinterpret_cast<float*>(base);
+  float* d_vox = reinterpret_cast<float*>(base + b_pts);
+  int32_t* d_crd = reinterpret_cast<int32_t*>(base + b_pts + b_vox);
+  int32_t* d_cnt = reinterpret_cast<int32_t*>(base + b_pts + b_vox + b_crd);
+  int32_t* d_num = reinterpret_cast<int32_t*>(base + b_pts + b_vox + b_crd + b_cnt);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (num_points > 0 &&
+      cudaMemcpyAsync(d_pts, points_host, 16 * static_cast<size_t>(num_points), cudaMemcpyHostToDevice, s) !=
+          cudaSuccess)
+    return PV_ERR_CUDA;
+  if ((st = launch(ws, pl, d_pts, num_points, point_cloud_range, voxel_size, max_points, max_voxels, d_vox, d_crd,
+                   d_cnt, d_num, stream)) != PV_OK)
+    return st;
+  if (cudaMemcpyAsync(out_voxels_host, d_vox, 16 * static_cast<size_t>(max_voxels) * max_points,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(out_coords_host, d_crd, 12 * static_cast<size_t>(max_voxels), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(out_counts_host, d_cnt, 4 * static_cast<size_t>(max_voxels), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(out_num_voxels_host, d_num, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PV_ERR_CUDA;
+  return *out_num_voxels_host < 0 ? *out_num_voxels_host : PV_OK;
+}
+
+int pv_grid_size(const float point_cloud_range[6], const float voxel_size[3], int64_t grid_out[3]) {
+  if (!grid_out) return PV_ERR_INVALID;
+  return grid_extents(point_cloud_range, voxel_size, grid_out);
+}
+
+int pv_query_plan(int64_t num_points, const float point_cloud_range[6], const float voxel_size[3],
+                  int max_points, int max_voxels, const pv_options* options, pv_plan* plan_out) {
+  if (!plan_out) return PV_ERR_INVALID;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PV_ERR_CUDA;
+  }
+  DeviceInfo di;
+  int st = device_info(dev, &di);
+  if (st != PV_OK) return st;
+  Plan pl;
+  if ((st = make_plan(num_points, point_cloud_range, voxel_size, max_points, max_voxels, options, di, &pl)) !=
+      PV_OK)
+    return st;
+  for (int a = 0; a < 3; ++a) plan_out->grid[a] = pl.g[a];
+  plan_out->table_mode = pl.mode;
+  plan_out->table_slots = pl.T;
+  plan_out->list_stride = pl.KS;
+  plan_out->ctas = pl.ctas;
+  plan_out->threads = kThreads;
+  plan_out->points_per_cta = pl.chunk;
+  plan_out->workspace_bytes = static_cast<int64_t>(pl.bytes);
+  return PV_OK;
+}
+
+int pv_release_workspace(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int st = PV_OK;
+  for (auto& kv : g_ws) {
+    Workspace* ws = kv.second;
+    DeviceGuard guard(ws->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) st = PV_ERR_CUDA;
+    cudaFree(ws->ctl);
+    cudaFree(ws->counts);
+    cudaFree(ws->slot_of_point);
+    cudaFree(ws->firsts);
+    cudaFree(ws->tile_buf);
+    cudaFree(ws->grp_info);
+    cudaFree(ws->lists);
+    cudaFree(ws->keys);
+    cudaFree(ws->staging);
+    delete ws;
+  }
+  g_ws.clear();
+  return st;
+}
+
+const char* pv_status_string(int status) {
+  switch (status) {
+    case PV_OK: return "PV_OK";
+    case PV_ERR_INVALID: return "PV_ERR_INVALID: invalid argument";
+    case PV_ERR_UNSUPPORTED: return "PV_ERR_UNSUPPORTED: only pillar grids (grid_z == 1) are supported";
+    case PV_ERR_ALLOC: return "PV_ERR_ALLOC: device workspace allocation failed";
+    case PV_ERR_CUDA: return "PV_ERR_CUDA: CUDA runtime error";
+    case PV_ERR_CAPACITY: return "PV_ERR_CAPACITY: pillar table full";
+    case PV_ERR_TIMEOUT: return "PV_ERR_TIMEOUT: a bounded device wait gave up";
+    case PV_ERR_INTERNAL: return "PV_ERR_INTERNAL: device consistency check failed";
+    default: return status >= 0 ? "pillar count" : "unknown status";
+  }
+}
+
+const char* pv_version(void) { return "0.1.0"; }
+
+#ifdef PV_INSTRUMENT
+// Instrumented builds only: copies [max_ctas][8] phase stamps (ns) to host.
+int pv_debug_phase_times(unsigned long long* out, int max_ctas) {
+  const int n = max_ctas < kStampCtas ? max_ctas : kStampCtas;
+  if (cudaMemcpyFromSymbol(out, g_phase_ns, sizeof(unsigned long long) * kStamps * n) != cudaSuccess)
+    return PV_ERR_CUDA;
+  return PV_OK;
+}
+#endif
+
+}  // extern "C"

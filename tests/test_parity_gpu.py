@@ -1,0 +1,190 @@
+"""GPU parity: the CUDA library against the CPU oracle, bit for bit.
+
+Every output buffer (the full padded [max_voxels, ...] tensors) and V are
+compared byte for byte: the operation is integer/bit-copy work once the
+binning is fixed to IEEE round-to-nearest binary32, so the bar is exact
+equality.  Covers the five workloads at full size, random tiny clouds where
+both caps bind, edge cases (empty, one point, all invalid, one pillar with
+many points, caps of 1, caps not a multiple of 4 or 32), both table modes,
+several launch shapes, repeated runs (determinism), two streams at once,
+the host-buffer entry point and the device error paths (undersized table,
+recovery afterwards).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from _helpers import first_difference, random_tiny_case, same_bits
+
+torch = pytest.importorskip("torch")
+pv = pytest.importorskip("lidar_point_cloud_gb300")
+from lidar_point_cloud_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def gpu_run(pts, r, v, K, M, stream=None, **opts):
+    t = torch.from_numpy(np.ascontiguousarray(pts, dtype=np.float32).reshape(-1, 4)).to(DEV)
+    out = pv.alloc_outputs(K, M, DEV)
+    for o in out:  # poison: the kernel must overwrite every byte
+        o.view(torch.int32).fill_(0x7FBADBAD)
+    pv.voxelize_into(t, r, v, K, M, out, stream=stream, **opts)
+    torch.cuda.synchronize()
+    vox, coords, counts, num = (o.cpu().numpy() for o in out)
+    return vox, coords, counts, int(num[0])
+
+
+def assert_parity(pts, r, v, K, M, **opts):
+    st, ov, oc, on, oV = oracle.voxelize(pts, r, v, K, M)
+    assert st == 0
+    gv, gc, gn, gV = gpu_run(pts, r, v, K, M, **opts)
+    assert gV == oV, (gV, oV)
+    assert same_bits(gc, oc), "coords: " + first_difference(gc, oc)
+    assert same_bits(gn, on), "counts: " + first_difference(gn, on)
+    assert same_bits(gv, ov), "voxels: " + first_difference(gv, ov)
+    return oV
+
+
+WORKLOADS = ["tiny", "kitti", *[f"uniform_{n}" for n in synth.UNIFORM_SIZES], "dense", "adversarial"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pv.load()
+    yield
+    pv.release_workspace()
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_workload_parity(name):
+    pts, P = synth.make(name)
+    assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+
+
+@pytest.mark.parametrize("name", ["kitti", "dense"])
+def test_hashed_table_parity(name):
+    pts, P = synth.make(name)
+    assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, table_mode=2)
+
+
+@pytest.mark.parametrize("ctas_per_sm", [1, 2, 3])
+def test_launch_shape_does_not_change_result(ctas_per_sm):
+    pts, P = synth.make("kitti")
+    assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, ctas_per_sm=ctas_per_sm)
+
+
+def test_random_tiny_clouds():
+    rng = np.random.Generator(np.random.PCG64(4242))
+    for t in range(150):
+        pts, r, v, K, M = random_tiny_case(rng)
+        assert_parity(pts, r, v, K, M, table_mode=(2 if t % 3 == 0 else 0))
+
+
+def test_determinism_repeats():
+    pts, P = synth.make("kitti")
+    ref = gpu_run(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    t = torch.from_numpy(pts).to(DEV)
+    out = pv.alloc_outputs(P.max_points, P.max_voxels, DEV)
+    for _ in range(50):
+        pv.voxelize_into(t, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, out)
+        torch.cuda.synchronize()
+        got = [o.cpu().numpy() for o in out]
+        assert int(got[3][0]) == ref[3]
+        for a, b in zip(got[:3], ref[:3]):
+            assert same_bits(a, b)
+
+
+KR, KV = synth.KITTI_RANGE, synth.KITTI_VOXEL
+
+
+def test_empty_cloud():
+    assert assert_parity(np.zeros((0, 4), np.float32), KR, KV, 32, 1000) == 0
+
+
+def test_single_point():
+    assert assert_parity(np.array([[10.0, 0.0, -1.0, 0.5]], np.float32), KR, KV, 32, 100) == 1
+
+
+def test_all_points_invalid():
+    pts = synth.uniform(5000, 11)
+    pts[:, 0] = -5.0  # every x below x_min
+    assert assert_parity(pts, KR, KV, 32, 100) == 0
+
+
+def test_one_pillar_many_points():
+    rng = np.random.Generator(np.random.PCG64(5))
+    pts = np.zeros((200_000, 4), np.float32)
+    pts[:, 0] = 10.0 + 0.05 * rng.random(200_000)  # cell 62 only
+    pts[:, 1] = 0.01 * rng.random(200_000)
+    pts[:, 2] = -1.0
+    pts[:, 3] = rng.random(200_000)
+    assert assert_parity(pts, KR, KV, 32, 10) == 1
+
+
+@pytest.mark.parametrize("K,M", [(1, 1), (1, 16000), (32, 1), (5, 500), (33, 2000), (64, 3000), (100, 700)])
+def test_caps(K, M):
+    pts, P = synth.make("kitti")
+    assert_parity(pts, P.point_cloud_range, P.voxel_size, K, M)
+
+
+def test_index_intensity_order():
+    pts, P = synth.make("uniform_130000")
+    pts = pts.copy()
+    pts[:, 3] = np.arange(pts.shape[0], dtype=np.float32)
+    assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, 200_000)
+
+
+def test_large_grid_uses_hashed_table():
+    # 1 cm pillars over the KITTI-shaped range: 6912 x 7936 cells, hashed table.
+    r, v = KR, (0.01, 0.01, 4.0)
+    plan = pv.query_plan(122_880, r, v, 32, 60_000)
+    assert plan["table_mode"] == "hashed"
+    pts, _ = synth.make("kitti")
+    assert_parity(pts, r, v, 32, 60_000)
+
+
+def test_capacity_error_then_recovery():
+    pts = synth.uniform(20_000, 12)
+    got = gpu_run(pts, KR, KV, 32, 16_000, table_mode=2, table_log2=4)  # 16 slots
+    assert got[3] == -5  # PV_ERR_CAPACITY
+    assert_parity(pts, KR, KV, 32, 16_000, table_mode=2)
+    assert_parity(pts, KR, KV, 32, 16_000)
+
+
+def test_two_streams():
+    a, Pa = synth.make("kitti")
+    b, Pb = synth.make("uniform_100000")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ta, tb = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
+    oa, ob = pv.alloc_outputs(32, 16000, DEV), pv.alloc_outputs(32, 16000, DEV)
+    torch.cuda.synchronize()
+    for _ in range(5):
+        pv.voxelize_into(ta, KR, KV, 32, 16000, oa, stream=s1)
+        pv.voxelize_into(tb, KR, KV, 32, 16000, ob, stream=s2)
+    torch.cuda.synchronize()
+    for pts, out in ((a, oa), (b, ob)):
+        st, ov, oc, on, oV = oracle.voxelize(pts, KR, KV, 32, 16000)
+        assert int(out[3].item()) == oV
+        assert same_bits(out[0].cpu().numpy(), ov)
+
+
+def test_host_entry_point():
+    pts, P = synth.make("kitti")
+    vox, coords, counts, V = pv.voxelize_host(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    st, ov, oc, on, oV = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    assert V == oV and same_bits(vox, ov) and same_bits(coords, oc) and same_bits(counts, on)
+
+
+def test_sliced_python_entry_point():
+    pts, P = synth.make("tiny")
+    vox, coords, counts = pv.voxelize(torch.from_numpy(pts).to(DEV), P.point_cloud_range, P.voxel_size)
+    st, ov, oc, on, oV = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, 32, 16000)
+    assert vox.shape == (oV, 32, 4) and coords.shape == (oV, 3) and counts.shape == (oV,)
+    assert same_bits(vox.cpu().numpy(), ov[:oV])
