@@ -65,9 +65,11 @@ typedef enum pv_status {
   PV_ERR_TIMEOUT = -6,     /* device: a bounded wait inside the kernel gave up (about
                               one second); the workspace is then fully reset by the
                               next call on the same stream */
-  PV_ERR_INTERNAL = -7     /* device: a consistency check failed (a point index read
+  PV_ERR_INTERNAL = -7,    /* device: a consistency check failed (a point index read
                               from the pillar table was out of range); the workspace is
                               fully reset by the next call on the same stream */
+  PV_ERR_TOO_LARGE = -8    /* pv_voxelize_static only: more points or a larger
+                              max_points than its fixed scratch holds */
 } pv_status;
 
 /* Largest max_points accepted. */
@@ -139,6 +141,39 @@ int pv_voxelize_host(const float* points_host, int64_t num_points, const float p
                      const float voxel_size[3], int max_points, int max_voxels,
                      float* out_voxels_host, int32_t* out_coords_host, int32_t* out_counts_host,
                      int32_t* out_num_voxels_host, pv_stream_t stream);
+
+/*
+ * pv_voxelize_static - pv_voxelize without any device allocation.
+ *
+ * The page has no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory while they run: code being recorded
+ * into a CUDA graph under global capture mode (where cudaMalloc is not
+ * allowed), inference plug-ins whose host owns all device memory, and
+ * real-time pipelines that forbid allocation after start-up.  It takes the
+ * same arguments and gives the same result as pv_voxelize, but its scratch
+ * (table, per-point arrays, control block) lives in one fixed array of
+ * about 17.5 MiB of device memory, declared in the library at file scope:
+ * every GPU that loads the library holds it until the process exits.  The
+ * caller still owns and passes the input and the outputs.
+ *
+ * Limits: num_points <= 65536 and max_points <= 32; beyond either the call
+ * returns PV_ERR_TOO_LARGE and enqueues nothing.  The table is always the
+ * hashed kind, with at most 2^17 slots.
+ *
+ * The first call on a device sets that device up: it looks up the array's
+ * device address, sets the kernel's shared-memory attribute and enqueues
+ * one memset of the array on `stream`.  Make that first call before any
+ * stream capture.  Every call on every stream of a device shares the one
+ * array, which keeps the state the last call left (the kernel empties its
+ * table and rearms its control block before it ends), so calls must not
+ * overlap on the GPU: calls on one stream are safe, calls on different
+ * streams race unless the caller orders them.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ */
+int pv_voxelize_static(const float* points, int64_t num_points, const float point_cloud_range[6],
+                       const float voxel_size[3], int max_points, int max_voxels, float* out_voxels,
+                       int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels,
+                       pv_stream_t stream);
 
 /* Grid extents for a range and a cell size: PV_OK, PV_ERR_INVALID or
  * PV_ERR_UNSUPPORTED, with grid_out = {grid_x, grid_y, grid_z}. */

@@ -26,10 +26,11 @@ STATUS = {
     -5: "PV_ERR_CAPACITY",
     -6: "PV_ERR_TIMEOUT",
     -7: "PV_ERR_INTERNAL",
+    -8: "PV_ERR_TOO_LARGE",
 }
 
 EXPORTS = (
-    "pv_voxelize", "pv_voxelize_ex", "pv_voxelize_host", "pv_grid_size", "pv_query_plan",
+    "pv_voxelize", "pv_voxelize_ex", "pv_voxelize_host", "pv_voxelize_static", "pv_grid_size", "pv_query_plan",
     "pv_release_workspace", "pv_status_string", "pv_version",
 )
 
@@ -85,6 +86,8 @@ def load(path: Optional[str] = None):
         lib.pv_voxelize_ex.restype = ci
         lib.pv_voxelize_host.argtypes = dev_args + [vp]
         lib.pv_voxelize_host.restype = ci
+        lib.pv_voxelize_static.argtypes = dev_args + [vp]
+        lib.pv_voxelize_static.restype = ci
         lib.pv_grid_size.argtypes = [f, f, ctypes.POINTER(ctypes.c_int64)]
         lib.pv_grid_size.restype = ci
         lib.pv_query_plan.argtypes = [i64, f, f, ci, ci, ctypes.POINTER(Options), ctypes.POINTER(Plan)]

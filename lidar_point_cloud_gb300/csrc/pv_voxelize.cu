@@ -1063,6 +1063,125 @@ int voxelize_impl(const float* points, int64_t N, const float range[6], const fl
   return launch(ws, pl, points, N, range, vsize, K, M, out_voxels, out_coords, out_counts, out_num, stream);
 }
 
+// ------------------------------------------------------------ allocation-free variant
+
+// pv_voxelize_static keeps all of its scratch in one file-scope device array
+// instead of the per-stream workspace, for callers that must not allocate
+// device memory.  Limits: num_points <= kStaticMaxPoints and max_points <=
+// kStaticMaxK; the table is always hashed, with at most 2^kStaticTableLog2
+// slots.  Layout (256-byte aligned regions): control block, per-block
+// counts, hashed keys, slot lists, then four per-point arrays.
+constexpr int64_t kStaticMaxPoints = 65536;
+constexpr int kStaticMaxK = 32;
+constexpr int kStaticTableLog2 = 17;
+constexpr size_t kStaticSlots = size_t(1) << kStaticTableLog2;
+constexpr size_t kStaticOffCounts = 256;
+constexpr size_t kStaticOffKeys = kStaticOffCounts + 4 * kMaxCtas;
+constexpr size_t kStaticOffLists = kStaticOffKeys + 4 * kStaticSlots;
+constexpr size_t kStaticListWords = kStaticSlots * kStaticMaxK;
+constexpr size_t kStaticOffPoints = kStaticOffLists + 4 * kStaticListWords;
+constexpr size_t kStaticBytes = kStaticOffPoints + 4 * 4 * static_cast<size_t>(kStaticMaxPoints);
+static_assert(sizeof(Control) <= kStaticOffCounts, "control block fits its region");
+static_assert(kStaticOffKeys % 256 == 0 && kStaticOffLists % 256 == 0 && kStaticOffPoints % 256 == 0,
+              "regions stay 256-byte aligned");
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
+
+// Per-device set-up state; fixed size, so no call allocates host memory either.
+constexpr int kStaticMaxDevices = 64;
+struct StaticDevice {
+  bool ready = false;
+  unsigned char* base = nullptr;  // device address of g_static_scratch on this device
+  DeviceInfo info;
+};
+std::mutex g_static_mu;
+StaticDevice g_static_dev[kStaticMaxDevices];
+
+// Once per device, with that device current: look up the array's device
+// address (the host-side symbol is only a stand-in), prepare the kernel's
+// attributes, and put the array in its initial state on `stream` (control
+// block and counts zero, table empty).
+int static_setup(int dev, pv_stream_t stream, StaticDevice** out) {
+  if (dev < 0 || dev >= kStaticMaxDevices) return PV_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  StaticDevice& sd = g_static_dev[dev];
+  if (!sd.ready) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return PV_ERR_CUDA;
+    }
+    DeviceInfo d;
+    int coop = 0;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(pv_voxelize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.blocks_per_sm, pv_voxelize_kernel, kThreads, kDynSmem) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return PV_ERR_CUDA;
+    }
+    d.cooperative = coop != 0;
+    if (d.blocks_per_sm < 1 || !d.cooperative) return PV_ERR_CUDA;
+    unsigned char* base = static_cast<unsigned char*>(ptr);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(base, 0, kStaticOffKeys, s) != cudaSuccess ||
+        cudaMemsetAsync(base + kStaticOffKeys, 0xFF, kStaticOffPoints - kStaticOffKeys, s) != cudaSuccess) {
+      cudaGetLastError();
+      return PV_ERR_CUDA;
+    }
+    sd.base = base;
+    sd.info = d;
+    sd.ready = true;
+  }
+  *out = &sd;
+  return PV_OK;
+}
+
+int voxelize_static_impl(const float* points, int64_t N, const float range[6], const float vsize[3], int K, int M,
+                         float* out_voxels, int32_t* out_coords, int32_t* out_counts, int32_t* out_num,
+                         pv_stream_t stream) {
+  if (!range || !vsize) return PV_ERR_INVALID;
+  if (!out_voxels || !out_coords || !out_counts || !out_num) return PV_ERR_INVALID;
+  if (N > 0 && !points) return PV_ERR_INVALID;
+  if (N > kStaticMaxPoints || K > kStaticMaxK) return PV_ERR_TOO_LARGE;
+  if (!aligned(out_voxels, 16) || !aligned(out_coords, 4) || !aligned(out_counts, 4) || !aligned(out_num, 4))
+    return PV_ERR_INVALID;
+  if (N > 0 && !aligned(points, 16)) return PV_ERR_INVALID;
+  const int dev = device_of(out_voxels);
+  if (dev < 0) return PV_ERR_INVALID;
+  if (device_of(out_coords) != dev || device_of(out_counts) != dev || device_of(out_num) != dev)
+    return PV_ERR_INVALID;
+  if (N > 0 && device_of(points) != dev) return PV_ERR_INVALID;
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return PV_ERR_CUDA;
+  StaticDevice* sd = nullptr;
+  int st = static_setup(dev, stream, &sd);
+  if (st != PV_OK) return st;
+  pv_options opt{};
+  opt.table_mode = 2;  // hashed: the static table has a fixed number of slots
+  Plan pl;
+  if ((st = make_plan(N, range, vsize, K, M, &opt, sd->info, &pl)) != PV_OK) return st;
+  if (pl.T > static_cast<int64_t>(kStaticSlots) || pl.list_words > kStaticListWords) return PV_ERR_TOO_LARGE;
+  // A stack view of the array in the workspace's shape; nothing is allocated.
+  Workspace view;
+  view.device = dev;
+  view.ctl = reinterpret_cast<Control*>(sd->base);
+  view.counts = reinterpret_cast<unsigned int*>(sd->base + kStaticOffCounts);
+  view.keys = reinterpret_cast<int32_t*>(sd->base + kStaticOffKeys);
+  view.key_words_cap = kStaticSlots;
+  view.lists = reinterpret_cast<uint32_t*>(sd->base + kStaticOffLists);
+  view.list_words_cap = kStaticListWords;
+  int32_t* pts = reinterpret_cast<int32_t*>(sd->base + kStaticOffPoints);
+  view.slot_of_point = pts;
+  view.firsts = pts + kStaticMaxPoints;
+  view.tile_buf = pts + 2 * kStaticMaxPoints;
+  view.grp_info = pts + 3 * kStaticMaxPoints;
+  view.points_cap = kStaticMaxPoints;
+  return launch(&view, pl, points, N, range, vsize, K, M, out_voxels, out_coords, out_counts, out_num, stream);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------ C ABI
@@ -1203,8 +1322,16 @@ const char* pv_status_string(int status) {
     case PV_ERR_CAPACITY: return "PV_ERR_CAPACITY: pillar table full";
     case PV_ERR_TIMEOUT: return "PV_ERR_TIMEOUT: a bounded device wait gave up";
     case PV_ERR_INTERNAL: return "PV_ERR_INTERNAL: device consistency check failed";
+    case PV_ERR_TOO_LARGE: return "PV_ERR_TOO_LARGE: beyond the limits of the allocation-free entry point";
     default: return status >= 0 ? "pillar count" : "unknown status";
   }
+}
+
+int pv_voxelize_static(const float* points, int64_t num_points, const float point_cloud_range[6],
+                       const float voxel_size[3], int max_points, int max_voxels, float* out_voxels,
+                       int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels, pv_stream_t stream) {
+  return voxelize_static_impl(points, num_points, point_cloud_range, voxel_size, max_points, max_voxels,
+                              out_voxels, out_coords, out_counts, out_num_voxels, stream);
 }
 
 const char* pv_version(void) { return "0.1.0"; }
