@@ -80,7 +80,7 @@ typedef enum pv_status {
  *
  *   points          device, [num_points, 4] float32 row-major (x, y, z, intensity),
  *                   16-byte aligned; may be NULL when num_points == 0.  Read only.
- *   num_points      0 <= num_points < 2^31 - 1.
+ *   num_points      0 <= num_points < 2^29.
  *   point_cloud_range  host, {x_min, y_min, z_min, x_max, y_max, z_max}.
  *   voxel_size      host, {v_x, v_y, v_z}, finite and > 0.
  *   max_points      points kept per pillar, 1..PV_MAX_POINTS_LIMIT (PointPillars: 32).
@@ -152,13 +152,13 @@ int pv_voxelize_host(const float* points_host, int64_t num_points, const float p
  * real-time pipelines that forbid allocation after start-up.  It takes the
  * same arguments and gives the same result as pv_voxelize, but its scratch
  * (table, per-point arrays, control block) lives in one fixed array of
- * about 17.5 MiB of device memory, declared in the library at file scope:
+ * 17,830,144 bytes (about 17 MiB) of device memory, declared in the library at file scope:
  * every GPU that loads the library holds it until the process exits.  The
  * caller still owns and passes the input and the outputs.
  *
- * Limits: num_points <= 65536 and max_points <= 32; beyond either the call
+ * Limits: num_points <= 32768 and max_points <= 32; beyond either the call
  * returns PV_ERR_TOO_LARGE and enqueues nothing.  The table is always the
- * hashed kind, with at most 2^17 slots.
+ * hashed kind, with at most 2^16 slots.
  *
  * The first call on a device sets that device up: it looks up the array's
  * device address, sets the kernel's shared-memory attribute and enqueues

@@ -58,13 +58,16 @@
 
 namespace {
 
-constexpr uint32_t kEmpty = 0xFFFFFFFFu;   // empty list entry (also an all-0xFF memset)
+constexpr uint32_t kEmpty = 0xFFFFFFFFu;   // empty 32-bit marker
+constexpr unsigned long long kEmpty64 = ~0ull;  // empty list entry (also an all-0xFF memset)
+constexpr int32_t kLeaderBit = 1 << 30;    // slot_of_point: the point leads its tile group
 constexpr int32_t kNoKey = -1;             // empty hashed slot
 constexpr int kThreads = 1024;             // one block per SM
 constexpr int kWarps = kThreads / 32;
+static_assert(kWarps == 32, "warp 0 scans one value per warp");
 constexpr int kMinBlocksPerSM = 1;
 constexpr int kMaxCtas = 1024;             // blocks per launch (prefix lives in shared memory)
-constexpr int kFlagUnroll = 2;             // block-wide tiles in flight when flagging
+constexpr int kFlagUnroll = 4;             // block-wide tiles in flight when flagging
 constexpr int kEmitUnroll = 4;             // pillars in flight per warp when emitting
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded spins: 1 s
 constexpr int64_t kMaxAxisCells = int64_t(1) << 24;
@@ -85,6 +88,7 @@ struct KParams {
   long long chunk;   // points owned by each block in phase 2
   float lo_x, lo_y, lo_z;
   float v_x, v_y, v_z;
+  float r_x, r_y, r_z;   // RN(1 / v) per axis, or 0 to always divide
   float g_xf, g_yf, g_zf;
   int g_x;
   int K;             // max_points
@@ -92,15 +96,14 @@ struct KParams {
   int max_voxels;
   int hash_mode;
   unsigned int table_mask;
-  uint32_t* lists;
+  unsigned long long* lists;  // [T][KS] entries (leader index << 32) | (offset << 11) | size
   int32_t* keys;
   int32_t* slot_of_point;
   int32_t* firsts;
-  int32_t* tile_buf;     // [N] each tile's point indices, grouped by pillar
-  int32_t* grp_info;     // [N] at a group leader's index: (offset in tile << 11) | size
+  float4* tile_rows;     // [N] each tile's point rows, grouped by pillar
   unsigned int* counts;  // [kMaxCtas] first points per block
   Control* ctl;
-  size_t list_words_cap;  // whole allocation, for the dirty reset
+  size_t list_words_cap;  // whole allocation (64-bit entries), for the dirty reset
   size_t key_words_cap;
   float4* out_voxels;
   int32_t* out_coords;
@@ -148,6 +151,16 @@ __device__ __forceinline__ unsigned int lanemask_lt() {
 constexpr int kStampCtas = 4096;
 constexpr int kStamps = 8;
 __device__ unsigned long long g_phase_ns[kStampCtas][kStamps];
+__device__ unsigned long long g_p1_ns[kStampCtas][kStamps];
+__device__ unsigned long long g_insert_stats[4];  // inserts, atomics, rejected up front, max atomics
+#define PV_SUB(k)                                                            \
+  do {                                                                       \
+    if (first_tile) {                                                        \
+      __syncthreads();                                                       \
+      if (threadIdx.x == 0 && blockIdx.x < kStampCtas)                       \
+        g_p1_ns[blockIdx.x][k] = global_timer_ns();                          \
+    }                                                                        \
+  } while (0)
 #define PV_STAMP(k)                                                          \
   do {                                                                       \
     __syncthreads();                                                         \
@@ -157,6 +170,9 @@ __device__ unsigned long long g_phase_ns[kStampCtas][kStamps];
 #else
 #define PV_STAMP(k) \
   do {              \
+  } while (0)
+#define PV_SUB(k) \
+  do {            \
   } while (0)
 #endif
 
@@ -200,6 +216,8 @@ __device__ bool grid_sync(Control* ctl, unsigned int target, int* s_flag) {
 }
 
 // Exclusive prefix sum over the block; *total receives the block sum.
+// Warp shuffle scan, then warp 0 scans the kWarps warp totals; s_tmp holds
+// kWarps + 1 words.
 __device__ unsigned int block_exclusive_scan(unsigned int x, unsigned int* s_tmp, unsigned int* total) {
   const unsigned int lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   unsigned int incl = x;
@@ -210,15 +228,21 @@ __device__ unsigned int block_exclusive_scan(unsigned int x, unsigned int* s_tmp
   }
   if (lane == 31) s_tmp[warp] = incl;
   __syncthreads();
-  unsigned int before = 0, tot = 0;
+  if (warp == 0) {
+    const unsigned int w = lane < static_cast<unsigned int>(kWarps) ? s_tmp[lane] : 0u;
+    unsigned int wi = w;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const unsigned int c = s_tmp[w];
-    before += (w < static_cast<int>(warp)) ? c : 0u;
-    tot += c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= static_cast<unsigned int>(o)) wi += y;
+    }
+    if (lane < static_cast<unsigned int>(kWarps)) s_tmp[lane] = wi - w;
+    if (lane == 31) s_tmp[kWarps] = wi;
   }
   __syncthreads();
-  *total = tot;
+  const unsigned int before = s_tmp[warp];
+  *total = s_tmp[kWarps];
+  __syncthreads();  // s_tmp may be reused right after
   return before + incl - x;
 }
 
@@ -228,21 +252,43 @@ __device__ __forceinline__ bool finite_bits(float f) {
   return (__float_as_uint(f) & 0x7f800000u) != 0x7f800000u;
 }
 
-// floorf of the IEEE round-to-nearest quotient; bounds tested on the float
-// cell, so a huge or infinite quotient never reaches the integer cast.
-__device__ __forceinline__ bool bin_axis(float c, float lo, float v, float g, int* cell) {
-  const float q = floorf(__fdiv_rn(__fsub_rn(c, lo), v));
-  const bool ok = (q >= 0.0f) && (q < g);
-  *cell = ok ? static_cast<int>(q) : 0;
+// Cell of one coordinate: floorf of the IEEE round-to-nearest quotient
+// RN((c - lo) / v), bounds tested on the float cell so a huge or infinite
+// quotient never reaches the integer cast.
+//
+// The quotient is first estimated as qa = RN(d * RN(1 / v)).  Each of the two
+// roundings is within a relative 2^-24, and RN(d / v) is within a relative
+// 2^-24 of d / v, so |qa - RN(d / v)| < 1.5 * 2^-23 * qa (1 + 2^-22) < qa * 2^-22.
+// When qa is farther than qa * 2^-22 from both neighbouring integers, no
+// integer lies between qa and RN(d / v), so floorf(qa) is the exact cell;
+// otherwise the cell is taken from the correctly rounded division itself.
+// (qa - floor(qa) and floor(qa) + 1 - qa are exact for 0 <= qa < 2^24, and
+// quotients in (0, 1) floor to 0 however they round, so the filter is safe for
+// subnormal quotients too.)  A negative difference (not -0.0) has a negative
+// quotient and is outside the grid.  rcp <= 0 turns the estimate off.
+__device__ __forceinline__ bool bin_axis(float c, float lo, float v, float rcp, float g, int* cell) {
+  const float d = __fsub_rn(c, lo);
+  if (d < 0.0f) return false;
+  float f;
+  const float qa = __fmul_rn(d, rcp);
+  const float fa = floorf(qa);
+  const float tol = qa * 0x1p-22f;
+  if (rcp > 0.0f && (qa - fa) > tol && (fa + 1.0f - qa) > tol) {
+    f = fa;
+  } else {
+    f = floorf(__fdiv_rn(d, v));
+  }
+  const bool ok = (f >= 0.0f) && (f < g);
+  *cell = ok ? static_cast<int>(f) : 0;
   return ok;
 }
 
 __device__ __forceinline__ bool bin_point(const float4& q, const KParams& p, int* key) {
   if (!(finite_bits(q.x) && finite_bits(q.y) && finite_bits(q.z))) return false;
   int cx, cy, cz;
-  if (!bin_axis(q.x, p.lo_x, p.v_x, p.g_xf, &cx)) return false;
-  if (!bin_axis(q.y, p.lo_y, p.v_y, p.g_yf, &cy)) return false;
-  if (!bin_axis(q.z, p.lo_z, p.v_z, p.g_zf, &cz)) return false;
+  if (!bin_axis(q.x, p.lo_x, p.v_x, p.r_x, p.g_xf, &cx)) return false;
+  if (!bin_axis(q.y, p.lo_y, p.v_y, p.r_y, p.g_yf, &cy)) return false;
+  if (!bin_axis(q.z, p.lo_z, p.v_z, p.r_z, p.g_zf, &cz)) return false;
   *key = cy * p.g_x + cx;
   return true;
 }
@@ -275,25 +321,35 @@ __device__ __forceinline__ int claim_slot(int32_t* keys, unsigned int mask, int 
   return -1;
 }
 
-// Insert the group-leader index x into list L, which keeps the K smallest
-// leader indices of a pillar in ascending order (atomicMin cascade: each
-// entry keeps the minimum of what reaches it and passes the larger value on,
-// so entry k ends as the (k+1)-th smallest whatever order inserts arrive in).
-// Values in a list only ever decrease, so an entry read below x stays below
-// x: the cascade may start at the length of the strictly increasing run of
-// entries read below x (distinct leaders, all smaller than x), and an entry
-// K-1 read below x keeps x out altogether.
-__device__ __forceinline__ void list_insert(uint32_t* L, int K, int KS, uint32_t x) {
+// Insert entry x into list L, which keeps the K smallest entries of a pillar
+// in ascending order.  An entry is (leader index << 32) | group info, and
+// leader indices are distinct, so entries order like their leaders.  The
+// atomicMin cascade: each position keeps the minimum of what reaches it and
+// passes the larger value on, so position k ends as the (k+1)-th smallest
+// whatever order inserts arrive in.  Values in a list only ever decrease, so
+// an entry read below x stays below x: the cascade may start at the length
+// of the strictly increasing run of entries read below x (distinct leaders,
+// all smaller), and a position K-1 read below x keeps x out altogether.
+__device__ __forceinline__ unsigned long long ull_of(uint32_t lo, uint32_t hi) {
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
+__device__ __forceinline__ void list_insert(unsigned long long* L, int K, int KS, unsigned long long x) {
   const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-  const uint32_t last = __ldcg(L + (K - 1));
-  uint4 q[4];
+  const unsigned long long last = __ldcg(L + (K - 1));
+  uint4 q[4];  // 8 entries per round trip
 #pragma unroll
-  for (int t = 0; t < 4; ++t) q[t] = (4 * t < KS) ? __ldcg(reinterpret_cast<const uint4*>(L + 4 * t)) : e4;
-  if (last < x) return;
+  for (int t = 0; t < 4; ++t) q[t] = (2 * t < KS) ? __ldcg(reinterpret_cast<const uint4*>(L + 2 * t)) : e4;
+  if (last < x) {
+#ifdef PV_INSTRUMENT
+    atomicAdd(&g_insert_stats[2], 1ull);
+#endif
+    return;
+  }
   int a = 0;
-  uint32_t prev = 0;
+  unsigned long long prev = 0;
   bool run = true;
-  auto step = [&](uint32_t y) {
+  auto step = [&](unsigned long long y) {
     if (run && y < x && (a == 0 || y > prev)) {
       prev = y;
       ++a;
@@ -303,23 +359,36 @@ __device__ __forceinline__ void list_insert(uint32_t* L, int K, int KS, uint32_t
   };
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    step(q[t].x); step(q[t].y); step(q[t].z); step(q[t].w);
+    step(ull_of(q[t].x, q[t].y));
+    step(ull_of(q[t].z, q[t].w));
   }
-  for (int e = 16; run && e < K; e += 16) {
+  for (int e = 8; run && e < K; e += 8) {
 #pragma unroll
     for (int t = 0; t < 4; ++t)
-      q[t] = (e + 4 * t < KS) ? __ldcg(reinterpret_cast<const uint4*>(L + e + 4 * t)) : e4;
+      q[t] = (e + 2 * t < KS) ? __ldcg(reinterpret_cast<const uint4*>(L + e + 2 * t)) : e4;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      step(q[t].x); step(q[t].y); step(q[t].z); step(q[t].w);
+      step(ull_of(q[t].x, q[t].y));
+      step(ull_of(q[t].z, q[t].w));
     }
   }
   // Stride padding past K reads empty, so a >= K only if K entries are below x.
+#ifdef PV_INSTRUMENT
+  unsigned long long n_atomics = 0;
+#endif
   for (int k = a; k < K; ++k) {
-    const uint32_t old = atomicMin(L + k, x);
-    if (old == kEmpty) return;
+    const unsigned long long old = atomicMin(L + k, x);
+#ifdef PV_INSTRUMENT
+    ++n_atomics;
+#endif
+    if (old == kEmpty64) break;
     x = old > x ? old : x;
   }
+#ifdef PV_INSTRUMENT
+  atomicAdd(&g_insert_stats[0], 1ull);
+  atomicAdd(&g_insert_stats[1], n_atomics);
+  atomicMax(&g_insert_stats[3], n_atomics);
+#endif
 }
 
 // ------------------------------------------------------------ block tiles
@@ -332,27 +401,47 @@ __device__ __forceinline__ void list_insert(uint32_t* L, int K, int KS, uint32_t
 // own warp (lanes hold consecutive indices).
 constexpr int kTileHash = 2 * kThreads;
 
-// Dynamic shared memory of the kernel: the tile map.
-constexpr int kDynSmem = kTileHash * kWarps + kTileHash * 4 + kTileHash * 2 + kThreads * 2;
+// Dynamic shared memory of the kernel: two tile maps, used by alternate
+// tiles so one can be emptied while the other is filled.
+constexpr int kMapBytes = kTileHash * kWarps + kTileHash * 4 + kTileHash * 2;
+constexpr int kDynSmem = 2 * kMapBytes;
+static_assert(kMapBytes % 16 == 0, "maps stay 16-byte aligned");
 
 struct TileMap {
   unsigned int* cnt;         // [kTileHash][kWarps / 4] packed byte counters
   int* key;                  // [kTileHash], -1 = free
   unsigned short* off;       // [kTileHash] group offset in the tile layout
-  unsigned short* used;      // [kThreads] map positions claimed in this tile
-  unsigned int* nused;
+  unsigned int* layout;      // rows handed out in the tile layout
 };
+
+__device__ __forceinline__ TileMap tile_map(unsigned char* base, unsigned int* layout) {
+  TileMap m;
+  m.cnt = reinterpret_cast<unsigned int*>(base);
+  m.key = reinterpret_cast<int*>(base + kTileHash * kWarps);
+  m.off = reinterpret_cast<unsigned short*>(base + kTileHash * kWarps + kTileHash * 4);
+  m.layout = layout;
+  return m;
+}
+
+// Empty the map positions h = tid, tid + kThreads, ... (keys and counters).
+__device__ __forceinline__ void tile_clear(const TileMap& m, unsigned int tid) {
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int h = static_cast<int>(tid); h < kTileHash; h += kThreads) {
+    if (m.key[h] != -1) {
+      m.key[h] = -1;
+      uint4* row = reinterpret_cast<uint4*>(m.cnt + h * (kWarps / 4));
+#pragma unroll
+      for (int r = 0; r < kWarps / 16; ++r) row[r] = z;
+    }
+  }
+}
 
 // The warp-group leader claims (or finds) the map position of `slot`.
 __device__ __forceinline__ int tile_claim(const TileMap& m, int slot) {
   unsigned int h = mix32(static_cast<unsigned int>(slot)) & (kTileHash - 1);
   for (int probe = 0; probe < kTileHash; ++probe) {  // at most kThreads keys: never full
     const int cur = atomicCAS(m.key + h, -1, slot);
-    if (cur == -1) {
-      m.used[atomicAdd(m.nused, 1u)] = static_cast<unsigned short>(h);
-      return static_cast<int>(h);
-    }
-    if (cur == slot) return static_cast<int>(h);
+    if (cur == -1 || cur == slot) return static_cast<int>(h);
     h = (h + 1) & (kTileHash - 1);
   }
   return -1;
@@ -403,9 +492,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   extern __shared__ __align__(16) unsigned char s_dyn[];
   __shared__ unsigned int s_prefix[kMaxCtas + 1];
   __shared__ unsigned int s_tile[kFlagUnroll][kWarps];
-  __shared__ unsigned int s_tmp[kWarps];
+  __shared__ unsigned int s_tmp[kWarps + 1];
   __shared__ int s_flag;
-  __shared__ unsigned int s_nused;
+  __shared__ unsigned int s_layout[2];
 
   const unsigned int P = gridDim.x;
   const unsigned int cta = blockIdx.x;
@@ -417,6 +506,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   const long long gwarp = static_cast<long long>(cta) * kWarps + warp;
   const long long nwarps = static_cast<long long>(P) * kWarps;
   const int K = p.K;
+  const long long begin = lmin(p.n, static_cast<long long>(cta) * p.chunk);
+  const long long end = lmin(p.n, begin + p.chunk);
 
   const unsigned int epoch = ld_relaxed(&p.ctl->epoch);
   const unsigned int dirty = ld_relaxed(&p.ctl->dirty);
@@ -429,48 +520,57 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   if (dirty) {
     const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
     uint4* l4 = reinterpret_cast<uint4*>(p.lists);
-    for (size_t q = gtid; q < p.list_words_cap / 4; q += gthreads) l4[q] = e4;
+    for (size_t q = gtid; q < p.list_words_cap / 2; q += gthreads) l4[q] = e4;
     for (size_t q = gtid; q < p.key_words_cap; q += gthreads) p.keys[q] = kNoKey;
     alive = grid_sync(p.ctl, bar_target, &s_flag);
     bar_target += P;
   }
 
   // ---- phase 1: bin every point; lay each block tile out grouped by pillar
-  // (first-appearance order inside the tile), and insert one entry per
-  // (pillar, tile) group, the group's first point, into the pillar's list.
+  // (groups in any order inside the tile, points of a group in index order),
+  // and insert one entry per (pillar, tile) group, the group's first point,
+  // into the pillar's list.  Two barriers per tile: after the warp groups
+  // register in the tile map, and after the group offsets are handed out.
   if (alive) {
-    TileMap tm;
-    tm.cnt = reinterpret_cast<unsigned int*>(s_dyn);
-    tm.key = reinterpret_cast<int*>(s_dyn + kTileHash * kWarps);
-    tm.off = reinterpret_cast<unsigned short*>(s_dyn + kTileHash * kWarps + kTileHash * 4);
-    tm.used = reinterpret_cast<unsigned short*>(s_dyn + kTileHash * kWarps + kTileHash * 6);
-    tm.nused = &s_nused;
-    for (int h = static_cast<int>(tid); h < kTileHash; h += kThreads) {
-      tm.key[h] = -1;
-#pragma unroll
-      for (int w4 = 0; w4 < kWarps / 4; ++w4) tm.cnt[h * (kWarps / 4) + w4] = 0u;
-    }
-    if (tid == 0) s_nused = 0;
-
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const long long stride = static_cast<long long>(P) * kThreads;
-    long long tb = static_cast<long long>(cta) * kThreads;
-    float4 q = (tb + tid < p.n) ? __ldg(p.points + tb + tid) : z4;
-    for (; tb < p.n; tb += stride) {
+    long long tb = begin;  // this block's contiguous, tile-aligned chunk
+    float4 q = (tb + tid < end) ? __ldg(p.points + tb + tid) : z4;
+    {  // both maps empty: counters zero, keys -1 (16-byte stores)
+      uint4* d4 = reinterpret_cast<uint4*>(s_dyn);
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 m1 = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        uint4* base = d4 + m * (kMapBytes / 16);
+        for (int j = static_cast<int>(tid); j < kTileHash * kWarps / 16; j += kThreads) base[j] = z;
+        for (int j = static_cast<int>(tid); j < kTileHash * 4 / 16; j += kThreads)
+          base[kTileHash * kWarps / 16 + j] = m1;
+      }
+    }
+    if (tid == 0) s_layout[0] = s_layout[1] = 0;
+    __syncthreads();
+    int buf = 0;
+    for (; tb < end; tb += kThreads, buf ^= 1) {
+#ifdef PV_INSTRUMENT
+      const bool first_tile = tb == begin;
+#endif
+      PV_SUB(0);
+      const TileMap tm = tile_map(s_dyn + buf * kMapBytes, &s_layout[buf]);
+      const TileMap prev = tile_map(s_dyn + (buf ^ 1) * kMapBytes, &s_layout[buf ^ 1]);
       const long long i = tb + tid;
-      const long long inext = i + stride;
-      const float4 qn = inext < p.n ? __ldg(p.points + inext) : z4;  // next tile, in flight early
+      const long long inext = i + kThreads;
+      const float4 qn = inext < end ? __ldg(p.points + inext) : z4;  // next tile, in flight early
       int slot = -1;
-      if (i < p.n) {
+      if (i < end) {
         int key;
         if (bin_point(q, p, &key)) {
           slot = p.hash_mode ? claim_slot(p.keys, p.table_mask, key) : key;
           if (slot < 0) atomicMin(&p.ctl->err, PV_ERR_CAPACITY);
         }
       }
+      PV_SUB(1);
       const unsigned int peers = __match_any_sync(0xffffffffu, slot);
       const int leader = __ffs(peers) - 1;
-      __syncthreads();  // the previous tile's map is clear
       int h = -1;
       if (slot >= 0 && static_cast<int>(lane) == leader) {
         h = tile_claim(tm, slot);
@@ -483,37 +583,44 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       }
       h = __shfl_sync(0xffffffffu, h, leader);
       if (h < 0) slot = -1;
-      if (i < p.n) p.slot_of_point[i] = slot;
-      __syncthreads();  // every warp group registered
+      __syncthreads();  // (A) every warp group registered; the previous tile's map is read
+      PV_SUB(2);
+      // Empty the previous tile's map (used again by the next tile, after barrier B).
+      if (tid == 0) *prev.layout = 0;
+      tile_clear(prev, tid);
       unsigned int trank = 0, tot = 0;
       if (slot >= 0) {
         tile_counts(tm, h, warp, &trank, &tot);
         trank += __popc(peers & lanemask_lt());
       }
-      // Group offsets in the tile layout: groups in order of their first point.
-      unsigned int tile_valid;
-      const unsigned int goff = block_exclusive_scan((slot >= 0 && trank == 0) ? tot : 0u, s_tmp, &tile_valid);
-      (void)tile_valid;
-      if (slot >= 0 && trank == 0) tm.off[h] = static_cast<unsigned short>(goff);
-      const unsigned int nu = s_nused;
-      __syncthreads();  // offsets published
-      unsigned int off = 0;
-      if (slot >= 0) off = tm.off[h];
-      __syncthreads();  // every map read done: empty the map for the next tile
-      if (tid == 0) s_nused = 0;
-      for (unsigned int j = tid; j < nu; j += kThreads) {
-        const int hh = tm.used[j];
-        tm.key[hh] = -1;
+      {  // group offsets: one shared-memory atomic per warp for all its tile-group leaders
+        const bool lead = slot >= 0 && trank == 0;
+        const unsigned int need = lead ? tot : 0u;
+        unsigned int incl = need;
 #pragma unroll
-        for (int w4 = 0; w4 < kWarps / 4; ++w4) tm.cnt[hh * (kWarps / 4) + w4] = 0u;
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= static_cast<unsigned int>(o)) incl += y;
+        }
+        const unsigned int wsum = __shfl_sync(0xffffffffu, incl, 31);
+        unsigned int base = 0;
+        if (lane == 31 && wsum) base = atomicAdd(tm.layout, wsum);
+        base = __shfl_sync(0xffffffffu, base, 31);
+        if (lead) tm.off[h] = static_cast<unsigned short>(base + incl - need);
       }
+      if (i < end) p.slot_of_point[i] = slot < 0 ? -1 : (trank == 0 ? (slot | kLeaderBit) : slot);
+      __syncthreads();  // (B) group offsets handed out; the previous map is empty
+      PV_SUB(3);
       if (slot >= 0) {
-        p.tile_buf[tb + off + trank] = static_cast<int32_t>(i);
+        const unsigned int off = tm.off[h];
+        p.tile_rows[tb + off + trank] = q;
         if (trank == 0) {
-          p.grp_info[i] = static_cast<int32_t>((off << 11) | tot);
-          list_insert(p.lists + static_cast<size_t>(slot) * p.KS, K, p.KS, static_cast<uint32_t>(i));
+          const unsigned long long entry =
+              (static_cast<unsigned long long>(i) << 32) | ((off << 11) | tot);
+          list_insert(p.lists + static_cast<size_t>(slot) * p.KS, K, p.KS, entry);
         }
       }
+      PV_SUB(4);
       q = qn;
     }
     PV_STAMP(1);
@@ -521,8 +628,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   }
   PV_STAMP(2);
 
-  const long long begin = lmin(p.n, static_cast<long long>(cta) * p.chunk);
-  const long long end = lmin(p.n, begin + p.chunk);
   const unsigned int M = static_cast<unsigned int>(p.max_voxels);
   unsigned int V = 0;
 
@@ -538,8 +643,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         s[u] = i < end ? __ldcg(p.slot_of_point + i) : -1;
       }
 #pragma unroll
-      for (int u = 0; u < kFlagUnroll; ++u)
-        head[u] = s[u] >= 0 ? __ldcg(p.lists + static_cast<size_t>(s[u]) * p.KS) : kEmpty;
+      for (int u = 0; u < kFlagUnroll; ++u) {
+        // Only a tile-group leader can be its pillar's first point.
+        head[u] = (s[u] >= 0 && (s[u] & kLeaderBit))
+                      ? static_cast<uint32_t>(__ldcg(p.lists + static_cast<size_t>(s[u] & ~kLeaderBit) * p.KS) >> 32)
+                      : kEmpty;
+        s[u] = s[u] >= 0 ? (s[u] & ~kLeaderBit) : -1;
+      }
       unsigned int ball[kFlagUnroll];
 #pragma unroll
       for (int u = 0; u < kFlagUnroll; ++u) {
@@ -548,19 +658,30 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         if (lane == 0) s_tile[u][warp] = __popc(ball[u]);
       }
       __syncthreads();
+      if (warp == 0) {  // exclusive prefix over (tile u, warp) in index order
+        unsigned int carry = 0;
+#pragma unroll
+        for (int u = 0; u < kFlagUnroll; ++u) {
+          const unsigned int c = s_tile[u][lane];
+          unsigned int incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= static_cast<unsigned int>(o)) incl += y;
+          }
+          s_tile[u][lane] = carry + incl - c;
+          carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) s_tmp[kWarps] = carry;
+      }
+      __syncthreads();
       unsigned int run = local;
 #pragma unroll
       for (int u = 0; u < kFlagUnroll; ++u) {
-        unsigned int before = 0, tile = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const unsigned int c = s_tile[u][w];
-          before += (w < static_cast<int>(warp)) ? c : 0u;
-          tile += c;
-        }
-        if ((ball[u] >> lane) & 1u) p.firsts[begin + run + before + __popc(ball[u] & lanemask_lt())] = s[u];
-        run += tile;
+        if ((ball[u] >> lane) & 1u)
+          p.firsts[begin + run + s_tile[u][warp] + __popc(ball[u] & lanemask_lt())] = s[u];
       }
+      run += s_tmp[kWarps];
       local = run;
       __syncthreads();
     }
@@ -582,41 +703,58 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     V = total < M ? total : M;
     PV_STAMP(4);
 
-    // ---- phase 2c: output rows, ranks spread over every warp of the grid.
-    // A pillar's points are its groups, concatenated in list order: lane g
-    // holds group g (leader index, tile offset, size); output position e
-    // belongs to the last group whose running start is <= e.
+    // ---- phase 2c: output rows.  Every warp of the grid takes a contiguous
+    // range of ranks (so its output rows are contiguous), kEmitUnroll at a
+    // time.  A pillar's points are its groups, concatenated in list order:
+    // lane g holds group g (leader index, tile offset, size); output position
+    // e belongs to the last group whose running start is <= e.
     bool stale = false;
-    for (long long r0 = gwarp; r0 < V; r0 += kEmitUnroll * nwarps) {
+    const long long per_warp = (static_cast<long long>(V) + nwarps - 1) / nwarps;
+    const long long rw0 = gwarp * per_warp;
+    const long long rw1 = rw0 + per_warp < static_cast<long long>(V) ? rw0 + per_warp : static_cast<long long>(V);
+    unsigned int owner = 0;  // block whose first points hold rank rw0 (binary search once)
+    if (rw0 < rw1) {
+      unsigned int lo = 0, hi = P;  // s_prefix[lo] <= rw0 < s_prefix[hi]
+      while (hi - lo > 1) {
+        const unsigned int mid = (lo + hi) >> 1;
+        if (s_prefix[mid] <= static_cast<unsigned int>(rw0)) lo = mid; else hi = mid;
+      }
+      owner = lo;
+    }
+    for (long long r0 = rw0; r0 < rw1; r0 += kEmitUnroll) {
       int slot[kEmitUnroll];
       bool ok[kEmitUnroll];
 #pragma unroll
       for (int u = 0; u < kEmitUnroll; ++u) {
-        const long long r = r0 + u * nwarps;
-        ok[u] = r < V;
-        slot[u] = ok[u] ? slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r)) : 0;
+        const long long r = r0 + u;
+        ok[u] = r < rw1;
+        slot[u] = 0;
+        if (ok[u]) {
+          while (s_prefix[owner + 1] <= static_cast<unsigned int>(r)) ++owner;  // ranks ascend
+          slot[u] = __ldcg(p.firsts + static_cast<long long>(owner) * p.chunk + (r - s_prefix[owner]));
+        }
       }
-      // Group descriptors: leader (list entry), then its (offset, size).
+      // Group descriptors: one list entry per lane (leader index, offset, size).
       uint32_t lead[kEmitUnroll];
-#pragma unroll
-      for (int u = 0; u < kEmitUnroll; ++u)
-        lead[u] = (ok[u] && static_cast<int>(lane) < K) ? __ldcg(p.lists + static_cast<size_t>(slot[u]) * p.KS + lane)
-                                                        : kEmpty;
       uint32_t ginfo[kEmitUnroll];
 #pragma unroll
       for (int u = 0; u < kEmitUnroll; ++u) {
+        const unsigned long long ent = (ok[u] && static_cast<int>(lane) < K)
+                                           ? __ldcg(p.lists + static_cast<size_t>(slot[u]) * p.KS + lane)
+                                           : kEmpty64;
+        lead[u] = static_cast<uint32_t>(ent >> 32);
+        ginfo[u] = static_cast<uint32_t>(ent);
         if (lead[u] != kEmpty && static_cast<long long>(lead[u]) >= p.n) {  // never in a clean table
           lead[u] = kEmpty;
           stale = true;
         }
-        ginfo[u] = lead[u] != kEmpty ? static_cast<uint32_t>(__ldcg(p.grp_info + lead[u])) : 0u;
       }
       unsigned int cnt[kEmitUnroll];
       int gstart[kEmitUnroll];
 #pragma unroll
       for (int u = 0; u < kEmitUnroll; ++u) {
         // Inclusive scan of group sizes over the lanes (groups), capped at K.
-        const unsigned int size = ginfo[u] & 2047u;
+        const unsigned int size = lead[u] != kEmpty ? (ginfo[u] & 2047u) : 0u;
         unsigned int incl = size;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -629,52 +767,44 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       }
       for (int e0 = 0; e0 < K; e0 += 32) {
         const int e = e0 + static_cast<int>(lane);
-        int32_t idx[kEmitUnroll];
+        float4 row[kEmitUnroll];
 #pragma unroll
         for (int u = 0; u < kEmitUnroll; ++u) {
-          idx[u] = -1;
           // Group of position e: the last valid group whose start is <= e
           // (valid groups fill lanes 0 .. G-1 with strictly increasing starts).
           const int G = __popc(__ballot_sync(0xffffffffu, lead[u] != kEmpty));
           int g = G > 0 ? 0 : -1;
+          if (G > 1) {  // warp-uniform: most pillars have a single group
 #pragma unroll
-          for (int step = 16; step >= 1; step >>= 1) {
-            const int j = g + step;
-            const int st = __shfl_sync(0xffffffffu, gstart[u], j < 32 ? j : 31);
-            if (g >= 0 && j < G && st <= e) g = j;
+            for (int step = 16; step >= 1; step >>= 1) {
+              const int j = g + step;
+              const int st = __shfl_sync(0xffffffffu, gstart[u], j < 32 ? j : 31);
+              if (j < G && st <= e) g = j;
+            }
           }
           const int gsafe = g < 0 ? 0 : g;
           const uint32_t gl_lead = __shfl_sync(0xffffffffu, lead[u], gsafe);
           const uint32_t gl_info = __shfl_sync(0xffffffffu, ginfo[u], gsafe);
           const int gl_start = __shfl_sync(0xffffffffu, gstart[u], gsafe);
+          row[u] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (ok[u] && e < K && g >= 0 && static_cast<unsigned int>(e) < cnt[u]) {
             const long long tbase = static_cast<long long>(gl_lead) & ~static_cast<long long>(kThreads - 1);
-            idx[u] = __ldcg(p.tile_buf + tbase + (gl_info >> 11) + (e - gl_start));
+            row[u] = __ldcg(p.tile_rows + tbase + (gl_info >> 11) + (e - gl_start));
           }
-        }
-        float4 row[kEmitUnroll];
-#pragma unroll
-        for (int u = 0; u < kEmitUnroll; ++u) {
-          bool has = idx[u] >= 0;
-          if (has && static_cast<long long>(idx[u]) >= p.n) {
-            has = false;
-            stale = true;
-          }
-          row[u] = has ? __ldg(p.points + idx[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < kEmitUnroll; ++u) {
           if (ok[u] && e < K) {
-            const long long r = r0 + u * nwarps;
+            const long long r = r0 + u;
             p.out_voxels[static_cast<size_t>(r) * K + e] = row[u];
-            p.lists[static_cast<size_t>(slot[u]) * p.KS + e] = kEmpty;
+            p.lists[static_cast<size_t>(slot[u]) * p.KS + e] = kEmpty64;
           }
         }
       }
 #pragma unroll
       for (int u = 0; u < kEmitUnroll; ++u) {
         if (ok[u] && lane == 0) {
-          const size_t r = static_cast<size_t>(r0 + u * nwarps);
+          const size_t r = static_cast<size_t>(r0 + u);
           const int key = p.hash_mode ? __ldcg(p.keys + slot[u]) : slot[u];
           p.out_coords[3 * r + 0] = 0;
           p.out_coords[3 * r + 1] = key / p.g_x;
@@ -694,8 +824,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       for (int t = 0; t < 32; ++t) {
         const int s = __shfl_sync(0xffffffffu, mine, t);
         if (s < 0) break;  // ranks ascend with t, so the rest are past the end too
-        uint32_t* L = p.lists + static_cast<size_t>(s) * p.KS;
-        for (int e = static_cast<int>(lane); e < K; e += 32) L[e] = kEmpty;
+        unsigned long long* L = p.lists + static_cast<size_t>(s) * p.KS;
+        for (int e = static_cast<int>(lane); e < K; e += 32) L[e] = kEmpty64;
         if (p.hash_mode && lane == 0) p.keys[s] = kNoKey;
       }
     }
@@ -748,10 +878,9 @@ struct Workspace {
   unsigned int* counts = nullptr;  // [kMaxCtas]
   int32_t* slot_of_point = nullptr;
   int32_t* firsts = nullptr;
-  int32_t* tile_buf = nullptr;
-  int32_t* grp_info = nullptr;
+  float4* tile_rows = nullptr;
   size_t points_cap = 0;
-  uint32_t* lists = nullptr;
+  unsigned long long* lists = nullptr;  // 64-bit entries
   size_t list_words_cap = 0;
   int32_t* keys = nullptr;
   size_t key_words_cap = 0;
@@ -826,7 +955,7 @@ int device_info(int dev, DeviceInfo* out) {
 
 int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int M, const pv_options* opt,
               const DeviceInfo& dev, Plan* pl) {
-  if (N < 0 || N >= (int64_t(1) << 31) - 1) return PV_ERR_INVALID;
+  if (N < 0 || N >= (int64_t(1) << 29)) return PV_ERR_INVALID;
   if (K < 1 || K > PV_MAX_POINTS_LIMIT || M < 1) return PV_ERR_INVALID;
   if (static_cast<int64_t>(K) * M >= (int64_t(1) << 31)) return PV_ERR_INVALID;
   int st = grid_extents(range, vsize, pl->g);
@@ -839,7 +968,7 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   const int64_t distinct_bound = std::max<int64_t>(1, std::min(N, cells));
   const int64_t hashed_T = next_pow2(std::max<int64_t>(2 * distinct_bound, 1024));
   pl->KS = (K + 3) & ~3;
-  const int64_t direct_bytes = cells * pl->KS * 4;
+  const int64_t direct_bytes = cells * pl->KS * 8;
   int mode = o.table_mode;
   if (mode == 0) mode = (cells <= 2 * hashed_T && direct_bytes <= (int64_t(1) << 31)) ? 1 : 2;
   pl->mode = mode;
@@ -848,16 +977,18 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
     pl->mask = 0;
   } else {
     pl->T = o.table_log2 ? (int64_t(1) << std::max(2, o.table_log2)) : hashed_T;
-    if (pl->T > (int64_t(1) << 31)) return PV_ERR_INVALID;
+    if (pl->T > (int64_t(1) << 30)) return PV_ERR_INVALID;  // slots stay below the leader bit
     pl->mask = static_cast<unsigned int>(pl->T - 1);
   }
   pl->list_words = static_cast<size_t>(pl->T) * pl->KS;
   pl->key_words = mode == 2 ? static_cast<size_t>(pl->T) : 0;
   const int per_sm = o.ctas_per_sm ? std::min(o.ctas_per_sm, dev.blocks_per_sm) : dev.blocks_per_sm;
   pl->ctas = std::min(kMaxCtas, std::max(1, dev.sms * per_sm));
-  pl->chunk = (N + pl->ctas - 1) / pl->ctas;
-  pl->bytes = sizeof(Control) + 4 * static_cast<size_t>(kMaxCtas) + 16 * static_cast<size_t>(N) +
-              4 * (pl->list_words + pl->key_words);
+  // Contiguous, tile-aligned chunks: phase 1 and phase 2 share them.
+  const int64_t tiles = (N + kThreads - 1) / kThreads;
+  pl->chunk = ((tiles + pl->ctas - 1) / pl->ctas) * kThreads;
+  pl->bytes = sizeof(Control) + 4 * static_cast<size_t>(kMaxCtas) + 24 * static_cast<size_t>(N) +
+              8 * pl->list_words + 4 * pl->key_words;
   return PV_OK;
 }
 
@@ -933,14 +1064,13 @@ int reserve(Workspace* ws, const Plan& pl, int64_t N, pv_stream_t stream) {
   const size_t np = round_up(static_cast<size_t>(std::max<int64_t>(N, 1)), 65536);
   if (ws->points_cap < np) {
     const size_t want = std::max(np, ws->points_cap + ws->points_cap / 2);
-    size_t cap_a = ws->points_cap, cap_b = ws->points_cap, cap_c = ws->points_cap, cap_d = ws->points_cap;
+    size_t cap_a = ws->points_cap, cap_b = ws->points_cap, cap_c = ws->points_cap;
     if ((st = grow(&ws->slot_of_point, &cap_a, want, 0, stream, &synced)) != PV_OK) return st;
     if ((st = grow(&ws->firsts, &cap_b, want, 0, stream, &synced)) != PV_OK) return st;
-    if ((st = grow(&ws->tile_buf, &cap_c, want, 0, stream, &synced)) != PV_OK) return st;
-    if ((st = grow(&ws->grp_info, &cap_d, want, 0, stream, &synced)) != PV_OK) return st;
+    if ((st = grow(&ws->tile_rows, &cap_c, want, 0, stream, &synced)) != PV_OK) return st;
     ws->points_cap = want;
   }
-  if ((st = grow(&ws->lists, &ws->list_words_cap, round_up(pl.list_words, 4), 0xFF, stream, &synced)) != PV_OK)
+  if ((st = grow(&ws->lists, &ws->list_words_cap, round_up(pl.list_words, 2), 0xFF, stream, &synced)) != PV_OK)
     return st;
   if (pl.key_words &&
       (st = grow(&ws->keys, &ws->key_words_cap, pl.key_words, 0xFF, stream, &synced)) != PV_OK)
@@ -994,6 +1124,11 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.v_x = vsize[0];
   kp.v_y = vsize[1];
   kp.v_z = vsize[2];
+  // Reciprocal estimates for the binning filter; only normal, finite values are used.
+  const float rx = 1.0f / vsize[0], ry = 1.0f / vsize[1], rz = 1.0f / vsize[2];
+  kp.r_x = std::isnormal(rx) ? rx : 0.0f;
+  kp.r_y = std::isnormal(ry) ? ry : 0.0f;
+  kp.r_z = std::isnormal(rz) ? rz : 0.0f;
   kp.g_xf = static_cast<float>(pl.g[0]);
   kp.g_yf = static_cast<float>(pl.g[1]);
   kp.g_zf = static_cast<float>(pl.g[2]);
@@ -1007,8 +1142,7 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.keys = ws->keys;
   kp.slot_of_point = ws->slot_of_point;
   kp.firsts = ws->firsts;
-  kp.tile_buf = ws->tile_buf;
-  kp.grp_info = ws->grp_info;
+  kp.tile_rows = ws->tile_rows;
   kp.counts = ws->counts;
   kp.ctl = ws->ctl;
   kp.list_words_cap = ws->list_words_cap;
@@ -1071,18 +1205,20 @@ int voxelize_impl(const float* points, int64_t N, const float range[6], const fl
 // kStaticMaxK; the table is always hashed, with at most 2^kStaticTableLog2
 // slots.  Layout (256-byte aligned regions): control block, per-block
 // counts, hashed keys, slot lists, then four per-point arrays.
-constexpr int64_t kStaticMaxPoints = 65536;
+constexpr int64_t kStaticMaxPoints = 32768;
 constexpr int kStaticMaxK = 32;
-constexpr int kStaticTableLog2 = 17;
+constexpr int kStaticTableLog2 = 16;
 constexpr size_t kStaticSlots = size_t(1) << kStaticTableLog2;
 constexpr size_t kStaticOffCounts = 256;
 constexpr size_t kStaticOffKeys = kStaticOffCounts + 4 * kMaxCtas;
 constexpr size_t kStaticOffLists = kStaticOffKeys + 4 * kStaticSlots;
-constexpr size_t kStaticListWords = kStaticSlots * kStaticMaxK;
-constexpr size_t kStaticOffPoints = kStaticOffLists + 4 * kStaticListWords;
-constexpr size_t kStaticBytes = kStaticOffPoints + 4 * 4 * static_cast<size_t>(kStaticMaxPoints);
+constexpr size_t kStaticListWords = kStaticSlots * kStaticMaxK;  // 64-bit entries
+constexpr size_t kStaticOffRows = kStaticOffLists + 8 * kStaticListWords;
+constexpr size_t kStaticOffPoints = kStaticOffRows + 16 * static_cast<size_t>(kStaticMaxPoints);
+constexpr size_t kStaticBytes = kStaticOffPoints + 2 * 4 * static_cast<size_t>(kStaticMaxPoints);
 static_assert(sizeof(Control) <= kStaticOffCounts, "control block fits its region");
-static_assert(kStaticOffKeys % 256 == 0 && kStaticOffLists % 256 == 0 && kStaticOffPoints % 256 == 0,
+static_assert(kStaticOffKeys % 256 == 0 && kStaticOffLists % 256 == 0 && kStaticOffRows % 256 == 0 &&
+                  kStaticOffPoints % 256 == 0,
               "regions stay 256-byte aligned");
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
@@ -1127,7 +1263,7 @@ int static_setup(int dev, pv_stream_t stream, StaticDevice** out) {
     unsigned char* base = static_cast<unsigned char*>(ptr);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(base, 0, kStaticOffKeys, s) != cudaSuccess ||
-        cudaMemsetAsync(base + kStaticOffKeys, 0xFF, kStaticOffPoints - kStaticOffKeys, s) != cudaSuccess) {
+        cudaMemsetAsync(base + kStaticOffKeys, 0xFF, kStaticOffRows - kStaticOffKeys, s) != cudaSuccess) {
       cudaGetLastError();
       return PV_ERR_CUDA;
     }
@@ -1171,13 +1307,12 @@ int voxelize_static_impl(const float* points, int64_t N, const float range[6], c
   view.counts = reinterpret_cast<unsigned int*>(sd->base + kStaticOffCounts);
   view.keys = reinterpret_cast<int32_t*>(sd->base + kStaticOffKeys);
   view.key_words_cap = kStaticSlots;
-  view.lists = reinterpret_cast<uint32_t*>(sd->base + kStaticOffLists);
+  view.lists = reinterpret_cast<unsigned long long*>(sd->base + kStaticOffLists);
   view.list_words_cap = kStaticListWords;
+  view.tile_rows = reinterpret_cast<float4*>(sd->base + kStaticOffRows);
   int32_t* pts = reinterpret_cast<int32_t*>(sd->base + kStaticOffPoints);
   view.slot_of_point = pts;
   view.firsts = pts + kStaticMaxPoints;
-  view.tile_buf = pts + 2 * kStaticMaxPoints;
-  view.grp_info = pts + 3 * kStaticMaxPoints;
   view.points_cap = kStaticMaxPoints;
   return launch(&view, pl, points, N, range, vsize, K, M, out_voxels, out_coords, out_counts, out_num, stream);
 }
@@ -1301,8 +1436,7 @@ int pv_release_workspace(void) {
     cudaFree(ws->counts);
     cudaFree(ws->slot_of_point);
     cudaFree(ws->firsts);
-    cudaFree(ws->tile_buf);
-    cudaFree(ws->grp_info);
+    cudaFree(ws->tile_rows);
     cudaFree(ws->lists);
     cudaFree(ws->keys);
     cudaFree(ws->staging);
@@ -1337,6 +1471,22 @@ int pv_voxelize_static(const float* points, int64_t num_points, const float poin
 const char* pv_version(void) { return "0.1.0"; }
 
 #ifdef PV_INSTRUMENT
+// Instrumented builds only: copies and clears the list-insert statistics.
+int pv_debug_insert_stats(unsigned long long* out) {
+  if (cudaMemcpyFromSymbol(out, g_insert_stats, sizeof(unsigned long long) * 4) != cudaSuccess) return PV_ERR_CUDA;
+  static const unsigned long long zeros[4] = {};
+  if (cudaMemcpyToSymbol(g_insert_stats, zeros, sizeof zeros) != cudaSuccess) return PV_ERR_CUDA;
+  return PV_OK;
+}
+
+// Instrumented builds only: copies [max_ctas][8] phase-1 first-tile stamps (ns) to host.
+int pv_debug_p1_times(unsigned long long* out, int max_ctas) {
+  const int n = max_ctas < kStampCtas ? max_ctas : kStampCtas;
+  if (cudaMemcpyFromSymbol(out, g_p1_ns, sizeof(unsigned long long) * kStamps * n) != cudaSuccess)
+    return PV_ERR_CUDA;
+  return PV_OK;
+}
+
 // Instrumented builds only: copies [max_ctas][8] phase stamps (ns) to host.
 int pv_debug_phase_times(unsigned long long* out, int max_ctas) {
   const int n = max_ctas < kStampCtas ? max_ctas : kStampCtas;

@@ -52,7 +52,7 @@ def test_static_entry_point_matches_twice_in_a_row():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     tiny, p_tiny = synth.make("tiny")
-    cloud = synth.uniform(50_000, 21)
+    cloud = synth.uniform(30_000, 21)
     runs = [(tiny, p_tiny), (cloud, synth.KITTI_PARAMS), (cloud, synth.KITTI_PARAMS)]
     static_out = []
     for pts, P in runs:  # back-to-back calls sharing the one scratch array
@@ -69,7 +69,7 @@ def test_static_entry_point_matches_twice_in_a_row():
 def test_static_entry_point_rejects_sizes_beyond_its_limits():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    pts = synth.uniform(65_537, 22)
+    pts = synth.uniform(32_769, 22)
     st, _ = _call("pv_voxelize_static", pts, synth.KITTI_PARAMS)
     assert st == PV_ERR_TOO_LARGE
     st, _ = _call("pv_voxelize_static", pts[:1000], synth.KITTI_PARAMS, K=33)
