@@ -62,10 +62,13 @@ constexpr uint32_t kEmpty = 0xFFFFFFFFu;   // empty 32-bit marker
 constexpr unsigned long long kEmpty64 = ~0ull;  // empty list entry (also an all-0xFF memset)
 constexpr int32_t kLeaderBit = 1 << 30;    // slot_of_point: the point leads its tile group
 constexpr int32_t kNoKey = -1;             // empty hashed slot
-constexpr int kThreads = 1024;             // one block per SM
+#ifndef PV_BLOCK_THREADS
+#define PV_BLOCK_THREADS 1024
+#endif
+constexpr int kThreads = PV_BLOCK_THREADS;  // also the tile: points grouped together in shared memory
 constexpr int kWarps = kThreads / 32;
-static_assert(kWarps == 32, "warp 0 scans one value per warp");
-constexpr int kMinBlocksPerSM = 1;
+static_assert(kWarps <= 32 && kWarps % 16 == 0, "warp 0 scans one value per warp; 16-byte counter rows");
+constexpr int kMinBlocksPerSM = 1024 / kThreads;
 constexpr int kMaxCtas = 1024;             // blocks per launch (prefix lives in shared memory)
 constexpr int kFlagUnroll = 4;             // block-wide tiles in flight when flagging
 constexpr int kEmitUnroll = 4;             // pillars in flight per warp when emitting
@@ -101,6 +104,7 @@ struct KParams {
   int32_t* slot_of_point;
   int32_t* firsts;
   float4* tile_rows;     // [N] each tile's point rows, grouped by pillar
+  unsigned long long* recs;  // [N] phase 1a records of a block's groups (the block's chunk region)
   unsigned int* counts;  // [kMaxCtas] first points per block
   Control* ctl;
   size_t list_words_cap;  // whole allocation (64-bit entries), for the dirty reset
@@ -326,22 +330,28 @@ __device__ __forceinline__ int claim_slot(int32_t* keys, unsigned int mask, int 
 // leader indices are distinct, so entries order like their leaders.  The
 // atomicMin cascade: each position keeps the minimum of what reaches it and
 // passes the larger value on, so position k ends as the (k+1)-th smallest
-// whatever order inserts arrive in.  Values in a list only ever decrease, so
-// an entry read below x stays below x: the cascade may start at the length
-// of the strictly increasing run of entries read below x (distinct leaders,
-// all smaller), and a position K-1 read below x keeps x out altogether.
+// whatever order inserts arrive in.  An entry may enter the cascade at any
+// position that does not exceed its final rank: the positions it skips would
+// have kept a smaller entry and passed it on unchanged.  The bound used is
+// crank (the number of this chunk's groups of the pillar before x, exact)
+// plus the length of the strictly increasing run of entries read below x
+// that come from other chunks (leaders outside [cbase, cbase + cspan)):
+// distinct smaller leaders, none counted twice.  Values in a list only ever
+// decrease, so an entry read below x stays below x, and a position K-1 read
+// below x keeps x out altogether.
 __device__ __forceinline__ unsigned long long ull_of(uint32_t lo, uint32_t hi) {
   return (static_cast<unsigned long long>(hi) << 32) | lo;
 }
 
-__device__ __forceinline__ void list_insert(unsigned long long* L, int K, int KS, unsigned long long x) {
+__device__ __forceinline__ void list_insert(unsigned long long* L, int K, int KS, unsigned long long x,
+                                            int crank, uint32_t cbase, uint32_t cspan) {
   const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
   const unsigned long long last = __ldcg(L + (K - 1));
   uint4 q[4];  // 8 entries per round trip
 #pragma unroll
   for (int t = 0; t < 4; ++t) q[t] = (2 * t < KS) ? __ldcg(reinterpret_cast<const uint4*>(L + 2 * t)) : e4;
   if (last < x) {
-#ifdef PV_INSTRUMENT
+#ifdef PV_INSTRUMENT_INSERTS
     atomicAdd(&g_insert_stats[2], 1ull);
 #endif
     return;
@@ -350,7 +360,8 @@ __device__ __forceinline__ void list_insert(unsigned long long* L, int K, int KS
   unsigned long long prev = 0;
   bool run = true;
   auto step = [&](unsigned long long y) {
-    if (run && y < x && (a == 0 || y > prev)) {
+    if (!run || static_cast<uint32_t>(y >> 32) - cbase < cspan) return;  // own chunk: counted by crank
+    if (y < x && (a == 0 || y > prev)) {
       prev = y;
       ++a;
     } else {
@@ -373,18 +384,18 @@ __device__ __forceinline__ void list_insert(unsigned long long* L, int K, int KS
     }
   }
   // Stride padding past K reads empty, so a >= K only if K entries are below x.
-#ifdef PV_INSTRUMENT
+#ifdef PV_INSTRUMENT_INSERTS
   unsigned long long n_atomics = 0;
 #endif
-  for (int k = a; k < K; ++k) {
+  for (int k = a + crank; k < K; ++k) {
     const unsigned long long old = atomicMin(L + k, x);
-#ifdef PV_INSTRUMENT
+#ifdef PV_INSTRUMENT_INSERTS
     ++n_atomics;
 #endif
     if (old == kEmpty64) break;
     x = old > x ? old : x;
   }
-#ifdef PV_INSTRUMENT
+#ifdef PV_INSTRUMENT_INSERTS
   atomicAdd(&g_insert_stats[0], 1ull);
   atomicAdd(&g_insert_stats[1], n_atomics);
   atomicMax(&g_insert_stats[3], n_atomics);
@@ -401,10 +412,13 @@ __device__ __forceinline__ void list_insert(unsigned long long* L, int K, int KS
 // own warp (lanes hold consecutive indices).
 constexpr int kTileHash = 2 * kThreads;
 
+constexpr int kChunkHash = 4096;   // chunk map positions (see chunk_rank)
+constexpr int kChunkProbes = 64;
+
 // Dynamic shared memory of the kernel: two tile maps, used by alternate
 // tiles so one can be emptied while the other is filled.
 constexpr int kMapBytes = kTileHash * kWarps + kTileHash * 4 + kTileHash * 2;
-constexpr int kDynSmem = 2 * kMapBytes;
+constexpr int kDynSmem = 2 * kMapBytes + 2 * 4 * kChunkHash;
 static_assert(kMapBytes % 16 == 0, "maps stay 16-byte aligned");
 
 struct TileMap {
@@ -445,6 +459,21 @@ __device__ __forceinline__ int tile_claim(const TileMap& m, int slot) {
     h = (h + 1) & (kTileHash - 1);
   }
   return -1;
+}
+
+// Chunk map: pillar -> number of this block's tile groups seen so far.
+// Tiles of a chunk are grouped one after the other, so the count a tile
+// group reads is its rank among the chunk's groups of the pillar.  When the
+// map is full the rank falls back to 0, which is still a valid lower bound.
+
+__device__ __forceinline__ int chunk_rank(int* ckey, int* ccnt, int slot) {
+  unsigned int h = mix32(static_cast<unsigned int>(slot) ^ 0x9e3779b9u) & (kChunkHash - 1);
+  for (int probe = 0; probe < kChunkProbes; ++probe) {
+    const int cur = atomicCAS(ckey + h, -1, slot);
+    if (cur == -1 || cur == slot) return atomicAdd(ccnt + h, 1);
+    h = (h + 1) & (kChunkHash - 1);
+  }
+  return 0;
 }
 
 // Byte counters at map position h: *before = warps 0 .. warp-1, *total = all.
@@ -495,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   __shared__ unsigned int s_tmp[kWarps + 1];
   __shared__ int s_flag;
   __shared__ unsigned int s_layout[2];
+  __shared__ unsigned int s_nrec;
 
   const unsigned int P = gridDim.x;
   const unsigned int cta = blockIdx.x;
@@ -526,16 +556,21 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     bar_target += P;
   }
 
-  // ---- phase 1: bin every point; lay each block tile out grouped by pillar
-  // (groups in any order inside the tile, points of a group in index order),
-  // and insert one entry per (pillar, tile) group, the group's first point,
-  // into the pillar's list.  Two barriers per tile: after the warp groups
-  // register in the tile map, and after the group offsets are handed out.
+  // ---- phase 1a: bin every point; lay each block tile out grouped by pillar
+  // (groups in any order inside the tile, points of a group in index order)
+  // and record one entry per (pillar, tile) group, with the group's rank among
+  // this chunk's groups of the pillar.  Two barriers per tile: after the warp
+  // groups register in the tile map, and after the group offsets are handed
+  // out.  No global atomics in this loop.
+  // ---- phase 1b: insert the recorded groups into the pillars' lists, all at
+  // once (their chunk ranks keep them apart).
   if (alive) {
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     long long tb = begin;  // this block's contiguous, tile-aligned chunk
     float4 q = (tb + tid < end) ? __ldg(p.points + tb + tid) : z4;
-    {  // both maps empty: counters zero, keys -1 (16-byte stores)
+    int* ckey = reinterpret_cast<int*>(s_dyn + 2 * kMapBytes);
+    int* ccnt = ckey + kChunkHash;
+    {  // both tile maps empty (counters zero, keys -1) and the chunk map empty
       uint4* d4 = reinterpret_cast<uint4*>(s_dyn);
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       const uint4 m1 = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
@@ -546,8 +581,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         for (int j = static_cast<int>(tid); j < kTileHash * 4 / 16; j += kThreads)
           base[kTileHash * kWarps / 16 + j] = m1;
       }
+      uint4* c4 = reinterpret_cast<uint4*>(ckey);
+      for (int j = static_cast<int>(tid); j < kChunkHash / 4; j += kThreads) {
+        c4[j] = m1;
+        c4[kChunkHash / 4 + j] = z;
+      }
     }
-    if (tid == 0) s_layout[0] = s_layout[1] = 0;
+    if (tid == 0) {
+      s_layout[0] = s_layout[1] = 0;
+      s_nrec = 0;
+    }
     __syncthreads();
     int buf = 0;
     for (; tb < end; tb += kThreads, buf ^= 1) {
@@ -593,35 +636,59 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         tile_counts(tm, h, warp, &trank, &tot);
         trank += __popc(peers & lanemask_lt());
       }
-      {  // group offsets: one shared-memory atomic per warp for all its tile-group leaders
-        const bool lead = slot >= 0 && trank == 0;
+      const bool lead = slot >= 0 && trank == 0;
+      const int crank = lead ? chunk_rank(ckey, ccnt, slot) : 0;
+      {  // group offsets and record slots: one shared-memory atomic per warp each
         const unsigned int need = lead ? tot : 0u;
-        unsigned int incl = need;
+        const unsigned int wants = (lead && crank < K) ? 1u : 0u;
+        unsigned int incl = need, rincl = wants;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= static_cast<unsigned int>(o)) incl += y;
+          const unsigned int ry = __shfl_up_sync(0xffffffffu, rincl, o);
+          if (lane >= static_cast<unsigned int>(o)) {
+            incl += y;
+            rincl += ry;
+          }
         }
         const unsigned int wsum = __shfl_sync(0xffffffffu, incl, 31);
-        unsigned int base = 0;
-        if (lane == 31 && wsum) base = atomicAdd(tm.layout, wsum);
+        const unsigned int rsum = __shfl_sync(0xffffffffu, rincl, 31);
+        unsigned int base = 0, rbase = 0;
+        if (lane == 31) {
+          if (wsum) base = atomicAdd(tm.layout, wsum);
+          if (rsum) rbase = atomicAdd(&s_nrec, rsum);
+        }
         base = __shfl_sync(0xffffffffu, base, 31);
-        if (lead) tm.off[h] = static_cast<unsigned short>(base + incl - need);
-      }
-      if (i < end) p.slot_of_point[i] = slot < 0 ? -1 : (trank == 0 ? (slot | kLeaderBit) : slot);
-      __syncthreads();  // (B) group offsets handed out; the previous map is empty
-      PV_SUB(3);
-      if (slot >= 0) {
-        const unsigned int off = tm.off[h];
-        p.tile_rows[tb + off + trank] = q;
-        if (trank == 0) {
-          const unsigned long long entry =
-              (static_cast<unsigned long long>(i) << 32) | ((off << 11) | tot);
-          list_insert(p.lists + static_cast<size_t>(slot) * p.KS, K, p.KS, entry);
+        rbase = __shfl_sync(0xffffffffu, rbase, 31);
+        if (lead) {
+          const unsigned int off = base + incl - need;
+          tm.off[h] = static_cast<unsigned short>(off);
+          if (crank < K) {  // a group ranked K or later in its own chunk can never be kept
+            const long long rj = begin + rbase + rincl - wants;
+            p.firsts[rj] = slot;  // the record's slot (firsts is rewritten after the barrier)
+            p.recs[rj] = (static_cast<unsigned long long>(i) << 32) |
+                         (static_cast<unsigned int>(crank) << 21) | (off << 11) | tot;
+          }
         }
       }
+      if (i < end) p.slot_of_point[i] = slot < 0 ? -1 : (lead ? (slot | kLeaderBit) : slot);
+      __syncthreads();  // (B) group offsets handed out; the previous map is empty
+      PV_SUB(3);
+      if (slot >= 0) p.tile_rows[tb + tm.off[h] + trank] = q;
       PV_SUB(4);
       q = qn;
+    }
+    __syncthreads();  // every record written
+#ifdef PV_INSTRUMENT
+    if (tid == 0 && cta < kStampCtas) g_p1_ns[cta][5] = global_timer_ns();
+#endif
+    const unsigned int nrec = s_nrec;
+    for (unsigned int j = tid; j < nrec; j += kThreads) {
+      const int rs = __ldcg(p.firsts + begin + j);
+      const unsigned long long entry = __ldcg(p.recs + begin + j);
+      const int crank = static_cast<int>((entry >> 21) & 2047u);
+      list_insert(p.lists + static_cast<size_t>(rs) * p.KS, K, p.KS, entry, crank, static_cast<uint32_t>(begin),
+                  static_cast<uint32_t>(end - begin));
     }
     PV_STAMP(1);
     alive = grid_sync(p.ctl, bar_target, &s_flag);
@@ -662,14 +729,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         unsigned int carry = 0;
 #pragma unroll
         for (int u = 0; u < kFlagUnroll; ++u) {
-          const unsigned int c = s_tile[u][lane];
+          const unsigned int c = lane < static_cast<unsigned int>(kWarps) ? s_tile[u][lane] : 0u;
           unsigned int incl = c;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
             const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= static_cast<unsigned int>(o)) incl += y;
           }
-          s_tile[u][lane] = carry + incl - c;
+          if (lane < static_cast<unsigned int>(kWarps)) s_tile[u][lane] = carry + incl - c;
           carry += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) s_tmp[kWarps] = carry;
@@ -789,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           row[u] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (ok[u] && e < K && g >= 0 && static_cast<unsigned int>(e) < cnt[u]) {
             const long long tbase = static_cast<long long>(gl_lead) & ~static_cast<long long>(kThreads - 1);
-            row[u] = __ldcg(p.tile_rows + tbase + (gl_info >> 11) + (e - gl_start));
+            row[u] = __ldcg(p.tile_rows + tbase + ((gl_info >> 11) & 1023u) + (e - gl_start));
           }
         }
 #pragma unroll
@@ -879,6 +946,7 @@ struct Workspace {
   int32_t* slot_of_point = nullptr;
   int32_t* firsts = nullptr;
   float4* tile_rows = nullptr;
+  unsigned long long* recs = nullptr;
   size_t points_cap = 0;
   unsigned long long* lists = nullptr;  // 64-bit entries
   size_t list_words_cap = 0;
@@ -983,11 +1051,12 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   pl->list_words = static_cast<size_t>(pl->T) * pl->KS;
   pl->key_words = mode == 2 ? static_cast<size_t>(pl->T) : 0;
   const int per_sm = o.ctas_per_sm ? std::min(o.ctas_per_sm, dev.blocks_per_sm) : dev.blocks_per_sm;
-  pl->ctas = std::min(kMaxCtas, std::max(1, dev.sms * per_sm));
+  // The count scan after the second barrier takes one count per thread.
+  pl->ctas = std::min(std::min(kMaxCtas, kThreads), std::max(1, dev.sms * per_sm));
   // Contiguous, tile-aligned chunks: phase 1 and phase 2 share them.
   const int64_t tiles = (N + kThreads - 1) / kThreads;
   pl->chunk = ((tiles + pl->ctas - 1) / pl->ctas) * kThreads;
-  pl->bytes = sizeof(Control) + 4 * static_cast<size_t>(kMaxCtas) + 24 * static_cast<size_t>(N) +
+  pl->bytes = sizeof(Control) + 4 * static_cast<size_t>(kMaxCtas) + 32 * static_cast<size_t>(N) +
               8 * pl->list_words + 4 * pl->key_words;
   return PV_OK;
 }
@@ -1064,10 +1133,11 @@ int reserve(Workspace* ws, const Plan& pl, int64_t N, pv_stream_t stream) {
   const size_t np = round_up(static_cast<size_t>(std::max<int64_t>(N, 1)), 65536);
   if (ws->points_cap < np) {
     const size_t want = std::max(np, ws->points_cap + ws->points_cap / 2);
-    size_t cap_a = ws->points_cap, cap_b = ws->points_cap, cap_c = ws->points_cap;
+    size_t cap_a = ws->points_cap, cap_b = ws->points_cap, cap_c = ws->points_cap, cap_d = ws->points_cap;
     if ((st = grow(&ws->slot_of_point, &cap_a, want, 0, stream, &synced)) != PV_OK) return st;
     if ((st = grow(&ws->firsts, &cap_b, want, 0, stream, &synced)) != PV_OK) return st;
     if ((st = grow(&ws->tile_rows, &cap_c, want, 0, stream, &synced)) != PV_OK) return st;
+    if ((st = grow(&ws->recs, &cap_d, want, 0, stream, &synced)) != PV_OK) return st;
     ws->points_cap = want;
   }
   if ((st = grow(&ws->lists, &ws->list_words_cap, round_up(pl.list_words, 2), 0xFF, stream, &synced)) != PV_OK)
@@ -1143,6 +1213,7 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.slot_of_point = ws->slot_of_point;
   kp.firsts = ws->firsts;
   kp.tile_rows = ws->tile_rows;
+  kp.recs = ws->recs;
   kp.counts = ws->counts;
   kp.ctl = ws->ctl;
   kp.list_words_cap = ws->list_words_cap;
@@ -1214,7 +1285,8 @@ constexpr size_t kStaticOffKeys = kStaticOffCounts + 4 * kMaxCtas;
 constexpr size_t kStaticOffLists = kStaticOffKeys + 4 * kStaticSlots;
 constexpr size_t kStaticListWords = kStaticSlots * kStaticMaxK;  // 64-bit entries
 constexpr size_t kStaticOffRows = kStaticOffLists + 8 * kStaticListWords;
-constexpr size_t kStaticOffPoints = kStaticOffRows + 16 * static_cast<size_t>(kStaticMaxPoints);
+constexpr size_t kStaticOffRecs = kStaticOffRows + 16 * static_cast<size_t>(kStaticMaxPoints);
+constexpr size_t kStaticOffPoints = kStaticOffRecs + 8 * static_cast<size_t>(kStaticMaxPoints);
 constexpr size_t kStaticBytes = kStaticOffPoints + 2 * 4 * static_cast<size_t>(kStaticMaxPoints);
 static_assert(sizeof(Control) <= kStaticOffCounts, "control block fits its region");
 static_assert(kStaticOffKeys % 256 == 0 && kStaticOffLists % 256 == 0 && kStaticOffRows % 256 == 0 &&
@@ -1310,6 +1382,7 @@ int voxelize_static_impl(const float* points, int64_t N, const float range[6], c
   view.lists = reinterpret_cast<unsigned long long*>(sd->base + kStaticOffLists);
   view.list_words_cap = kStaticListWords;
   view.tile_rows = reinterpret_cast<float4*>(sd->base + kStaticOffRows);
+  view.recs = reinterpret_cast<unsigned long long*>(sd->base + kStaticOffRecs);
   int32_t* pts = reinterpret_cast<int32_t*>(sd->base + kStaticOffPoints);
   view.slot_of_point = pts;
   view.firsts = pts + kStaticMaxPoints;
@@ -1437,6 +1510,7 @@ int pv_release_workspace(void) {
     cudaFree(ws->slot_of_point);
     cudaFree(ws->firsts);
     cudaFree(ws->tile_rows);
+    cudaFree(ws->recs);
     cudaFree(ws->lists);
     cudaFree(ws->keys);
     cudaFree(ws->staging);
