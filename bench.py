@@ -52,6 +52,23 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(value, device=None):
+    """Maximum of a per-rank float over the process group (identity at N = 1)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(points_per_frame, steps, world, region_ms):
+    """Mpoints/s over all ranks: every rank voxelizes `steps` frames of its own."""
+    return world * points_per_frame * steps / (region_ms * 1e-3) / 1e6
+
+
 def algorithmic_bytes(n, max_points, max_voxels):
     # Input read once (16 B/point) + every output byte written once:
     # voxels 16*K B, coords 12 B, counts 4 B per pillar row, plus V (4 B).
@@ -256,17 +273,14 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     clocks = sampler.stop() if sampler else None
 
-    if dist:
-        t = torch.tensor([region_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        region_ms = float(t.item())
+    region_ms = max_over_ranks(region_ms, device=dev)
     # Result check after timing: the last timed output against the first.
     last = outs[(args.warmup + args.steps - 1) % R]
     V = int(last[3].item())
 
     if rank != 0:
         return
-    value = world * n * args.steps / (region_ms * 1e-3) / 1e6
+    value = whole_job_rate(n, args.steps, world, region_ms)
     avg_kernel_s = statistics.mean(kernel_ms) * 1e-3
     peak, peak_src = measured_peak()
     achieved = bytes_launch / avg_kernel_s / 1e9

@@ -114,12 +114,16 @@ int pv_voxelize(const float* points, int64_t num_points, const float point_cloud
  *                PV_ERR_CAPACITY (used by the tests of that error path).
  *   ctas_per_sm  resident blocks per SM of the single cooperative launch
  *                (capped at what fits).
+ *   test_stall_barrier  for tests of the timeout path only (see the field).
  */
 typedef struct pv_options {
   int table_mode;
   int table_log2;
   int ctas_per_sm;
-  int reserved[5];
+  int test_stall_barrier;  /* test hook: nonzero makes the first grid barrier wait for
+                              one arrival that never comes, so the bounded wait runs out
+                              (about 1 s) and the call reports PV_ERR_TIMEOUT */
+  int reserved[4];
 } pv_options;
 
 int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cloud_range[6],

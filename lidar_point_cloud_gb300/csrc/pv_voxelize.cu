@@ -98,6 +98,7 @@ struct KParams {
   int KS;            // list stride in uint32 entries (K rounded up to 4)
   int max_voxels;
   int hash_mode;
+  unsigned int bar_extra;  // test hook: extra arrivals the first barrier waits for
   unsigned int table_mask;
   unsigned long long* lists;  // [T][KS] entries (leader index << 32) | (offset << 11) | size
   int32_t* keys;
@@ -691,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
                   static_cast<uint32_t>(end - begin));
     }
     PV_STAMP(1);
-    alive = grid_sync(p.ctl, bar_target, &s_flag);
+    alive = grid_sync(p.ctl, bar_target + p.bar_extra, &s_flag);
   }
   PV_STAMP(2);
 
@@ -962,6 +963,7 @@ std::map<int, DeviceInfo> g_devices;
 std::map<std::pair<int, pv_stream_t>, Workspace*> g_ws;
 
 struct Plan {
+  unsigned int stall = 0;  // test hook (pv_options.test_stall_barrier)
   int64_t g[3];
   int mode;
   int64_t T;
@@ -1032,6 +1034,7 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   if (opt) o = *opt;
   if (o.table_mode < 0 || o.table_mode > 2 || o.table_log2 < 0 || o.table_log2 > 31 || o.ctas_per_sm < 0)
     return PV_ERR_INVALID;
+  pl->stall = o.test_stall_barrier ? 1u : 0u;
   const int64_t cells = pl->g[0] * pl->g[1];
   const int64_t distinct_bound = std::max<int64_t>(1, std::min(N, cells));
   const int64_t hashed_T = next_pow2(std::max<int64_t>(2 * distinct_bound, 1024));
@@ -1207,6 +1210,7 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.KS = pl.KS;
   kp.max_voxels = M;
   kp.hash_mode = pl.mode == 2 ? 1 : 0;
+  kp.bar_extra = pl.stall;
   kp.table_mask = pl.mask;
   kp.lists = ws->lists;
   kp.keys = ws->keys;

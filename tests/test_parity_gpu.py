@@ -158,6 +158,18 @@ def test_capacity_error_then_recovery():
     assert_parity(pts, KR, KV, 32, 16_000)
 
 
+def test_wait_timeout_is_reported_and_recovered():
+    """A grid barrier that can never complete gives up after its time limit
+    (about one second), the call reports PV_ERR_TIMEOUT through V, the
+    context stays usable, and the next call on the stream is exact again
+    (the kernel resets the table it could not clean)."""
+    pts, P = synth.make("kitti")
+    got = gpu_run(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, test_stall_barrier=1)
+    assert got[3] == -6  # PV_ERR_TIMEOUT
+    assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, table_mode=2)
+
+
 def test_two_streams():
     a, Pa = synth.make("kitti")
     b, Pb = synth.make("uniform_100000")
