@@ -136,10 +136,6 @@ __device__ __forceinline__ unsigned int ld_relaxed(const unsigned int* p) {
   return v;
 }
 
-__device__ __forceinline__ void st_release(unsigned int* p, unsigned int v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ long long lmin(long long a, long long b) { return a < b ? a : b; }
 
 __device__ __forceinline__ unsigned int lanemask_lt() {
@@ -183,15 +179,20 @@ __device__ unsigned long long g_insert_stats[4];  // inserts, atomics, rejected 
 
 // ------------------------------------------------------------ block-wide helpers
 
-// Thread 0 waits (bounded) until *flag reaches `target` (>=) or equals it
-// (exact); returns false after the time limit, recording PV_ERR_TIMEOUT.
-__device__ bool wait_flag(Control* ctl, const unsigned int* flag, unsigned int target, bool exact,
-                          int* s_flag) {
+// All blocks of the cooperative launch arrive; returns false if the wait ran
+// past the time limit (PV_ERR_TIMEOUT is then recorded).  `target` counts
+// arrivals since the launch began (P for the first barrier, 2P for the next).
+// Thread 0 arrives with a release reduction (the block's earlier writes are
+// ordered before it by the CTA barrier), polls with acquire loads, and the
+// closing CTA barrier passes the acquired view to the rest of the block.
+__device__ bool grid_sync(Control* ctl, unsigned int target, int* s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    unsigned int v = ld_acquire(flag);
-    if (exact ? v != target : v < target) {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&ctl->bar) : "memory");
+    unsigned int v = ld_acquire(&ctl->bar);
+    if (v < target) {
       const unsigned long long t0 = global_timer_ns();
       do {
         if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -199,25 +200,14 @@ __device__ bool wait_flag(Control* ctl, const unsigned int* flag, unsigned int t
           ok = 0;
           break;
         }
-        v = ld_acquire(flag);
-      } while (exact ? v != target : v < target);
+        v = ld_acquire(&ctl->bar);
+      } while (v < target);
     }
-    __threadfence();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     *s_flag = ok;
   }
   __syncthreads();
   return *s_flag != 0;
-}
-
-// All blocks of the cooperative launch arrive; `target` counts arrivals
-// since the launch began (P for the first barrier, 2P for the next).
-__device__ bool grid_sync(Control* ctl, unsigned int target, int* s_flag) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&ctl->bar, 1u);
-  }
-  return wait_flag(ctl, &ctl->bar, target, false, s_flag);
 }
 
 // Exclusive prefix sum over the block; *total receives the block sum.
@@ -569,25 +559,32 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     long long tb = begin;  // this block's contiguous, tile-aligned chunk
     float4 q = (tb + tid < end) ? __ldg(p.points + tb + tid) : z4;
+    const bool multi = end - begin > kThreads;  // more than one tile: second map and chunk map in use
     int* ckey = reinterpret_cast<int*>(s_dyn + 2 * kMapBytes);
     int* ccnt = ckey + kChunkHash;
-    {  // both tile maps empty (counters zero, keys -1) and the chunk map empty
+    {  // tile map 0 empty (counters zero, keys -1); map 1 and the chunk map only if used
       uint4* d4 = reinterpret_cast<uint4*>(s_dyn);
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       const uint4 m1 = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
+      const int maps = multi ? 2 : 1;
+      for (int m = 0; m < maps; ++m) {
         uint4* base = d4 + m * (kMapBytes / 16);
         for (int j = static_cast<int>(tid); j < kTileHash * kWarps / 16; j += kThreads) base[j] = z;
         for (int j = static_cast<int>(tid); j < kTileHash * 4 / 16; j += kThreads)
           base[kTileHash * kWarps / 16 + j] = m1;
       }
-      uint4* c4 = reinterpret_cast<uint4*>(ckey);
-      for (int j = static_cast<int>(tid); j < kChunkHash / 4; j += kThreads) {
-        c4[j] = m1;
-        c4[kChunkHash / 4 + j] = z;
+      if (multi) {
+        uint4* c4 = reinterpret_cast<uint4*>(ckey);
+        for (int j = static_cast<int>(tid); j < kChunkHash / 4; j += kThreads) {
+          c4[j] = m1;
+          c4[kChunkHash / 4 + j] = z;
+        }
       }
     }
+#ifdef PV_INSTRUMENT
+    __syncthreads();
+    if (tid == 0 && cta < kStampCtas) g_p1_ns[cta][6] = global_timer_ns();
+#endif
     if (tid == 0) {
       s_layout[0] = s_layout[1] = 0;
       s_nrec = 0;
@@ -630,15 +627,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       __syncthreads();  // (A) every warp group registered; the previous tile's map is read
       PV_SUB(2);
       // Empty the previous tile's map (used again by the next tile, after barrier B).
-      if (tid == 0) *prev.layout = 0;
-      tile_clear(prev, tid);
+      if (multi) {
+        if (tid == 0) *prev.layout = 0;
+        tile_clear(prev, tid);
+      }
       unsigned int trank = 0, tot = 0;
       if (slot >= 0) {
         tile_counts(tm, h, warp, &trank, &tot);
         trank += __popc(peers & lanemask_lt());
       }
       const bool lead = slot >= 0 && trank == 0;
-      const int crank = lead ? chunk_rank(ckey, ccnt, slot) : 0;
+      const int crank = (lead && multi) ? chunk_rank(ckey, ccnt, slot) : 0;
       {  // group offsets and record slots: one shared-memory atomic per warp each
         const unsigned int need = lead ? tot : 0u;
         const unsigned int wants = (lead && crank < K) ? 1u : 0u;
@@ -790,94 +789,124 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       owner = lo;
     }
     for (long long r0 = rw0; r0 < rw1; r0 += kEmitUnroll) {
+      // Lane u < kEmitUnroll finds the slot of rank r0 + u (walking the owner forward).
+      int my_slot = 0;
+      unsigned int my_owner = owner;
+      if (static_cast<int>(lane) < kEmitUnroll && r0 + lane < rw1) {
+        const unsigned int r = static_cast<unsigned int>(r0 + lane);
+        while (s_prefix[my_owner + 1] <= r) ++my_owner;  // ranks ascend
+        my_slot = __ldcg(p.firsts + static_cast<long long>(my_owner) * p.chunk + (r - s_prefix[my_owner]));
+      }
+      owner = __shfl_sync(0xffffffffu, my_owner, kEmitUnroll - 1);
       int slot[kEmitUnroll];
       bool ok[kEmitUnroll];
+      unsigned long long ent[kEmitUnroll];
+#pragma unroll
+      for (int u = 0; u < kEmitUnroll; ++u) {
+        ok[u] = r0 + u < rw1;
+        slot[u] = __shfl_sync(0xffffffffu, my_slot, u);
+        // Group descriptors: entry g of the list on lane g (leader, offset, size).
+        ent[u] = (ok[u] && static_cast<int>(lane) < K) ? __ldcg(p.lists + static_cast<size_t>(slot[u]) * p.KS + lane)
+                                                       : kEmpty64;
+      }
+      unsigned int cnt[kEmitUnroll];
 #pragma unroll
       for (int u = 0; u < kEmitUnroll; ++u) {
         const long long r = r0 + u;
-        ok[u] = r < rw1;
-        slot[u] = 0;
-        if (ok[u]) {
-          while (s_prefix[owner + 1] <= static_cast<unsigned int>(r)) ++owner;  // ranks ascend
-          slot[u] = __ldcg(p.firsts + static_cast<long long>(owner) * p.chunk + (r - s_prefix[owner]));
-        }
-      }
-      // Group descriptors: one list entry per lane (leader index, offset, size).
-      uint32_t lead[kEmitUnroll];
-      uint32_t ginfo[kEmitUnroll];
-#pragma unroll
-      for (int u = 0; u < kEmitUnroll; ++u) {
-        const unsigned long long ent = (ok[u] && static_cast<int>(lane) < K)
-                                           ? __ldcg(p.lists + static_cast<size_t>(slot[u]) * p.KS + lane)
-                                           : kEmpty64;
-        lead[u] = static_cast<uint32_t>(ent >> 32);
-        ginfo[u] = static_cast<uint32_t>(ent);
-        if (lead[u] != kEmpty && static_cast<long long>(lead[u]) >= p.n) {  // never in a clean table
-          lead[u] = kEmpty;
+        float4* orow = p.out_voxels + static_cast<size_t>(r) * K;
+        unsigned long long* L = p.lists + static_cast<size_t>(slot[u]) * p.KS;
+        if (static_cast<uint32_t>(ent[u] >> 32) != kEmpty && (ent[u] >> 32) >= static_cast<unsigned long long>(p.n)) {
+          ent[u] = kEmpty64;  // never in a clean table
           stale = true;
         }
-      }
-      unsigned int cnt[kEmitUnroll];
-      int gstart[kEmitUnroll];
+        const unsigned int present = __ballot_sync(0xffffffffu, ent[u] != kEmpty64);  // lanes 0 .. G-1
+        unsigned int written = 0;
+        if (ok[u] && present != 0u && (present & (present + 1u)) == 0u && (present == 1u || K <= 32)) {
+          // Up to 32 groups, all on the warp's lanes.
+          const int G = __popc(present);
+          if (G == 1) {  // the common case: the pillar's first points are one tile group
+            const unsigned int info = static_cast<unsigned int>(ent[u]);
+            const unsigned int n = (info & 2047u) < static_cast<unsigned int>(K) ? (info & 2047u) : static_cast<unsigned int>(K);
+            const long long base = (static_cast<long long>(ent[u] >> 32) & ~static_cast<long long>(kThreads - 1)) +
+                                   ((info >> 11) & 1023u);
+            const long long b0 = __shfl_sync(0xffffffffu, base, 0);
+            const unsigned int n0 = __shfl_sync(0xffffffffu, n, 0);
+            for (int e = static_cast<int>(lane); e < K; e += 32)
+              orow[e] = static_cast<unsigned int>(e) < n0 ? __ldcg(p.tile_rows + b0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            written = n0;
+          } else {  // several groups: position e comes from the last group starting at or before e
+            const unsigned int size = ent[u] != kEmpty64 ? (static_cast<unsigned int>(ent[u]) & 2047u) : 0u;
+            unsigned int incl = size;
 #pragma unroll
-      for (int u = 0; u < kEmitUnroll; ++u) {
-        // Inclusive scan of group sizes over the lanes (groups), capped at K.
-        const unsigned int size = lead[u] != kEmpty ? (ginfo[u] & 2047u) : 0u;
-        unsigned int incl = size;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= static_cast<unsigned int>(o)) incl += y;
-        }
-        gstart[u] = static_cast<int>(incl - size);
-        const unsigned int all = __shfl_sync(0xffffffffu, incl, 31);
-        cnt[u] = all < static_cast<unsigned int>(K) ? all : static_cast<unsigned int>(K);
-      }
-      for (int e0 = 0; e0 < K; e0 += 32) {
-        const int e = e0 + static_cast<int>(lane);
-        float4 row[kEmitUnroll];
-#pragma unroll
-        for (int u = 0; u < kEmitUnroll; ++u) {
-          // Group of position e: the last valid group whose start is <= e
-          // (valid groups fill lanes 0 .. G-1 with strictly increasing starts).
-          const int G = __popc(__ballot_sync(0xffffffffu, lead[u] != kEmpty));
-          int g = G > 0 ? 0 : -1;
-          if (G > 1) {  // warp-uniform: most pillars have a single group
+            for (int o = 1; o < 32; o <<= 1) {
+              const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= static_cast<unsigned int>(o)) incl += y;
+            }
+            const int gstart = static_cast<int>(incl - size);
+            const unsigned int all = __shfl_sync(0xffffffffu, incl, 31);
+            written = all < static_cast<unsigned int>(K) ? all : static_cast<unsigned int>(K);
+            const int e = static_cast<int>(lane);  // K <= 32 here
+            int g = 0;
 #pragma unroll
             for (int step = 16; step >= 1; step >>= 1) {
               const int j = g + step;
-              const int st = __shfl_sync(0xffffffffu, gstart[u], j < 32 ? j : 31);
+              const int st = __shfl_sync(0xffffffffu, gstart, j < 32 ? j : 31);
               if (j < G && st <= e) g = j;
             }
+            const unsigned long long ge = __shfl_sync(0xffffffffu, ent[u], g);
+            const int gs = __shfl_sync(0xffffffffu, gstart, g);
+            if (e < K) {
+              float4 row = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (static_cast<unsigned int>(e) < written) {
+                const long long tbase = static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1);
+                row = __ldcg(p.tile_rows + tbase + ((static_cast<unsigned int>(ge) >> 11) & 1023u) + (e - gs));
+              }
+              orow[e] = row;
+            }
           }
-          const int gsafe = g < 0 ? 0 : g;
-          const uint32_t gl_lead = __shfl_sync(0xffffffffu, lead[u], gsafe);
-          const uint32_t gl_info = __shfl_sync(0xffffffffu, ginfo[u], gsafe);
-          const int gl_start = __shfl_sync(0xffffffffu, gstart[u], gsafe);
-          row[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (ok[u] && e < K && g >= 0 && static_cast<unsigned int>(e) < cnt[u]) {
-            const long long tbase = static_cast<long long>(gl_lead) & ~static_cast<long long>(kThreads - 1);
-            row[u] = __ldcg(p.tile_rows + tbase + ((gl_info >> 11) & 1023u) + (e - gl_start));
+          if (ent[u] != kEmpty64) L[lane] = kEmpty64;
+        } else if (ok[u]) {
+          // General case (max_points > 32 with more than one group, or many groups):
+          // walk the list 32 entries at a time and copy each group's run.
+          unsigned long long chunk = ent[u];
+          for (int g0 = 0; g0 < K; g0 += 32) {
+            if (g0 > 0) chunk = (g0 + static_cast<int>(lane) < K) ? __ldcg(L + g0 + lane) : kEmpty64;
+            const unsigned int here = __ballot_sync(0xffffffffu, chunk != kEmpty64);
+            if (here == 0u) break;
+            for (unsigned int m = here; m != 0u && written < static_cast<unsigned int>(K); m &= m - 1u) {
+              const unsigned long long ge = __shfl_sync(0xffffffffu, chunk, __ffs(m) - 1);
+              const unsigned int info = static_cast<unsigned int>(ge);
+              const unsigned int room = static_cast<unsigned int>(K) - written;
+              const unsigned int n = (info & 2047u) < room ? (info & 2047u) : room;
+              const long long base =
+                  (static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1)) + ((info >> 11) & 1023u);
+              for (unsigned int j = lane; j < n; j += 32) orow[written + j] = __ldcg(p.tile_rows + base + j);
+              written += n;
+            }
+            if (chunk != kEmpty64) L[g0 + lane] = kEmpty64;
           }
+          for (unsigned int e = written + lane; e < static_cast<unsigned int>(K); e += 32)
+            orow[e] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        cnt[u] = written;
+      }
+      // Coordinates and counts of the batch: lane 3u + c writes coordinate c of pillar u,
+      // lane u writes count u.
+      if (static_cast<int>(lane) < 3 * kEmitUnroll) {
+        const int u = static_cast<int>(lane) / 3, c = static_cast<int>(lane) % 3;
+        int su = 0;
 #pragma unroll
-        for (int u = 0; u < kEmitUnroll; ++u) {
-          if (ok[u] && e < K) {
-            const long long r = r0 + u;
-            p.out_voxels[static_cast<size_t>(r) * K + e] = row[u];
-            p.lists[static_cast<size_t>(slot[u]) * p.KS + e] = kEmpty64;
-          }
+        for (int v = 0; v < kEmitUnroll; ++v) su = (v == u) ? slot[v] : su;
+        if (r0 + u < rw1) {
+          const int key = p.hash_mode ? __ldcg(p.keys + su) : su;
+          p.out_coords[3 * static_cast<size_t>(r0 + u) + c] = c == 0 ? 0 : (c == 1 ? key / p.g_x : key % p.g_x);
         }
       }
+      __syncwarp();  // hashed keys are read above before lane u empties them below
 #pragma unroll
       for (int u = 0; u < kEmitUnroll; ++u) {
-        if (ok[u] && lane == 0) {
-          const size_t r = static_cast<size_t>(r0 + u);
-          const int key = p.hash_mode ? __ldcg(p.keys + slot[u]) : slot[u];
-          p.out_coords[3 * r + 0] = 0;
-          p.out_coords[3 * r + 1] = key / p.g_x;
-          p.out_coords[3 * r + 2] = key % p.g_x;
-          p.out_counts[r] = static_cast<int32_t>(cnt[u]);
+        if (lane == static_cast<unsigned int>(u) && ok[u]) {
+          p.out_counts[static_cast<size_t>(r0 + u)] = static_cast<int32_t>(cnt[u]);
           if (p.hash_mode) p.keys[slot[u]] = kNoKey;
         }
       }
