@@ -71,7 +71,10 @@ static_assert(kWarps <= 32 && kWarps % 16 == 0, "warp 0 scans one value per warp
 constexpr int kMinBlocksPerSM = 1024 / kThreads;
 constexpr int kMaxCtas = 1024;             // blocks per launch (prefix lives in shared memory)
 constexpr int kFlagUnroll = 4;             // block-wide tiles in flight when flagging
-constexpr int kEmitUnroll = 4;             // pillars in flight per warp when emitting
+#ifndef PV_EMIT_UNROLL
+#define PV_EMIT_UNROLL 4
+#endif
+constexpr int kEmitUnroll = PV_EMIT_UNROLL;  // pillars in flight per warp when emitting
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded spins: 1 s
 constexpr int64_t kMaxAxisCells = int64_t(1) << 24;
 
