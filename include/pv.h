@@ -188,7 +188,8 @@ typedef struct pv_plan {
   int64_t grid[3];          /* pillar grid extents */
   int table_mode;           /* 1 direct, 2 hashed */
   int64_t table_slots;      /* pillar slots in the table */
-  int list_stride;          /* uint32 entries per slot (max_points rounded up to 4) */
+  int list_stride;          /* 64-bit list entries per slot: a head row of 4, plus a tail
+                               row of max_points rounded up to 4, less 4 */
   int ctas;                 /* blocks of the cooperative launch */
   int threads;              /* threads per block */
   int64_t points_per_cta;   /* contiguous points each block owns */

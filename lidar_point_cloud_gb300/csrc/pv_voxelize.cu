@@ -71,10 +71,24 @@ static_assert(kWarps <= 32 && kWarps % 16 == 0, "warp 0 scans one value per warp
 constexpr int kMinBlocksPerSM = 1024 / kThreads;
 constexpr int kMaxCtas = 1024;             // blocks per launch (prefix lives in shared memory)
 constexpr int kFlagUnroll = 4;             // block-wide tiles in flight when flagging
+#ifndef PV_HEAD_ENTRIES
+#define PV_HEAD_ENTRIES 4
+#endif
+// List positions 0 .. kHead-1 of every slot sit together in one dense head
+// array (kHead * 8 bytes per slot), positions kHead .. max_points-1 in a
+// separate tail array: most pillars hold a few groups, so the random
+// accesses of a launch stay inside a table a fraction of the size.
+constexpr int kHead = PV_HEAD_ENTRIES;
+static_assert(kHead == 4 || kHead == 8, "head rows are 32 or 64 bytes");
 #ifndef PV_EMIT_UNROLL
 #define PV_EMIT_UNROLL 4
 #endif
 constexpr int kEmitUnroll = PV_EMIT_UNROLL;  // pillars in flight per warp when emitting
+#ifndef PV_INSERT_UNROLL
+#define PV_INSERT_UNROLL 1
+#endif
+constexpr int kInsertUnroll = PV_INSERT_UNROLL;  // records in flight per thread when inserting
+static_assert(kEmitUnroll >= 1 && kEmitUnroll <= 16 && 32 % kEmitUnroll == 0, "emit batches tile a warp");
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded spins: 1 s
 constexpr int64_t kMaxAxisCells = int64_t(1) << 24;
 
@@ -98,12 +112,13 @@ struct KParams {
   float g_xf, g_yf, g_zf;
   int g_x;
   int K;             // max_points
-  int KS;            // list stride in uint32 entries (K rounded up to 4)
+  int KT;            // tail entries per slot (max_points rounded up to 4, less kHead; >= 0)
   int max_voxels;
   int hash_mode;
   unsigned int bar_extra;  // test hook: extra arrivals the first barrier waits for
   unsigned int table_mask;
-  unsigned long long* lists;  // [T][KS] entries (leader index << 32) | (offset << 11) | size
+  unsigned long long* lists;  // heads [T][kHead], then tails [T][KT]; entries (leader << 32) | info
+  unsigned long long* tails;  // lists + T * kHead
   int32_t* keys;
   int32_t* slot_of_point;
   int32_t* firsts;
@@ -157,6 +172,11 @@ constexpr int kStamps = 8;
 __device__ unsigned long long g_phase_ns[kStampCtas][kStamps];
 __device__ unsigned long long g_p1_ns[kStampCtas][kStamps];
 __device__ unsigned long long g_insert_stats[4];  // inserts, atomics, rejected up front, max atomics
+__device__ unsigned long long g_ins_ns[kStampCtas][4];  // thread 0's first insert: start, records, heads, done
+__device__ __forceinline__ void pv_wait_reg(unsigned int v) {
+  unsigned int d;
+  asm volatile("mov.b32 %0, %1;" : "=r"(d) : "r"(v));
+}
 #define PV_SUB(k)                                                            \
   do {                                                                       \
     if (first_tile) {                                                        \
@@ -331,26 +351,39 @@ __device__ __forceinline__ int claim_slot(int32_t* keys, unsigned int mask, int 
 // plus the length of the strictly increasing run of entries read below x
 // that come from other chunks (leaders outside [cbase, cbase + cspan)):
 // distinct smaller leaders, none counted twice.  Values in a list only ever
-// decrease, so an entry read below x stays below x, and a position K-1 read
-// below x keeps x out altogether.
+// decrease, so an entry read below x stays below x.  Only the head row is
+// read up front; the tail only while the run goes on.
+//
+// A group whose pillar has K points before it never contributes a point.
+// The groups of that run lie in other tiles than x's and have smaller
+// leaders, so all their points come before x's: when their sizes add up to K
+// the entry is dropped.  Dropping such entries changes nothing for the
+// others: every entry compares below a dropped one, so the needed entries
+// (those with fewer than K points before them) cascade exactly as if it had
+// never existed and end in positions 0, 1, ... in order, which is all the
+// emit reads before it has K points.
 __device__ __forceinline__ unsigned long long ull_of(uint32_t lo, uint32_t hi) {
   return (static_cast<unsigned long long>(hi) << 32) | lo;
 }
 
-__device__ __forceinline__ void list_insert(unsigned long long* L, int K, int KS, unsigned long long x,
-                                            int crank, uint32_t cbase, uint32_t cspan) {
+// A slot's list: positions 0 .. kHead-1 in its head row, the rest in its tail row.
+struct ListRef {
+  unsigned long long* head;
+  unsigned long long* tail;
+  __device__ __forceinline__ unsigned long long* at(int k) const { return k < kHead ? head + k : tail + (k - kHead); }
+};
+
+__device__ __forceinline__ ListRef list_of(const KParams& p, int slot) {
+  return ListRef{p.lists + static_cast<size_t>(slot) * kHead, p.tails + static_cast<size_t>(slot) * p.KT};
+}
+
+// h: the list's head row, read by the caller (any time earlier: a stale
+// copy only shortens the run).
+__device__ __forceinline__ void list_insert(const ListRef& L, const uint4 (&h)[kHead / 2], int K, int KT,
+                                            unsigned long long x, int crank, uint32_t cbase, uint32_t cspan) {
   const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-  const unsigned long long last = __ldcg(L + (K - 1));
-  uint4 q[4];  // 8 entries per round trip
-#pragma unroll
-  for (int t = 0; t < 4; ++t) q[t] = (2 * t < KS) ? __ldcg(reinterpret_cast<const uint4*>(L + 2 * t)) : e4;
-  if (last < x) {
-#ifdef PV_INSTRUMENT_INSERTS
-    atomicAdd(&g_insert_stats[2], 1ull);
-#endif
-    return;
-  }
   int a = 0;
+  unsigned int before = 0;  // points in the run's groups
   unsigned long long prev = 0;
   bool run = true;
   auto step = [&](unsigned long long y) {
@@ -358,31 +391,39 @@ __device__ __forceinline__ void list_insert(unsigned long long* L, int K, int KS
     if (y < x && (a == 0 || y > prev)) {
       prev = y;
       ++a;
+      before += static_cast<unsigned int>(y) & 2047u;
     } else {
       run = false;
     }
   };
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    step(ull_of(q[t].x, q[t].y));
-    step(ull_of(q[t].z, q[t].w));
+  for (int t = 0; t < kHead / 2; ++t) {
+    step(ull_of(h[t].x, h[t].y));
+    step(ull_of(h[t].z, h[t].w));
   }
-  for (int e = 8; run && e < K; e += 8) {
+  for (int e = 0; run && kHead + e < K && before < static_cast<unsigned int>(K); e += 8) {  // tail: 8 per trip
+    uint4 q[4];
 #pragma unroll
     for (int t = 0; t < 4; ++t)
-      q[t] = (e + 2 * t < KS) ? __ldcg(reinterpret_cast<const uint4*>(L + e + 2 * t)) : e4;
+      q[t] = (e + 2 * t < KT) ? __ldcg(reinterpret_cast<const uint4*>(L.tail + e + 2 * t)) : e4;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       step(ull_of(q[t].x, q[t].y));
       step(ull_of(q[t].z, q[t].w));
     }
   }
+  if (before >= static_cast<unsigned int>(K)) {
+#ifdef PV_INSTRUMENT_INSERTS
+    atomicAdd(&g_insert_stats[2], 1ull);
+#endif
+    return;
+  }
   // Stride padding past K reads empty, so a >= K only if K entries are below x.
 #ifdef PV_INSTRUMENT_INSERTS
   unsigned long long n_atomics = 0;
 #endif
   for (int k = a + crank; k < K; ++k) {
-    const unsigned long long old = atomicMin(L + k, x);
+    const unsigned long long old = atomicMin(L.at(k), x);
 #ifdef PV_INSTRUMENT_INSERTS
     ++n_atomics;
 #endif
@@ -407,18 +448,21 @@ __device__ __forceinline__ void list_insert(unsigned long long* L, int K, int KS
 constexpr int kTileHash = 2 * kThreads;
 
 constexpr int kChunkHash = 4096;   // chunk map positions (see chunk_rank)
-constexpr int kChunkProbes = 64;
+#ifndef PV_CHUNK_PROBES
+#define PV_CHUNK_PROBES 8
+#endif
+constexpr int kChunkProbes = PV_CHUNK_PROBES;  // a full chunk map costs this many probes per lookup
 
 // Dynamic shared memory of the kernel: two tile maps, used by alternate
 // tiles so one can be emptied while the other is filled.
-constexpr int kMapBytes = kTileHash * kWarps + kTileHash * 4 + kTileHash * 2;
+constexpr int kMapBytes = kTileHash * kWarps + kTileHash * 4 + kTileHash * 4;
 constexpr int kDynSmem = 2 * kMapBytes + 2 * 4 * kChunkHash;
 static_assert(kMapBytes % 16 == 0, "maps stay 16-byte aligned");
 
 struct TileMap {
   unsigned int* cnt;         // [kTileHash][kWarps / 4] packed byte counters
   int* key;                  // [kTileHash], -1 = free
-  unsigned short* off;       // [kTileHash] group offset in the tile layout
+  unsigned int* off;         // [kTileHash] (rows to write << 16) | group offset in the tile layout
   unsigned int* layout;      // rows handed out in the tile layout
 };
 
@@ -426,7 +470,7 @@ __device__ __forceinline__ TileMap tile_map(unsigned char* base, unsigned int* l
   TileMap m;
   m.cnt = reinterpret_cast<unsigned int*>(base);
   m.key = reinterpret_cast<int*>(base + kTileHash * kWarps);
-  m.off = reinterpret_cast<unsigned short*>(base + kTileHash * kWarps + kTileHash * 4);
+  m.off = reinterpret_cast<unsigned int*>(base + kTileHash * kWarps + kTileHash * 4);
   m.layout = layout;
   return m;
 }
@@ -455,19 +499,24 @@ __device__ __forceinline__ int tile_claim(const TileMap& m, int slot) {
   return -1;
 }
 
-// Chunk map: pillar -> number of this block's tile groups seen so far.
-// Tiles of a chunk are grouped one after the other, so the count a tile
-// group reads is its rank among the chunk's groups of the pillar.  When the
-// map is full the rank falls back to 0, which is still a valid lower bound.
+// Chunk map: pillar -> (tile groups << 16) | points of this block's chunk
+// seen so far.  Tiles of a chunk are grouped one after the other, so what a
+// tile group reads is its rank among the chunk's groups of the pillar and the
+// number of the pillar's points in earlier tiles of the chunk.  Both are
+// exact while they matter: a group is kept only with fewer than max_points
+// (<= 1024) points before it, so neither field has wrapped by then; after
+// that the values only decide to drop the group.  When the map is full both
+// fall back to 0, which is still a valid lower bound.
 
-__device__ __forceinline__ int chunk_rank(int* ckey, int* ccnt, int slot) {
+__device__ __forceinline__ unsigned int chunk_rank(int* ckey, unsigned int* ccnt, int slot, unsigned int size) {
   unsigned int h = mix32(static_cast<unsigned int>(slot) ^ 0x9e3779b9u) & (kChunkHash - 1);
   for (int probe = 0; probe < kChunkProbes; ++probe) {
-    const int cur = atomicCAS(ckey + h, -1, slot);
-    if (cur == -1 || cur == slot) return atomicAdd(ccnt + h, 1);
+    int cur = *reinterpret_cast<volatile int*>(ckey + h);  // a plain read first: most probes find a key
+    if (cur == -1) cur = atomicCAS(ckey + h, -1, slot);
+    if (cur == -1 || cur == slot) return atomicAdd(ccnt + h, (1u << 16) | size);
     h = (h + 1) & (kChunkHash - 1);
   }
-  return 0;
+  return 0u;
 }
 
 // Byte counters at map position h: *before = warps 0 .. warp-1, *total = all.
@@ -507,6 +556,153 @@ __device__ __forceinline__ int slot_of_rank(const KParams& p, const unsigned int
     if (s_prefix[mid] <= r) lo = mid; else hi = mid;
   }
   return __ldcg(p.firsts + static_cast<long long>(lo) * p.chunk + (r - s_prefix[lo]));
+}
+
+// The first four positions of a pillar's list, as one lane reads them.
+// few: the pillar's points all come from groups among them: either the list
+// ends there (a group is missing after ng present ones and the groups hold
+// fewer than max_points points: a needed group is never missing before
+// another, so nothing follows) or the first ng groups already hold
+// max_points points (filled; unused entries may then follow anywhere).
+struct Head {
+  unsigned long long e[4];
+  unsigned int n;   // points taken: min(points of the first ng groups, max_points)
+  int ng;           // groups the points come from (0: none present)
+  bool few;
+  bool filled;
+};
+
+__device__ __forceinline__ Head read_head(const KParams& p, const unsigned long long* L, bool valid) {
+  Head h;
+  uint4 a = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty), b = a;
+  if (valid) {  // positions 0..3 (head row; positions past max_points are never written and read empty)
+    a = __ldcg(reinterpret_cast<const uint4*>(L));
+    b = __ldcg(reinterpret_cast<const uint4*>(L) + 1);
+  }
+  h.e[0] = ull_of(a.x, a.y);
+  h.e[1] = ull_of(a.z, a.w);
+  h.e[2] = ull_of(b.x, b.y);
+  h.e[3] = ull_of(b.z, b.w);
+  unsigned int cum = 0;
+  int g = 0;
+  bool filled = false, gap_clean = true;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool good = h.e[j] != kEmpty64 && (h.e[j] >> 32) < static_cast<unsigned long long>(p.n);
+    if (!filled && g == j && good) {
+      cum += static_cast<unsigned int>(h.e[j]) & 2047u;
+      g = j + 1;
+      if (cum >= static_cast<unsigned int>(p.K)) filled = true;
+    } else if (!filled && h.e[j] != kEmpty64) {
+      gap_clean = false;  // something after a missing or bad position
+    }
+  }
+  h.ng = g;
+  h.filled = filled;
+  h.few = g > 0 && (filled || (g < 4 && gap_clean));
+  h.n = filled ? static_cast<unsigned int>(p.K) : cum;
+  return h;
+}
+
+// Source row (index into tile_rows) of output position e of the pillar
+// whose head lane u holds, or -1 for a zero row.  Every lane calls it with
+// the same u.
+__device__ __forceinline__ long long head_source(const Head& h, int u, unsigned int e) {
+  const int ng = __shfl_sync(0xffffffffu, h.ng, u);
+  const unsigned int n = __shfl_sync(0xffffffffu, h.n, u);
+  unsigned long long ge = 0;
+  unsigned int start = 0, run = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const unsigned long long ej = __shfl_sync(0xffffffffu, h.e[j], u);
+    if (j < ng && run <= e) {
+      ge = ej;
+      start = run;
+    }
+    run += static_cast<unsigned int>(ej) & 2047u;
+  }
+  if (e >= n) return -1;
+  return (static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1)) +
+         ((static_cast<unsigned int>(ge) >> 11) & 1023u) + (e - start);
+}
+
+// Writes the output row of a pillar from its whole list: groups in list
+// order, each group's points in index order, max_points at most, zeros
+// after them; empties every list position.  Returns the points written.
+// All 32 lanes call it with the same arguments.  With max_points <= 32 and
+// the groups in positions 0 .. G-1, lane e takes position e from the last
+// group whose running start is <= e; otherwise the groups are walked 32
+// list positions at a time.  An entry whose leader is out of range (never
+// in a clean table) is skipped and reported through *stale.
+__device__ unsigned int emit_groups(const KParams& p, const ListRef& L, float4* orow, int K, unsigned int lane,
+                                    bool* stale) {
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const unsigned long long raw = static_cast<int>(lane) < K ? __ldcg(L.at(lane)) : kEmpty64;
+  unsigned long long ent = raw;
+  if (ent != kEmpty64 && (ent >> 32) >= static_cast<unsigned long long>(p.n)) {
+    ent = kEmpty64;
+    *stale = true;
+  }
+  const unsigned int present = __ballot_sync(0xffffffffu, ent != kEmpty64);
+  unsigned int written = 0;
+  if (K <= 32 && (present & (present + 1u)) == 0u) {
+    const int G = __popc(present);
+    const unsigned int size = ent != kEmpty64 ? (static_cast<unsigned int>(ent) & 2047u) : 0u;
+    unsigned int incl = size;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= static_cast<unsigned int>(o)) incl += y;
+    }
+    const int gstart = static_cast<int>(incl - size);
+    const unsigned int all = __shfl_sync(0xffffffffu, incl, 31);
+    written = all < static_cast<unsigned int>(K) ? all : static_cast<unsigned int>(K);
+    const int e = static_cast<int>(lane);
+    int g = 0;
+#pragma unroll
+    for (int step = 16; step >= 1; step >>= 1) {
+      const int j = g + step;
+      const int st = __shfl_sync(0xffffffffu, gstart, j < 32 ? j : 31);
+      if (j < G && st <= e) g = j;
+    }
+    const unsigned long long ge = __shfl_sync(0xffffffffu, ent, g);
+    const int gs = __shfl_sync(0xffffffffu, gstart, g);
+    if (e < K) {
+      float4 row = z4;
+      if (static_cast<unsigned int>(e) < written) {
+        const long long tbase = static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1);
+        row = __ldcg(p.tile_rows + tbase + ((static_cast<unsigned int>(ge) >> 11) & 1023u) + (e - gs));
+      }
+      orow[e] = row;
+    }
+    if (raw != kEmpty64) *L.at(lane) = kEmpty64;
+    return written;
+  }
+  unsigned long long chunk = ent, chunk_raw = raw;
+  for (int g0 = 0; g0 < K; g0 += 32) {
+    if (g0 > 0) {
+      chunk_raw = (g0 + static_cast<int>(lane) < K) ? __ldcg(L.at(g0 + lane)) : kEmpty64;
+      chunk = chunk_raw;
+      if (chunk != kEmpty64 && (chunk >> 32) >= static_cast<unsigned long long>(p.n)) {
+        chunk = kEmpty64;
+        *stale = true;
+      }
+    }
+    const unsigned int here = __ballot_sync(0xffffffffu, chunk != kEmpty64);
+    for (unsigned int m = here; m != 0u && written < static_cast<unsigned int>(K); m &= m - 1u) {
+      const unsigned long long ge = __shfl_sync(0xffffffffu, chunk, __ffs(m) - 1);
+      const unsigned int info = static_cast<unsigned int>(ge);
+      const unsigned int room = static_cast<unsigned int>(K) - written;
+      const unsigned int n = (info & 2047u) < room ? (info & 2047u) : room;
+      const long long base =
+          (static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1)) + ((info >> 11) & 1023u);
+      for (unsigned int j = lane; j < n; j += 32) orow[written + j] = __ldcg(p.tile_rows + base + j);
+      written += n;
+    }
+    if (chunk_raw != kEmpty64) *L.at(g0 + lane) = kEmpty64;
+  }
+  for (unsigned int e = written + lane; e < static_cast<unsigned int>(K); e += 32) orow[e] = z4;
+  return written;
 }
 
 // ------------------------------------------------------------ the kernel
@@ -564,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     float4 q = (tb + tid < end) ? __ldg(p.points + tb + tid) : z4;
     const bool multi = end - begin > kThreads;  // more than one tile: second map and chunk map in use
     int* ckey = reinterpret_cast<int*>(s_dyn + 2 * kMapBytes);
-    int* ccnt = ckey + kChunkHash;
+    unsigned int* ccnt = reinterpret_cast<unsigned int*>(ckey + kChunkHash);
     {  // tile map 0 empty (counters zero, keys -1); map 1 and the chunk map only if used
       uint4* d4 = reinterpret_cast<uint4*>(s_dyn);
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -640,10 +836,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         trank += __popc(peers & lanemask_lt());
       }
       const bool lead = slot >= 0 && trank == 0;
-      const int crank = (lead && multi) ? chunk_rank(ckey, ccnt, slot) : 0;
+      const unsigned int cseen = (lead && multi) ? chunk_rank(ckey, ccnt, slot, tot) : 0u;
+      const int crank = static_cast<int>(cseen >> 16);
       {  // group offsets and record slots: one shared-memory atomic per warp each
         const unsigned int need = lead ? tot : 0u;
-        const unsigned int wants = (lead && crank < K) ? 1u : 0u;
+        // A group with max_points of its pillar's points before it in this
+        // chunk (or max_points groups) can never be kept: not recorded.
+        const unsigned int wants =
+            (lead && crank < K && (cseen & 0xFFFFu) < static_cast<unsigned int>(K)) ? 1u : 0u;
         unsigned int incl = need, rincl = wants;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -665,8 +865,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         rbase = __shfl_sync(0xffffffffu, rbase, 31);
         if (lead) {
           const unsigned int off = base + incl - need;
-          tm.off[h] = static_cast<unsigned short>(off);
-          if (crank < K) {  // a group ranked K or later in its own chunk can never be kept
+          // Rows of the group that can ever be emitted: those with fewer than
+          // max_points of the pillar's points before them in the chunk.
+          const unsigned int cpts = cseen & 0xFFFFu;
+          const unsigned int room = cpts < static_cast<unsigned int>(K) ? static_cast<unsigned int>(K) - cpts : 0u;
+          tm.off[h] = ((tot < room ? tot : room) << 16) | off;
+          if (wants) {
             const long long rj = begin + rbase + rincl - wants;
             p.firsts[rj] = slot;  // the record's slot (firsts is rewritten after the barrier)
             p.recs[rj] = (static_cast<unsigned long long>(i) << 32) |
@@ -677,7 +881,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       if (i < end) p.slot_of_point[i] = slot < 0 ? -1 : (lead ? (slot | kLeaderBit) : slot);
       __syncthreads();  // (B) group offsets handed out; the previous map is empty
       PV_SUB(3);
-      if (slot >= 0) p.tile_rows[tb + tm.off[h] + trank] = q;
+      if (slot >= 0) {
+        const unsigned int ow = tm.off[h];
+        if (trank < (ow >> 16)) p.tile_rows[tb + (ow & 0xFFFFu) + trank] = q;
+      }
       PV_SUB(4);
       q = qn;
     }
@@ -686,12 +893,47 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     if (tid == 0 && cta < kStampCtas) g_p1_ns[cta][5] = global_timer_ns();
 #endif
     const unsigned int nrec = s_nrec;
-    for (unsigned int j = tid; j < nrec; j += kThreads) {
-      const int rs = __ldcg(p.firsts + begin + j);
-      const unsigned long long entry = __ldcg(p.recs + begin + j);
-      const int crank = static_cast<int>((entry >> 21) & 2047u);
-      list_insert(p.lists + static_cast<size_t>(rs) * p.KS, K, p.KS, entry, crank, static_cast<uint32_t>(begin),
-                  static_cast<uint32_t>(end - begin));
+    // kInsertUnroll records per thread at a time: their records, then their
+    // head rows, are read together before the cascades run one by one.
+    for (unsigned int j0 = tid; j0 < nrec; j0 += kInsertUnroll * kThreads) {
+#ifdef PV_INSTRUMENT
+      if (tid == 0 && j0 == 0 && cta < kStampCtas) g_ins_ns[cta][0] = global_timer_ns();
+#endif
+      int rs[kInsertUnroll];
+      unsigned long long entry[kInsertUnroll];
+#pragma unroll
+      for (int u = 0; u < kInsertUnroll; ++u) {
+        const unsigned int j = j0 + u * kThreads;
+        rs[u] = j < nrec ? __ldcg(p.firsts + begin + j) : -1;
+        entry[u] = j < nrec ? __ldcg(p.recs + begin + j) : 0ull;
+      }
+#ifdef PV_INSTRUMENT
+      if (tid == 0 && j0 == 0 && cta < kStampCtas) {
+        pv_wait_reg(static_cast<unsigned int>(rs[0]) ^ static_cast<unsigned int>(entry[0]));
+        g_ins_ns[cta][1] = global_timer_ns();
+      }
+#endif
+      uint4 h[kInsertUnroll][kHead / 2];
+#pragma unroll
+      for (int u = 0; u < kInsertUnroll; ++u)
+#pragma unroll
+        for (int t = 0; t < kHead / 2; ++t)
+          h[u][t] = rs[u] >= 0 ? __ldcg(reinterpret_cast<const uint4*>(p.lists + static_cast<size_t>(rs[u]) * kHead) + t)
+                               : make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+#ifdef PV_INSTRUMENT
+      if (tid == 0 && j0 == 0 && cta < kStampCtas) {
+        pv_wait_reg(h[0][0].x ^ h[0][kHead / 2 - 1].w);
+        g_ins_ns[cta][2] = global_timer_ns();
+      }
+#endif
+#pragma unroll
+      for (int u = 0; u < kInsertUnroll; ++u)
+        if (rs[u] >= 0)
+          list_insert(list_of(p, rs[u]), h[u], K, p.KT, entry[u], static_cast<int>((entry[u] >> 21) & 2047u),
+                      static_cast<uint32_t>(begin), static_cast<uint32_t>(end - begin));
+#ifdef PV_INSTRUMENT
+      if (tid == 0 && j0 == 0 && cta < kStampCtas) g_ins_ns[cta][3] = global_timer_ns();
+#endif
     }
     PV_STAMP(1);
     alive = grid_sync(p.ctl, bar_target + p.bar_extra, &s_flag);
@@ -716,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       for (int u = 0; u < kFlagUnroll; ++u) {
         // Only a tile-group leader can be its pillar's first point.
         head[u] = (s[u] >= 0 && (s[u] & kLeaderBit))
-                      ? static_cast<uint32_t>(__ldcg(p.lists + static_cast<size_t>(s[u] & ~kLeaderBit) * p.KS) >> 32)
+                      ? static_cast<uint32_t>(__ldcg(p.lists + static_cast<size_t>(s[u] & ~kLeaderBit) * kHead) >> 32)
                       : kEmpty;
         s[u] = s[u] >= 0 ? (s[u] & ~kLeaderBit) : -1;
       }
@@ -773,162 +1015,108 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     V = total < M ? total : M;
     PV_STAMP(4);
 
-    // ---- phase 2c: output rows.  Every warp of the grid takes a contiguous
-    // range of ranks (so its output rows are contiguous), kEmitUnroll at a
-    // time.  A pillar's points are its groups, concatenated in list order:
-    // lane g holds group g (leader index, tile offset, size); output position
-    // e belongs to the last group whose running start is <= e.
+    // ---- phase 2c: empty the slots of pillars past the budget (ranks M..total-1),
+    // before the output rows load the memory system with writes:
+    // a list known to end inside positions 0..3 loses those, any other list
+    // every position.
+    for (long long r0 = static_cast<long long>(M) + gwarp * 32; r0 < total; r0 += nwarps * 32) {
+      const long long r = r0 + lane;
+      const bool valid = r < total;
+      const int slot = valid ? slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r)) : 0;
+      unsigned long long* L = p.lists + static_cast<size_t>(slot) * kHead;  // head row
+      const Head hd = read_head(p, L, valid);
+      const bool short_list = valid && hd.few && !hd.filled;
+      if (short_list) {
+        const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+        reinterpret_cast<uint4*>(L)[0] = e4;
+        reinterpret_cast<uint4*>(L)[1] = e4;
+      }
+      if (valid && p.hash_mode) p.keys[slot] = kNoKey;
+      for (unsigned int m = __ballot_sync(0xffffffffu, valid && !short_list); m != 0u; m &= m - 1u) {
+        const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, __ffs(m) - 1));
+        for (int e = static_cast<int>(lane); e < K; e += 32) *Lu.at(e) = kEmpty64;
+      }
+    }
+    PV_STAMP(5);
+
+    // ---- phase 2d: output rows.  Every warp of the grid takes a contiguous
+    // range of ranks (so its output rows are contiguous) and works through
+    // it 32 ranks at a time.  Lane l finds the slot of rank r0 + l and reads
+    // list positions 0..3 (one round trip each for 32 pillars).  A pillar
+    // whose points all come from those groups (its list ends inside them, or
+    // they already hold max_points points) is copied by the warp kEmitUnroll
+    // pillars at a time; the others are emitted one by one from their whole
+    // list.
     bool stale = false;
     const long long per_warp = (static_cast<long long>(V) + nwarps - 1) / nwarps;
     const long long rw0 = gwarp * per_warp;
     const long long rw1 = rw0 + per_warp < static_cast<long long>(V) ? rw0 + per_warp : static_cast<long long>(V);
-    unsigned int owner = 0;  // block whose first points hold rank rw0 (binary search once)
-    if (rw0 < rw1) {
-      unsigned int lo = 0, hi = P;  // s_prefix[lo] <= rw0 < s_prefix[hi]
-      while (hi - lo > 1) {
-        const unsigned int mid = (lo + hi) >> 1;
-        if (s_prefix[mid] <= static_cast<unsigned int>(rw0)) lo = mid; else hi = mid;
-      }
-      owner = lo;
-    }
-    for (long long r0 = rw0; r0 < rw1; r0 += kEmitUnroll) {
-      // Lane u < kEmitUnroll finds the slot of rank r0 + u (walking the owner forward).
-      int my_slot = 0;
-      unsigned int my_owner = owner;
-      if (static_cast<int>(lane) < kEmitUnroll && r0 + lane < rw1) {
-        const unsigned int r = static_cast<unsigned int>(r0 + lane);
-        while (s_prefix[my_owner + 1] <= r) ++my_owner;  // ranks ascend
-        my_slot = __ldcg(p.firsts + static_cast<long long>(my_owner) * p.chunk + (r - s_prefix[my_owner]));
-      }
-      owner = __shfl_sync(0xffffffffu, my_owner, kEmitUnroll - 1);
-      int slot[kEmitUnroll];
-      bool ok[kEmitUnroll];
-      unsigned long long ent[kEmitUnroll];
+    for (long long r0 = rw0; r0 < rw1; r0 += 32) {
+      const long long r = r0 + lane;
+      const bool valid = r < rw1;
+      int slot = 0;
+      if (valid) slot = slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r));
+      unsigned long long* L = p.lists + static_cast<size_t>(slot) * kHead;  // head row
+      Head hd = read_head(p, L, valid);
+      int key = slot;
+      if (valid && p.hash_mode) key = __ldcg(p.keys + slot);
+      const bool few = valid && hd.few;
+      const unsigned int cnt0 = few ? hd.n : 0u;
+      float4* const orow0 = p.out_voxels + static_cast<size_t>(r0) * K;
+      unsigned int cnt = cnt0;
+      const unsigned int fmask = __ballot_sync(0xffffffffu, few);
+      // Pillars served by their first groups, kEmitUnroll at a time: lane e copies position e.
+      for (int u0 = 0; u0 < 32; u0 += kEmitUnroll) {
+        if (((fmask >> u0) & ((1u << kEmitUnroll) - 1u)) == 0u) continue;
+        float4 v[kEmitUnroll];
 #pragma unroll
-      for (int u = 0; u < kEmitUnroll; ++u) {
-        ok[u] = r0 + u < rw1;
-        slot[u] = __shfl_sync(0xffffffffu, my_slot, u);
-        // Group descriptors: entry g of the list on lane g (leader, offset, size).
-        ent[u] = (ok[u] && static_cast<int>(lane) < K) ? __ldcg(p.lists + static_cast<size_t>(slot[u]) * p.KS + lane)
-                                                       : kEmpty64;
-      }
-      unsigned int cnt[kEmitUnroll];
-#pragma unroll
-      for (int u = 0; u < kEmitUnroll; ++u) {
-        const long long r = r0 + u;
-        float4* orow = p.out_voxels + static_cast<size_t>(r) * K;
-        unsigned long long* L = p.lists + static_cast<size_t>(slot[u]) * p.KS;
-        if (static_cast<uint32_t>(ent[u] >> 32) != kEmpty && (ent[u] >> 32) >= static_cast<unsigned long long>(p.n)) {
-          ent[u] = kEmpty64;  // never in a clean table
-          stale = true;
+        for (int j = 0; j < kEmitUnroll; ++j) {
+          const long long src = head_source(hd, u0 + j, lane);
+          v[j] = src >= 0 ? __ldcg(p.tile_rows + src) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const unsigned int present = __ballot_sync(0xffffffffu, ent[u] != kEmpty64);  // lanes 0 .. G-1
-        unsigned int written = 0;
-        if (ok[u] && present != 0u && (present & (present + 1u)) == 0u && (present == 1u || K <= 32)) {
-          // Up to 32 groups, all on the warp's lanes.
-          const int G = __popc(present);
-          if (G == 1) {  // the common case: the pillar's first points are one tile group
-            const unsigned int info = static_cast<unsigned int>(ent[u]);
-            const unsigned int n = (info & 2047u) < static_cast<unsigned int>(K) ? (info & 2047u) : static_cast<unsigned int>(K);
-            const long long base = (static_cast<long long>(ent[u] >> 32) & ~static_cast<long long>(kThreads - 1)) +
-                                   ((info >> 11) & 1023u);
-            const long long b0 = __shfl_sync(0xffffffffu, base, 0);
-            const unsigned int n0 = __shfl_sync(0xffffffffu, n, 0);
-            for (int e = static_cast<int>(lane); e < K; e += 32)
-              orow[e] = static_cast<unsigned int>(e) < n0 ? __ldcg(p.tile_rows + b0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            written = n0;
-          } else {  // several groups: position e comes from the last group starting at or before e
-            const unsigned int size = ent[u] != kEmpty64 ? (static_cast<unsigned int>(ent[u]) & 2047u) : 0u;
-            unsigned int incl = size;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= static_cast<unsigned int>(o)) incl += y;
-            }
-            const int gstart = static_cast<int>(incl - size);
-            const unsigned int all = __shfl_sync(0xffffffffu, incl, 31);
-            written = all < static_cast<unsigned int>(K) ? all : static_cast<unsigned int>(K);
-            const int e = static_cast<int>(lane);  // K <= 32 here
-            int g = 0;
-#pragma unroll
-            for (int step = 16; step >= 1; step >>= 1) {
-              const int j = g + step;
-              const int st = __shfl_sync(0xffffffffu, gstart, j < 32 ? j : 31);
-              if (j < G && st <= e) g = j;
-            }
-            const unsigned long long ge = __shfl_sync(0xffffffffu, ent[u], g);
-            const int gs = __shfl_sync(0xffffffffu, gstart, g);
-            if (e < K) {
-              float4 row = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (static_cast<unsigned int>(e) < written) {
-                const long long tbase = static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1);
-                row = __ldcg(p.tile_rows + tbase + ((static_cast<unsigned int>(ge) >> 11) & 1023u) + (e - gs));
-              }
-              orow[e] = row;
+        for (int j = 0; j < kEmitUnroll; ++j)
+          if (((fmask >> (u0 + j)) & 1u) && static_cast<int>(lane) < K) orow0[static_cast<size_t>(u0 + j) * K + lane] = v[j];
+        if (K > 32) {  // positions 32 .. K-1 (every lane runs the same trips: head_source shuffles)
+          const unsigned int k32 = (static_cast<unsigned int>(K) + 31u) & ~31u;
+          for (int j = 0; j < kEmitUnroll; ++j) {
+            if (!((fmask >> (u0 + j)) & 1u)) continue;
+            for (unsigned int e = lane + 32; e < k32; e += 32) {
+              const long long src = head_source(hd, u0 + j, e);
+              if (e < static_cast<unsigned int>(K))
+                orow0[static_cast<size_t>(u0 + j) * K + e] = src >= 0 ? __ldcg(p.tile_rows + src) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
-          if (ent[u] != kEmpty64) L[lane] = kEmpty64;
-        } else if (ok[u]) {
-          // General case (max_points > 32 with more than one group, or many groups):
-          // walk the list 32 entries at a time and copy each group's run.
-          unsigned long long chunk = ent[u];
-          for (int g0 = 0; g0 < K; g0 += 32) {
-            if (g0 > 0) chunk = (g0 + static_cast<int>(lane) < K) ? __ldcg(L + g0 + lane) : kEmpty64;
-            const unsigned int here = __ballot_sync(0xffffffffu, chunk != kEmpty64);
-            if (here == 0u) break;
-            for (unsigned int m = here; m != 0u && written < static_cast<unsigned int>(K); m &= m - 1u) {
-              const unsigned long long ge = __shfl_sync(0xffffffffu, chunk, __ffs(m) - 1);
-              const unsigned int info = static_cast<unsigned int>(ge);
-              const unsigned int room = static_cast<unsigned int>(K) - written;
-              const unsigned int n = (info & 2047u) < room ? (info & 2047u) : room;
-              const long long base =
-                  (static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1)) + ((info >> 11) & 1023u);
-              for (unsigned int j = lane; j < n; j += 32) orow[written + j] = __ldcg(p.tile_rows + base + j);
-              written += n;
-            }
-            if (chunk != kEmpty64) L[g0 + lane] = kEmpty64;
-          }
-          for (unsigned int e = written + lane; e < static_cast<unsigned int>(K); e += 32)
-            orow[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        cnt[u] = written;
-      }
-      // Coordinates and counts of the batch: lane 3u + c writes coordinate c of pillar u,
-      // lane u writes count u.
-      if (static_cast<int>(lane) < 3 * kEmitUnroll) {
-        const int u = static_cast<int>(lane) / 3, c = static_cast<int>(lane) % 3;
-        int su = 0;
-#pragma unroll
-        for (int v = 0; v < kEmitUnroll; ++v) su = (v == u) ? slot[v] : su;
-        if (r0 + u < rw1) {
-          const int key = p.hash_mode ? __ldcg(p.keys + su) : su;
-          p.out_coords[3 * static_cast<size_t>(r0 + u) + c] = c == 0 ? 0 : (c == 1 ? key / p.g_x : key % p.g_x);
         }
       }
-      __syncwarp();  // hashed keys are read above before lane u empties them below
-#pragma unroll
-      for (int u = 0; u < kEmitUnroll; ++u) {
-        if (lane == static_cast<unsigned int>(u) && ok[u]) {
-          p.out_counts[static_cast<size_t>(r0 + u)] = static_cast<int32_t>(cnt[u]);
-          if (p.hash_mode) p.keys[slot[u]] = kNoKey;
+      // A list whose first groups fill the pillar may hold unused entries
+      // anywhere after them: empty every position.
+      for (unsigned int m = __ballot_sync(0xffffffffu, few && hd.filled); m != 0u; m &= m - 1u) {
+        const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, __ffs(m) - 1));
+        for (int e = static_cast<int>(lane); e < K; e += 32) *Lu.at(e) = kEmpty64;
+      }
+      // Everything else, one pillar at a time from its whole list.
+      for (unsigned int m = __ballot_sync(0xffffffffu, valid && !few); m != 0u; m &= m - 1u) {
+        const int u = __ffs(m) - 1;
+        const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, u));
+        const unsigned int w = emit_groups(p, Lu, orow0 + static_cast<size_t>(u) * K, K, lane, &stale);
+        if (static_cast<int>(lane) == u) cnt = w;
+      }
+      if (valid) {
+        if (hd.ng == 0) stale = true;  // a ranked pillar always has its first group
+        if (few && !hd.filled) {  // the list held only these entries
+          const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+          reinterpret_cast<uint4*>(L)[0] = e4;
+          reinterpret_cast<uint4*>(L)[1] = e4;
         }
+        p.out_coords[3 * static_cast<size_t>(r)] = 0;
+        p.out_coords[3 * static_cast<size_t>(r) + 1] = key / p.g_x;
+        p.out_coords[3 * static_cast<size_t>(r) + 2] = key % p.g_x;
+        p.out_counts[static_cast<size_t>(r)] = static_cast<int32_t>(cnt);
+        if (p.hash_mode) p.keys[slot] = kNoKey;
       }
     }
     if (stale) atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
-    PV_STAMP(5);
-
-    // ---- phase 2d: empty the slots of pillars past the budget (ranks M..total-1).
-    for (long long r0 = static_cast<long long>(M) + gwarp * 32; r0 < total; r0 += nwarps * 32) {
-      const long long r = r0 + lane;
-      const int mine = r < total ? slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r)) : -1;
-      for (int t = 0; t < 32; ++t) {
-        const int s = __shfl_sync(0xffffffffu, mine, t);
-        if (s < 0) break;  // ranks ascend with t, so the rest are past the end too
-        unsigned long long* L = p.lists + static_cast<size_t>(s) * p.KS;
-        for (int e = static_cast<int>(lane); e < K; e += 32) L[e] = kEmpty64;
-        if (p.hash_mode && lane == 0) p.keys[s] = kNoKey;
-      }
-    }
     PV_STAMP(6);
 
     // ---- phase 2e: zero rows V .. max_voxels-1 (all blocks share it).
@@ -999,7 +1187,7 @@ struct Plan {
   int64_t g[3];
   int mode;
   int64_t T;
-  int KS;
+  int KT;             // tail entries per slot
   int ctas;
   int64_t chunk;
   unsigned int mask;
@@ -1070,8 +1258,8 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   const int64_t cells = pl->g[0] * pl->g[1];
   const int64_t distinct_bound = std::max<int64_t>(1, std::min(N, cells));
   const int64_t hashed_T = next_pow2(std::max<int64_t>(2 * distinct_bound, 1024));
-  pl->KS = (K + 3) & ~3;
-  const int64_t direct_bytes = cells * pl->KS * 8;
+  pl->KT = std::max(0, ((K + 3) & ~3) - kHead);
+  const int64_t direct_bytes = cells * (kHead + pl->KT) * 8;
   int mode = o.table_mode;
   if (mode == 0) mode = (cells <= 2 * hashed_T && direct_bytes <= (int64_t(1) << 31)) ? 1 : 2;
   pl->mode = mode;
@@ -1083,7 +1271,7 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
     if (pl->T > (int64_t(1) << 30)) return PV_ERR_INVALID;  // slots stay below the leader bit
     pl->mask = static_cast<unsigned int>(pl->T - 1);
   }
-  pl->list_words = static_cast<size_t>(pl->T) * pl->KS;
+  pl->list_words = static_cast<size_t>(pl->T) * (kHead + pl->KT);
   pl->key_words = mode == 2 ? static_cast<size_t>(pl->T) : 0;
   const int per_sm = o.ctas_per_sm ? std::min(o.ctas_per_sm, dev.blocks_per_sm) : dev.blocks_per_sm;
   // The count scan after the second barrier takes one count per thread.
@@ -1239,12 +1427,13 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.g_zf = static_cast<float>(pl.g[2]);
   kp.g_x = static_cast<int>(pl.g[0]);
   kp.K = K;
-  kp.KS = pl.KS;
+  kp.KT = pl.KT;
   kp.max_voxels = M;
   kp.hash_mode = pl.mode == 2 ? 1 : 0;
   kp.bar_extra = pl.stall;
   kp.table_mask = pl.mask;
   kp.lists = ws->lists;
+  kp.tails = ws->lists + static_cast<size_t>(pl.T) * kHead;
   kp.keys = ws->keys;
   kp.slot_of_point = ws->slot_of_point;
   kp.firsts = ws->firsts;
@@ -1526,7 +1715,7 @@ int pv_query_plan(int64_t num_points, const float point_cloud_range[6], const fl
   for (int a = 0; a < 3; ++a) plan_out->grid[a] = pl.g[a];
   plan_out->table_mode = pl.mode;
   plan_out->table_slots = pl.T;
-  plan_out->list_stride = pl.KS;
+  plan_out->list_stride = kHead + pl.KT;
   plan_out->ctas = pl.ctas;
   plan_out->threads = kThreads;
   plan_out->points_per_cta = pl.chunk;
@@ -1594,6 +1783,13 @@ int pv_debug_p1_times(unsigned long long* out, int max_ctas) {
   const int n = max_ctas < kStampCtas ? max_ctas : kStampCtas;
   if (cudaMemcpyFromSymbol(out, g_p1_ns, sizeof(unsigned long long) * kStamps * n) != cudaSuccess)
     return PV_ERR_CUDA;
+  return PV_OK;
+}
+
+// Instrumented builds only: thread 0's first insert round, [max_ctas][4] stamps (ns).
+int pv_debug_ins_times(unsigned long long* out, int max_ctas) {
+  const int n = max_ctas < kStampCtas ? max_ctas : kStampCtas;
+  if (cudaMemcpyFromSymbol(out, g_ins_ns, sizeof(unsigned long long) * 4 * n) != cudaSuccess) return PV_ERR_CUDA;
   return PV_OK;
 }
 

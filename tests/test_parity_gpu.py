@@ -128,6 +128,38 @@ def test_one_pillar_many_points():
     assert assert_parity(pts, KR, KV, 32, 10) == 1
 
 
+def hot_cloud(n, hot_pillars, hot_frac, seed):
+    """A cloud over the KITTI-shaped range with hot_frac of its points inside
+    hot_pillars cells, in random order (the hot pillars overflow every cap)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    pts = synth.uniform(n, seed)
+    n_hot = int(n * hot_frac)
+    cells = rng.choice(432 * 496, size=hot_pillars, replace=False)
+    pick = cells[rng.integers(0, hot_pillars, size=n_hot)]
+    u = rng.random((n_hot, 2))
+    pts[:n_hot, 0] = (0.0 + ((pick % 432) + 0.05 + 0.9 * u[:, 0]) * 0.16).astype(np.float32)
+    pts[:n_hot, 1] = (-39.68 + ((pick // 432) + 0.05 + 0.9 * u[:, 1]) * 0.16).astype(np.float32)
+    return pts[rng.permutation(n)]
+
+
+@pytest.mark.parametrize("K", [32, 64, 200, 1024])
+def test_hot_pillars_large_caps_twice(K):
+    # Most groups of the hot pillars have max_points points before them and are
+    # dropped; a second call checks that the first left no list entry behind.
+    pts = hot_cloud(600_000, 8, 0.6, 31)
+    for _ in range(2):
+        assert_parity(pts, KR, KV, K, 2000)
+
+
+@pytest.mark.parametrize("K", [32, 1024])
+def test_chunk_point_counter_wraps(K):
+    # About 70,000 points of one pillar per block chunk: the 16-bit point count
+    # of the chunk map wraps; the groups it then lets through are never needed.
+    pts = hot_cloud(11_010_048, 1, 0.95, 32)
+    for _ in range(2):
+        assert_parity(pts, KR, KV, K, 500)
+
+
 @pytest.mark.parametrize("K,M", [(1, 1), (1, 16000), (32, 1), (5, 500), (33, 2000), (64, 3000), (100, 700)])
 def test_caps(K, M):
     pts, P = synth.make("kitti")
