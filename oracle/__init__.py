@@ -68,6 +68,11 @@ def _bind(lib):
         f, ctypes.c_int64, f, f, ctypes.c_int, ctypes.c_int, f, i32, i32, i32,
     ]
     lib.pv_oracle_voxelize.restype = ctypes.c_int
+    if hasattr(lib, "pv_oracle_voxelize3d"):  # absent from some planted-mistake builds
+        lib.pv_oracle_grid3d.argtypes = [f, f, i64]
+        lib.pv_oracle_grid3d.restype = ctypes.c_int
+        lib.pv_oracle_voxelize3d.argtypes = lib.pv_oracle_voxelize.argtypes
+        lib.pv_oracle_voxelize3d.restype = ctypes.c_int
     return lib
 
 
@@ -120,7 +125,23 @@ def bin_point(p, pc_range, voxel_size, lib=None):
     return tuple(int(c) for c in cell) if ok else None
 
 
-def voxelize(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int, lib=None):
+def grid3d(pc_range, voxel_size, lib=None) -> Tuple[int, Tuple[int, int, int]]:
+    """(status, (gx, gy, gz)) for true 3-D voxels (any z extent)."""
+    lib = lib or load()
+    r, v = _f32(pc_range), _f32(voxel_size)
+    g = np.zeros(3, dtype=np.int64)
+    st = lib.pv_oracle_grid3d(_fptr(r), _fptr(v), g.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+    return st, tuple(int(x) for x in g)
+
+
+def voxelize3d(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int, lib=None):
+    """The C++ oracle for true 3-D voxels: coordinates (z, y, x) of the voxel.
+    Same return values as :func:`voxelize`."""
+    return voxelize(points, pc_range, voxel_size, max_points, max_voxels, lib, three_d=True)
+
+
+def voxelize(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int, lib=None,
+             three_d: bool = False):
     """The C++ oracle.  Returns (status, voxels, coords, counts, V).
 
     ``voxels`` is [max_voxels, max_points, 4] float32, ``coords`` [max_voxels, 3]
@@ -134,7 +155,8 @@ def voxelize(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxe
     counts = np.empty((max(max_voxels, 0),), dtype=np.int32)
     num = np.zeros(1, dtype=np.int32)
     i32 = ctypes.POINTER(ctypes.c_int32)
-    st = lib.pv_oracle_voxelize(
+    fn = lib.pv_oracle_voxelize3d if three_d else lib.pv_oracle_voxelize
+    st = fn(
         _fptr(pts) if pts.size else None, pts.shape[0], _fptr(r), _fptr(v),
         int(max_points), int(max_voxels), _fptr(vox),
         coords.ctypes.data_as(i32), counts.ctypes.data_as(i32), num.ctypes.data_as(i32),
@@ -161,6 +183,12 @@ def grid_py(pc_range, voxel_size) -> Tuple[int, int, int]:
 
 def bin_numpy(points: np.ndarray, pc_range, voxel_size):
     """Per-point (valid mask, cx, cy) with float32 NumPy arithmetic."""
+    ok, cx, cy, _, g = cells_numpy(points, pc_range, voxel_size)
+    return ok, cx, cy, g
+
+
+def cells_numpy(points: np.ndarray, pc_range, voxel_size):
+    """Per-point (valid mask, cx, cy, cz, grid) with float32 NumPy arithmetic."""
     pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
     g = grid_py(pc_range, voxel_size)
     lo = np.asarray(pc_range[:3], dtype=np.float32)
@@ -173,13 +201,16 @@ def bin_numpy(points: np.ndarray, pc_range, voxel_size):
     ok = finite & np.all(q >= np.float32(0), axis=1) & np.all(q < gf, axis=1)
     cx = np.where(ok, q[:, 0], 0).astype(np.int64)
     cy = np.where(ok, q[:, 1], 0).astype(np.int64)
-    return ok, cx, cy, g
+    cz = np.where(ok, q[:, 2], 0).astype(np.int64)
+    return ok, cx, cy, cz, g
 
 
-def voxelize_numpy(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int):
-    """Vectorised restatement.  Returns (voxels, coords, counts, V)."""
+def voxelize_numpy(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int,
+                   three_d: bool = False):
+    """Vectorised restatement.  Returns (voxels, coords, counts, V).  With
+    ``three_d`` the z cell is part of the key and of the coordinates."""
     pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
-    ok, cx, cy, g = bin_numpy(pts, pc_range, voxel_size)
+    ok, cx, cy, cz, g = cells_numpy(pts, pc_range, voxel_size)
     vox = np.zeros((max_voxels, max_points, 4), dtype=np.float32)
     coords = np.zeros((max_voxels, 3), dtype=np.int32)
     counts = np.zeros((max_voxels,), dtype=np.int32)
@@ -187,6 +218,8 @@ def voxelize_numpy(points: np.ndarray, pc_range, voxel_size, max_points: int, ma
     if idx.size == 0:
         return vox, coords, counts, 0
     key = cy[idx] * g[0] + cx[idx]
+    if three_d:
+        key = key + cz[idx] * (g[0] * g[1])
     uniq, first_pos, inverse = np.unique(key, return_index=True, return_inverse=True)
     first_idx = idx[first_pos]
     order = np.argsort(first_idx, kind="stable")       # pillars by first point
@@ -203,7 +236,8 @@ def voxelize_numpy(points: np.ndarray, pc_range, voxel_size, max_points: int, ma
     V = int(min(uniq.size, max_voxels))
     counts[:V] = np.minimum(np.bincount(rank, minlength=uniq.size)[:V], max_points)
     kept_keys = uniq[order[:V]]
-    coords[:V, 1] = kept_keys // g[0]
+    coords[:V, 0] = kept_keys // (g[0] * g[1])
+    coords[:V, 1] = (kept_keys // g[0]) % g[1]
     coords[:V, 2] = kept_keys % g[0]
     return vox, coords, counts, V
 
@@ -212,8 +246,11 @@ def voxelize_numpy(points: np.ndarray, pc_range, voxel_size, max_points: int, ma
 # O(N^2) brute force from the definition, plain Python loops (tiny N only).
 # --------------------------------------------------------------------------
 
-def voxelize_bruteforce(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int):
-    """Definition written out point by point.  Returns (voxels, coords, counts, V)."""
+def voxelize_bruteforce(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int,
+                        three_d: bool = False):
+    """Definition written out point by point.  Returns (voxels, coords, counts, V).
+    A key is the tuple of the cells that identify the pillar (cy, cx) or, with
+    ``three_d``, the voxel (cz, cy, cx)."""
     pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
     g = grid_py(pc_range, voxel_size)
     lo = [np.float32(pc_range[a]) for a in range(3)]
@@ -233,7 +270,7 @@ def voxelize_bruteforce(points: np.ndarray, pc_range, voxel_size, max_points: in
                     else:
                         break
                 if len(cells) == 3:
-                    key = cells[1] * g[0] + cells[0]
+                    key = (cells[2], cells[1], cells[0]) if three_d else (0, cells[1], cells[0])
             keys.append(key)
     first = {}
     for i, k in enumerate(keys):
@@ -251,6 +288,6 @@ def voxelize_bruteforce(points: np.ndarray, pc_range, voxel_size, max_points: in
         if rank < max_voxels and pos < max_points:
             vox.view(np.uint32)[rank, pos] = pts.view(np.uint32)[i]
             counts[rank] += 1
-            coords[rank] = (0, k // g[0], k % g[0])
+            coords[rank] = k
     V = min(len(first), max_voxels)
     return vox, coords, counts, V

@@ -124,31 +124,27 @@ int pv_oracle_bin_point(const float p[4], const float range[6],
 //   out_counts   [max_voxels] int32
 //   out_num      number of pillars V written
 // Every output element is written: zero wherever no point lands.
-int pv_oracle_voxelize(const float* points, int64_t N, const float range[6],
-                       const float voxel_size[3], int max_points,
-                       int max_voxels, float* out_voxels, int32_t* out_coords,
-                       int32_t* out_counts, int32_t* out_num) {
-  if (N < 0 || N >= (int64_t(1) << 31) || max_points < 1 || max_voxels < 1)
-    return kErrInvalid;
-  if (N > 0 && points == nullptr) return kErrInvalid;
-  if (!out_voxels || !out_coords || !out_counts || !out_num) return kErrInvalid;
-  int64_t grid[3];
-  int st = pv_oracle_grid(range, voxel_size, grid);
-  if (st != kOk) return st;
-
+// With three_d the z cell is kept: voxel id (cz * grid_y + cy) * grid_x + cx
+// and coordinates (cz, cy, cx); see pv_oracle_voxelize3d.
+static int voxelize_pass(const float* points, int64_t N, const float range[6],
+                         const float voxel_size[3], const int64_t grid[3],
+                         int max_points, int max_voxels, float* out_voxels,
+                         int32_t* out_coords, int32_t* out_counts,
+                         int32_t* out_num, bool three_d) {
   const size_t row_floats = static_cast<size_t>(max_points) * 4;
   std::memset(out_voxels, 0,
               sizeof(float) * row_floats * static_cast<size_t>(max_voxels));
   std::memset(out_coords, 0, sizeof(int32_t) * 3 * static_cast<size_t>(max_voxels));
   std::memset(out_counts, 0, sizeof(int32_t) * static_cast<size_t>(max_voxels));
 
-  std::map<int64_t, int32_t> pillar;  // pillar id -> output row
+  std::map<int64_t, int32_t> pillar;  // pillar (or voxel) id -> output row
   int32_t V = 0;
   for (int64_t i = 0; i < N; ++i) {
     const float* p = points + 4 * i;
     int64_t cell[3];
     if (!pv_oracle_bin_point(p, range, voxel_size, grid, cell)) continue;
-    const int64_t id = cell[1] * grid[0] + cell[0];  // flattened pillar id
+    const int64_t id = three_d ? (cell[2] * grid[1] + cell[1]) * grid[0] + cell[0]
+                               : cell[1] * grid[0] + cell[0];  // flattened pillar id
     auto it = pillar.find(id);
     int32_t r;
     if (it == pillar.end()) {
@@ -157,9 +153,15 @@ int pv_oracle_voxelize(const float* points, int64_t N, const float range[6],
       if (V >= max_voxels) continue;
       r = V++;
       pillar.emplace(id, r);
-      out_coords[3 * r + 0] = 0;  // pillars have no z extent
-      out_coords[3 * r + 1] = static_cast<int32_t>(id / grid[0]);
-      out_coords[3 * r + 2] = static_cast<int32_t>(id % grid[0]);
+      if (three_d) {
+        out_coords[3 * r + 0] = static_cast<int32_t>(cell[2]);
+        out_coords[3 * r + 1] = static_cast<int32_t>(cell[1]);
+        out_coords[3 * r + 2] = static_cast<int32_t>(cell[0]);
+      } else {
+        out_coords[3 * r + 0] = 0;  // pillars have no z extent
+        out_coords[3 * r + 1] = static_cast<int32_t>(id / grid[0]);
+        out_coords[3 * r + 2] = static_cast<int32_t>(id % grid[0]);
+      }
     } else {
       r = it->second;
     }
@@ -172,6 +174,69 @@ int pv_oracle_voxelize(const float* points, int64_t N, const float range[6],
   }
   *out_num = V;
   return kOk;
+}
+
+static int check_args(const float* points, int64_t N, int max_points, int max_voxels,
+                      const float* out_voxels, const int32_t* out_coords,
+                      const int32_t* out_counts, const int32_t* out_num) {
+  if (N < 0 || N >= (int64_t(1) << 31) || max_points < 1 || max_voxels < 1)
+    return kErrInvalid;
+  if (N > 0 && points == nullptr) return kErrInvalid;
+  if (!out_voxels || !out_coords || !out_counts || !out_num) return kErrInvalid;
+  return kOk;
+}
+
+int pv_oracle_voxelize(const float* points, int64_t N, const float range[6],
+                       const float voxel_size[3], int max_points,
+                       int max_voxels, float* out_voxels, int32_t* out_coords,
+                       int32_t* out_counts, int32_t* out_num) {
+  int st = check_args(points, N, max_points, max_voxels, out_voxels, out_coords, out_counts, out_num);
+  if (st != kOk) return st;
+  int64_t grid[3];
+  st = pv_oracle_grid(range, voxel_size, grid);
+  if (st != kOk) return st;
+  return voxelize_pass(points, N, range, voxel_size, grid, max_points, max_voxels,
+                       out_voxels, out_coords, out_counts, out_num, false);
+}
+
+// Grid extents for true 3-D voxels: the checks of pv_oracle_grid without the
+// pillar restriction on the z extent; the voxel count must stay below 2^31.
+int pv_oracle_grid3d(const float range[6], const float voxel_size[3],
+                     int64_t grid_out[3]) {
+  for (int a = 0; a < 3; ++a) {
+    float lo = range[a], hi = range[a + 3], v = voxel_size[a];
+    if (!std::isfinite(lo) || !std::isfinite(hi) || !std::isfinite(v))
+      return kErrInvalid;
+    if (!(v > 0.0f) || !(hi > lo)) return kErrInvalid;
+    int64_t g = axis_cells(lo, hi, v);
+    if (g < 1 || g > kMaxAxisCells) return kErrInvalid;
+    grid_out[a] = g;
+  }
+  if (grid_out[0] * grid_out[1] * grid_out[2] >= (int64_t(1) << 31))
+    return kErrInvalid;
+  return kOk;
+}
+
+// True 3-D voxels.  The page "Voxelize" hard-codes z = 0 because a pillar
+// spans the whole z slab ("Claiming a pillar and packing points"); the
+// voxel-grid downsampling kernel of the cuda-kdtree ICP page ("4.4",
+// "voxel_downsample") bins all three axes.  This is the same sequential
+// pass with the z cell kept: voxel id (cz * grid_y + cy) * grid_x + cx,
+// coordinates (cz, cy, cx), the same binning rule on every axis (floorf,
+// strict upper bound), the same canonical order, caps and zero padding.
+// With grid_z == 1 it equals pv_oracle_voxelize.
+int pv_oracle_voxelize3d(const float* points, int64_t N, const float range[6],
+                         const float voxel_size[3], int max_points,
+                         int max_voxels, float* out_voxels,
+                         int32_t* out_coords, int32_t* out_counts,
+                         int32_t* out_num) {
+  int st = check_args(points, N, max_points, max_voxels, out_voxels, out_coords, out_counts, out_num);
+  if (st != kOk) return st;
+  int64_t grid[3];
+  st = pv_oracle_grid3d(range, voxel_size, grid);
+  if (st != kOk) return st;
+  return voxelize_pass(points, N, range, voxel_size, grid, max_points, max_voxels,
+                       out_voxels, out_coords, out_counts, out_num, true);
 }
 
 }  // extern "C"

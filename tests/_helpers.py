@@ -47,12 +47,12 @@ def read_division_points():
     return out
 
 
-def read_worked_example():
-    """(range, voxel, points[N,4] float32, cases) from worked_example.txt."""
+def read_worked_example(name: str = "worked_example.txt"):
+    """(range, voxel, points[N,4] float32, cases) from a worked-example file."""
     rng = vox = None
     pts = []
     cases = []
-    with open(os.path.join(GOLDEN, "worked_example.txt")) as f:
+    with open(os.path.join(GOLDEN, name)) as f:
         for line in f:
             s = _strip(line)
             if not s:
@@ -141,10 +141,12 @@ def exact_cell(coord_bits: int, lo: float, v: float, cells: int):
 # Random tiny clouds for the brute-force comparison.
 # --------------------------------------------------------------------------
 
-def random_tiny_case(rng: np.random.Generator):
-    g = [int(rng.integers(1, 7)), int(rng.integers(1, 7)), 1]
+def random_tiny_case(rng: np.random.Generator, gz_max: int = 1):
+    """A tiny cloud with both caps likely to bind; gz_max > 1 draws a z extent
+    of up to gz_max cells (true 3-D voxels)."""
+    g = [int(rng.integers(1, 7)), int(rng.integers(1, 7)), int(rng.integers(1, gz_max + 1))]
     v = [float(np.float32(rng.choice([0.25, 0.5, 1.0, 0.16, 0.1, 0.3]))) for _ in range(2)]
-    v.append(float(np.float32(rng.choice([1.0, 2.0, 4.0]))))
+    v.append(float(np.float32(rng.choice([1.0, 2.0, 4.0] if gz_max == 1 else [0.25, 0.5, 0.3, 1.0]))))
     lo = [float(np.float32(rng.uniform(-5, 5))), float(np.float32(rng.uniform(-5, 5))),
           float(np.float32(rng.uniform(-3, 0)))]
     hi = [float(np.float32(lo[a] + g[a] * v[a])) for a in range(3)]

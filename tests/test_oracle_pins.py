@@ -79,6 +79,47 @@ def pin_worked(lib):
     return fails
 
 
+def pin_grid3d(lib):
+    fails = []
+    st, g = oracle.grid3d(KR, (0.16, 0.16, 0.5), lib)
+    if st != 0 or g != (432, 496, 8):  # 4 m slab / 0.5 m
+        fails.append(f"KITTI 3-D grid {st} {g}")
+    # A SECOND-style grid: [0, 70.4] x [-40, 40] x [-3, 1] at 0.05 x 0.05 x 0.1 m.
+    st, g = oracle.grid3d((0.0, -40.0, -3.0, 70.4, 40.0, 1.0), (0.05, 0.05, 0.1), lib)
+    if st != 0 or g != (1408, 1600, 40):
+        fails.append(f"fine 3-D grid {st} {g}")
+    st, g = oracle.grid3d(KR, KV, lib)  # one layer: the pillar grid
+    if st != 0 or g != (432, 496, 1):
+        fails.append(f"one-layer grid {st} {g}")
+    return fails
+
+
+def pin_worked3d(lib):
+    fails = []
+    rng, vox, pts, cases = read_worked_example("worked_example_3d.txt")
+    for case in cases:
+        ev, ec, en, eV = worked_expected(pts, case)
+        st, v, c, n, V = oracle.voxelize3d(pts, rng, vox, case["max_points"], case["max_voxels"], lib)
+        if st != 0 or V != eV or not (same_bits(v, ev) and same_bits(c, ec) and same_bits(n, en)):
+            fails.append(f"3-D worked case {case['max_points']},{case['max_voxels']}: "
+                         f"V {V} vs {eV}; vox {first_difference(v, ev)}; coords {first_difference(c, ec)}")
+    return fails
+
+
+def pin_bruteforce3d(lib, n_cases=80, seed=2025):
+    fails = []
+    rng = np.random.Generator(np.random.PCG64(seed))
+    for t in range(n_cases):
+        pts, r, v, K, M = random_tiny_case(rng, gz_max=5)
+        st, ov, oc, on, oV = oracle.voxelize3d(pts, r, v, K, M, lib)
+        bv, bc, bn, bV = oracle.voxelize_bruteforce(pts, r, v, K, M, three_d=True)
+        if st != 0 or oV != bV or not (same_bits(ov, bv) and same_bits(oc, bc) and same_bits(on, bn)):
+            fails.append(f"3-D case {t}: V {oV} vs {bV}; {first_difference(ov, bv)}; {first_difference(oc, bc)}")
+            if len(fails) > 3:
+                break
+    return fails
+
+
 def pin_bruteforce(lib, n_cases=120, seed=2024):
     fails = []
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -93,7 +134,7 @@ def pin_bruteforce(lib, n_cases=120, seed=2024):
     return fails
 
 
-ALL_PINS = (pin_grid, pin_edges, pin_division, pin_worked, pin_bruteforce)
+ALL_PINS = (pin_grid, pin_edges, pin_division, pin_worked, pin_bruteforce, pin_grid3d, pin_worked3d, pin_bruteforce3d)
 
 
 # ------------------------------------------------------------- the pins pass
@@ -159,6 +200,44 @@ def test_worked_example_all_three():
 
 def test_bruteforce_random_tiny():
     assert pin_bruteforce(oracle.load()) == []
+
+
+def test_voxel3d_grid():
+    assert pin_grid3d(oracle.load()) == []
+
+
+def test_voxel3d_worked_example_all_three():
+    assert pin_worked3d(oracle.load()) == []
+    rng, vox, pts, cases = read_worked_example("worked_example_3d.txt")
+    for case in cases:
+        ev, ec, en, eV = worked_expected(pts, case)
+        for fn in (oracle.voxelize_numpy, oracle.voxelize_bruteforce):
+            v, c, n, V = fn(pts, rng, vox, case["max_points"], case["max_voxels"], three_d=True)
+            assert V == eV and same_bits(v, ev) and same_bits(c, ec) and same_bits(n, en), fn.__name__
+
+
+def test_voxel3d_bruteforce_random_tiny():
+    assert pin_bruteforce3d(oracle.load()) == []
+
+
+def test_voxel3d_numpy_restatement_random_tiny():
+    rng = np.random.Generator(np.random.PCG64(78))
+    lib = oracle.load()
+    for _ in range(150):
+        pts, r, v, K, M = random_tiny_case(rng, gz_max=5)
+        st, ov, oc, on, oV = oracle.voxelize3d(pts, r, v, K, M, lib)
+        nv, nc, nn, nV = oracle.voxelize_numpy(pts, r, v, K, M, three_d=True)
+        assert st == 0 and oV == nV
+        assert same_bits(ov, nv) and same_bits(oc, nc) and same_bits(on, nn)
+
+
+@pytest.mark.parametrize("name", ["tiny", "kitti", "uniform_50000"])
+def test_voxel3d_with_one_layer_is_the_pillar_oracle(name):
+    pts, P = synth.make(name)
+    a = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    b = oracle.voxelize3d(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    assert a[0] == b[0] == 0 and a[4] == b[4]
+    assert all(same_bits(x, y) for x, y in zip(a[1:4], b[1:4]))
 
 
 def test_numpy_restatement_random_tiny():
@@ -247,8 +326,13 @@ MUTANTS = {
     "upper_bound_inclusive": ("f < static_cast<float>(cells)", "f <= static_cast<float>(cells)"),
     "reciprocal_multiply": ("float q = d / v;", "float q = d * (1.0f / v);"),
     "sign_of_offset": ("float d = c - lo;", "float d = c + lo;"),
-    "coords_transposed": ("static_cast<int32_t>(id / grid[0]);\n      out_coords[3 * r + 2] = static_cast<int32_t>(id % grid[0]);",
-                          "static_cast<int32_t>(id % grid[0]);\n      out_coords[3 * r + 2] = static_cast<int32_t>(id / grid[0]);"),
+    "coords_transposed": ("static_cast<int32_t>(id / grid[0]);\n        out_coords[3 * r + 2] = static_cast<int32_t>(id % grid[0]);",
+                          "static_cast<int32_t>(id % grid[0]);\n        out_coords[3 * r + 2] = static_cast<int32_t>(id / grid[0]);"),
+    "voxel_z_stride": ("(cell[2] * grid[1] + cell[1])", "(cell[2] * grid[0] + cell[1])"),
+    "voxel_z_coordinate_zero": ("out_coords[3 * r + 0] = static_cast<int32_t>(cell[2]);",
+                                "out_coords[3 * r + 0] = 0;"),
+    "voxel_grid_keeps_pillar_check": ("  if (grid_out[0] * grid_out[1] * grid_out[2] >= (int64_t(1) << 31))\n    return kErrInvalid;\n  return kOk;",
+                                      "  if (grid_out[0] * grid_out[1] * grid_out[2] >= (int64_t(1) << 31))\n    return kErrInvalid;\n  if (grid_out[2] != 1) return kErrUnsupported;\n  return kOk;"),
     "wrong_row_stride": ("cell[1] * grid[0] + cell[0]", "cell[1] * grid[1] + cell[0]"),
     "nan_check_on_intensity": ("!is_finite_bits(p[2])", "!is_finite_bits(p[3])"),
     # (Dropping the explicit NaN/Inf test is an equivalent mutant: the float
