@@ -157,16 +157,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(busy)}
 
 
+def oracle_frame(pts, P, lib):
+    """One frame through the C++ oracle (the 3-D pass when the grid has layers)."""
+    import oracle
+
+    three_d = oracle.grid3d(P.point_cloud_range, P.voxel_size, lib)[1][2] > 1
+    return oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib,
+                           three_d=three_d)
+
+
 def cpu_oracle_rate(pts, P, seconds):
     """Single-threaded C++ oracle on the host: (Mpoints/s, frames, seconds)."""
     import oracle
 
     lib = oracle.load()
     n = pts.shape[0]
-    oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib)  # warm
+    oracle_frame(pts, P, lib)  # warm
     frames, t0 = 0, time.perf_counter()
     while True:
-        oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib)
+        oracle_frame(pts, P, lib)
         frames += 1
         el = time.perf_counter() - t0
         if el >= seconds or frames >= 100000:
@@ -184,10 +193,10 @@ def run_reference(args, rank, world):
 
     lib = oracle.load()
     for _ in range(args.warmup):
-        oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib)
+        oracle_frame(pts, P, lib)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib)
+        oracle_frame(pts, P, lib)
     el = time.perf_counter() - t0
     n = pts.shape[0]
     value = n * args.steps / el / 1e6

@@ -15,6 +15,11 @@
  *     dropped unless 0 <= cell < grid on every axis (a strict < on the upper
  *     bound, so a point exactly on x_max is excluded; z outside the slab is
  *     dropped the same way).  The pillar id is cy * grid_x + cx.
+ *   True 3-D voxels (grid_z > 1): the same rule on z gives cz, the voxel id
+ *     is (cz * grid_y + cy) * grid_x + cx and the coordinates are
+ *     (cz, cy, cx), as the voxel-grid downsampling kernel of the cuda-kdtree
+ *     ICP page ("4.4", voxel_downsample) bins all three axes.  Everything
+ *     else below holds per voxel; with grid_z == 1 it is the pillar case.
  *   "Claiming a pillar and packing points": one pillar per distinct id, with
  *     coordinates (0, id / grid_x, id % grid_x); at most max_points points
  *     per pillar ("keep the first K"); the intensity is copied bit for bit.
@@ -30,9 +35,8 @@
  *
  * Grid extents: grid_c = round((max_c - min_c) / v_c), computed in double
  * and rounded half away from zero (432 x 496 for the page's 0.16 m cells over
- * [0, 69.12] x [-39.68, 39.68], "Fig. 2").  Only pillar grids (grid_z == 1)
- * are supported; each of grid_x, grid_y must be <= 2^24 and
- * grid_x * grid_y < 2^31.
+ * [0, 69.12] x [-39.68, 39.68], "Fig. 2").  Each of grid_x, grid_y, grid_z
+ * must be <= 2^24 and grid_x * grid_y * grid_z < 2^31.
  *
  * Errors: a status found on the host is returned and nothing is enqueued;
  * *out_num_voxels is then left untouched.  A status found on the device is
@@ -57,7 +61,8 @@ typedef enum pv_status {
   PV_ERR_INVALID = -1,     /* bad argument: null/misaligned pointer, host pointer where a
                               device pointer is needed, non-finite or non-positive cell
                               size, max <= min, size out of range */
-  PV_ERR_UNSUPPORTED = -2, /* grid_z != 1 (true 3-D voxels are not built) */
+  PV_ERR_UNSUPPORTED = -2, /* a request this build does not support (a device index past
+                              the allocation-free entry point's table) */
   PV_ERR_ALLOC = -3,       /* the library's device workspace could not be allocated */
   PV_ERR_CUDA = -4,        /* a CUDA runtime call failed (launch, copy, ...) */
   PV_ERR_CAPACITY = -5,    /* device: the pillar table ran out of slots (only with a
@@ -86,7 +91,7 @@ typedef enum pv_status {
  *   max_points      points kept per pillar, 1..PV_MAX_POINTS_LIMIT (PointPillars: 32).
  *   max_voxels      pillars kept, >= 1, max_voxels * max_points < 2^31.
  *   out_voxels      device, [max_voxels, max_points, 4] float32, 16-byte aligned.
- *   out_coords      device, [max_voxels, 3] int32, (z = 0, y, x).
+ *   out_coords      device, [max_voxels, 3] int32, (z, y, x); z = 0 on a pillar grid.
  *   out_counts      device, [max_voxels] int32.
  *   out_num_voxels  device, one int32: V (>= 0) or a negative pv_status.
  *   stream          CUDA stream the work is enqueued on.

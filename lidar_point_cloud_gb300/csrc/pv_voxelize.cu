@@ -111,6 +111,7 @@ struct KParams {
   float r_x, r_y, r_z;   // RN(1 / v) per axis, or 0 to always divide
   float g_xf, g_yf, g_zf;
   int g_x;
+  int g_y;
   int K;             // max_points
   int KT;            // tail entries per slot (max_points rounded up to 4, less kHead; >= 0)
   int max_voxels;
@@ -307,7 +308,7 @@ __device__ __forceinline__ bool bin_point(const float4& q, const KParams& p, int
   if (!bin_axis(q.x, p.lo_x, p.v_x, p.r_x, p.g_xf, &cx)) return false;
   if (!bin_axis(q.y, p.lo_y, p.v_y, p.r_y, p.g_yf, &cy)) return false;
   if (!bin_axis(q.z, p.lo_z, p.v_z, p.r_z, p.g_zf, &cz)) return false;
-  *key = cy * p.g_x + cx;
+  *key = (cz * p.g_y + cy) * p.g_x + cx;  // cz = 0 on a pillar grid
   return true;
 }
 
@@ -1109,8 +1110,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           reinterpret_cast<uint4*>(L)[0] = e4;
           reinterpret_cast<uint4*>(L)[1] = e4;
         }
-        p.out_coords[3 * static_cast<size_t>(r)] = 0;
-        p.out_coords[3 * static_cast<size_t>(r) + 1] = key / p.g_x;
+        const int kxy = key / p.g_x;
+        p.out_coords[3 * static_cast<size_t>(r)] = kxy / p.g_y;  // 0 on a pillar grid
+        p.out_coords[3 * static_cast<size_t>(r) + 1] = kxy % p.g_y;
         p.out_coords[3 * static_cast<size_t>(r) + 2] = key % p.g_x;
         p.out_counts[static_cast<size_t>(r)] = static_cast<int32_t>(cnt);
         if (p.hash_mode) p.keys[slot] = kNoKey;
@@ -1214,8 +1216,7 @@ int grid_extents(const float r[6], const float v[3], int64_t g[3]) {
     if (cells < 1 || cells > kMaxAxisCells) return PV_ERR_INVALID;
     g[a] = cells;
   }
-  if (g[0] * g[1] >= (int64_t(1) << 31)) return PV_ERR_INVALID;
-  if (g[2] != 1) return PV_ERR_UNSUPPORTED;
+  if (g[0] * g[1] * g[2] >= (int64_t(1) << 31)) return PV_ERR_INVALID;  // ids stay int32
   return PV_OK;
 }
 
@@ -1255,7 +1256,7 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   if (o.table_mode < 0 || o.table_mode > 2 || o.table_log2 < 0 || o.table_log2 > 31 || o.ctas_per_sm < 0)
     return PV_ERR_INVALID;
   pl->stall = o.test_stall_barrier ? 1u : 0u;
-  const int64_t cells = pl->g[0] * pl->g[1];
+  const int64_t cells = pl->g[0] * pl->g[1] * pl->g[2];
   const int64_t distinct_bound = std::max<int64_t>(1, std::min(N, cells));
   const int64_t hashed_T = next_pow2(std::max<int64_t>(2 * distinct_bound, 1024));
   pl->KT = std::max(0, ((K + 3) & ~3) - kHead);
@@ -1426,6 +1427,7 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.g_yf = static_cast<float>(pl.g[1]);
   kp.g_zf = static_cast<float>(pl.g[2]);
   kp.g_x = static_cast<int>(pl.g[0]);
+  kp.g_y = static_cast<int>(pl.g[1]);
   kp.K = K;
   kp.KT = pl.KT;
   kp.max_voxels = M;
@@ -1749,7 +1751,7 @@ const char* pv_status_string(int status) {
   switch (status) {
     case PV_OK: return "PV_OK";
     case PV_ERR_INVALID: return "PV_ERR_INVALID: invalid argument";
-    case PV_ERR_UNSUPPORTED: return "PV_ERR_UNSUPPORTED: only pillar grids (grid_z == 1) are supported";
+    case PV_ERR_UNSUPPORTED: return "PV_ERR_UNSUPPORTED: a request this build does not support";
     case PV_ERR_ALLOC: return "PV_ERR_ALLOC: device workspace allocation failed";
     case PV_ERR_CUDA: return "PV_ERR_CUDA: CUDA runtime error";
     case PV_ERR_CAPACITY: return "PV_ERR_CAPACITY: pillar table full";

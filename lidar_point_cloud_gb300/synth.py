@@ -59,6 +59,14 @@ class Params:
 KITTI_PARAMS = Params(KITTI_RANGE, KITTI_VOXEL, 32, 16_000)
 DENSE_PARAMS = Params(DENSE_RANGE, DENSE_VOXEL, 32, 60_000)
 ADV_PARAMS = Params(DENSE_RANGE, ADV_VOXEL, 32, 200_000)
+# True 3-D voxels on the same frames: 0.25 m layers over the KITTI slab
+# (432 x 496 x 16), a SECOND-style fine grid (0.05 x 0.05 x 0.1 m over
+# [0, 70.4] x [-40, 40] x [-3, 1]: 1408 x 1600 x 40, hashed table), and the
+# dense grid in 2 m layers (1024 x 1024 x 4, direct table).
+KITTI3D_PARAMS = Params(KITTI_RANGE, (0.16, 0.16, 0.25), 32, 40_000)
+SECOND_PARAMS = Params((0.0, -40.0, -3.0, 70.4, 40.0, 1.0), (0.05, 0.05, 0.1), 5, 40_000)
+DENSE3D_PARAMS = Params(DENSE_RANGE, (0.1, 0.1, 2.0), 32, 60_000)
+VOXEL3D_WORKLOADS = ("kitti3d", "second", "dense3d")
 
 
 def _f32(bits: int) -> np.float32:
@@ -293,6 +301,12 @@ def make(name: str) -> Tuple[np.ndarray, Params]:
         return dense(7), DENSE_PARAMS
     if name == "adversarial":
         return adversarial(8), ADV_PARAMS
+    if name == "kitti3d":
+        return kitti(1), KITTI3D_PARAMS
+    if name == "second":
+        return kitti(1), SECOND_PARAMS
+    if name == "dense3d":
+        return dense(7), DENSE3D_PARAMS
     raise KeyError(name)
 
 
@@ -302,4 +316,7 @@ WORKLOADS: Dict[str, str] = {
     **{f"uniform_{n}": f"{n:,} uniform points, 432x496 grid, 16,000 pillars" for n in UNIFORM_SIZES},
     "dense": "1,048,576-return 128-beam frame, 1024x1024 grid, 60,000 pillars",
     "adversarial": "4,194,304 points, 64 hot pillars + colliding ids, 2048x2048 grid, 200,000 pillars",
+    "kitti3d": "122,880-return 64-beam frame, 432x496x16 voxels (0.25 m layers), 40,000 voxels",
+    "second": "122,880-return 64-beam frame, 1408x1600x40 voxels (0.05x0.05x0.1 m), 5 points, 40,000 voxels",
+    "dense3d": "1,048,576-return 128-beam frame, 1024x1024x4 voxels (2 m layers), 60,000 voxels",
 }

@@ -80,9 +80,10 @@ def test_grid_size_matches_oracle(lib, rng_vox):
 
 
 def test_grid_size_errors(lib):
-    with pytest.raises(pv.PVError) as e:
-        pv.grid_size(synth.KITTI_RANGE, (0.16, 0.16, 1.0))  # 4 z-cells: not a pillar grid
-    assert e.value.status == -2
+    assert pv.grid_size(synth.KITTI_RANGE, (0.16, 0.16, 1.0)) == (432, 496, 4)  # true 3-D voxels
+    with pytest.raises(pv.PVError) as e:  # 2^31 voxels or more: ids would not fit int32
+        pv.grid_size((0, 0, 0, 2048, 2048, 512), (1, 1, 1))
+    assert e.value.status == -1
     for bad in [(0.0, 0.16, 4.0), (-0.16, 0.16, 4.0), (float("nan"), 0.16, 4.0), (float("inf"), 0.16, 4.0)]:
         with pytest.raises(pv.PVError) as e:
             pv.grid_size(synth.KITTI_RANGE, bad)
