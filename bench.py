@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="kitti")
+    ap.add_argument("--order", default="canonical", choices=["canonical", "unordered"],
+                    help="canonical order (default) or the page's own unordered contract")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample length")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -91,10 +93,10 @@ def kernel_sha():
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, kernel="pv_voxelize_kernel"):
     """DRAM bytes per launch from the committed ncu summary, if it still
     describes the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"pv_voxelize_kernel_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -234,8 +236,12 @@ def run_gb300(args, rank, world, local_rank):
     outs = [pv.alloc_outputs(K, M, dev) for _ in range(R)]
     stream = torch.cuda.current_stream(dev)
 
+    unordered = args.order == "unordered"
+    kernel = "pv_unordered_kernel" if unordered else "pv_voxelize_kernel"
+
     def step(k):
-        pv.voxelize_into(inputs[k % R], P.point_cloud_range, P.voxel_size, K, M, outs[k % R], stream=stream)
+        pv.voxelize_into(inputs[k % R], P.point_cloud_range, P.voxel_size, K, M, outs[k % R], stream=stream,
+                         unordered=unordered)
 
     for k in range(args.warmup):
         step(k)
@@ -300,15 +306,30 @@ def run_gb300(args, rank, world, local_rank):
                 torch.empty((M, 3), dtype=torch.int32).pin_memory().numpy(),
                 torch.empty((M,), dtype=torch.int32).pin_memory().numpy(),
                 torch.empty((1,), dtype=torch.int32).pin_memory().numpy())
+    if unordered:  # Python API: pinned host -> device, voxelize_into, device -> pinned host
+        host_t = [torch.from_numpy(a) for a in host_out]
+        pin_t = torch.from_numpy(pin_pts)
+
+        def e2e_step():
+            d_pts = pin_t.to(dev, non_blocking=True)
+            pv.voxelize_into(d_pts, P.point_cloud_range, P.voxel_size, K, M, outs[0], stream=stream, unordered=True)
+            for h, d in zip(host_t, outs[0]):
+                h.copy_(d, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        api = "voxelize_into(unordered=True) with pinned host copies in and out, synchronous"
+    else:
+        def e2e_step():
+            pv.voxelize_host(pin_pts, P.point_cloud_range, P.voxel_size, K, M, out=host_out, stream=stream)
+        api = "pv_voxelize_host (C ABI, pinned host buffers, synchronous)"
     for _ in range(5):
-        pv.voxelize_host(pin_pts, P.point_cloud_range, P.voxel_size, K, M, out=host_out, stream=stream)
+        e2e_step()
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
-        pv.voxelize_host(pin_pts, P.point_cloud_range, P.voxel_size, K, M, out=host_out, stream=stream)
+        e2e_step()
     e2e_s = time.perf_counter() - t0
     e2e = {"value": round(n * args.e2e_steps / e2e_s / 1e6, 3), "unit": "Mpoints/s",
            "h2d_bytes_per_step": 16 * n, "d2h_bytes_per_step": M * (16 * K + 16) + 4,
-           "api": "pv_voxelize_host (C ABI, pinned host buffers, synchronous)", "steps": args.e2e_steps}
+           "api": api, "steps": args.e2e_steps}
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -336,11 +357,12 @@ def run_gb300(args, rank, world, local_rank):
             "launch": f"1 cooperative kernel per step, {plan['ctas']} blocks x {plan['threads']} threads",
             "l2": f"inputs+outputs rotate over {R} frame buffers ({R * frame_bytes / 2**20:.0f} MiB > 2x L2)",
             "parallelism": f"replicas x{world}",
+            "order": args.order,
         },
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
-            "peak_source": f"{peak_src} (hbm_gbs)", "kernel": "pv_voxelize_kernel",
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload, kernel),
+            "peak_source": f"{peak_src} (hbm_gbs)", "kernel": kernel,
             "bytes_per_launch": bytes_launch, "avg_launch_us": round(avg_kernel_s * 1e6, 3),
         },
         "cpu_baseline": cpu,

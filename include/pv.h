@@ -110,8 +110,18 @@ int pv_voxelize(const float* points, int64_t num_points, const float point_cloud
                 pv_stream_t stream);
 
 /*
- * Tuning and test knobs for pv_voxelize_ex.  Zero in any field means "use the
- * library's choice".  The result never depends on these settings.
+ * Options of pv_voxelize_ex.  Zero in any field means "use the library's
+ * choice".  Apart from `order`, the result never depends on these settings.
+ *   order        0 the canonical order (the contract above); 1 the page's own
+ *                unordered contract ("The hash slot is the output index",
+ *                "Claiming a pillar and packing points", "Compaction"): the
+ *                same pillar set and counts, but pillars in whatever order
+ *                they were created, the points of a pillar in arrival order,
+ *                and, where a cap binds, whichever max_points points and
+ *                max_voxels pillars arrived first.  Zero padding as above.
+ *                The result may differ from run to run; the page checks its
+ *                own kernel the same way ("Results": sort by (z, y, x), then
+ *                compare the pillar sets and counts).
  *   table_mode   0 auto, 1 direct (one slot per grid cell), 2 hashed (open
  *                addressing, linear probing).
  *   table_log2   hashed mode only: force 2^table_log2 slots.  A table smaller
@@ -128,7 +138,8 @@ typedef struct pv_options {
   int test_stall_barrier;  /* test hook: nonzero makes the first grid barrier wait for
                               one arrival that never comes, so the bounded wait runs out
                               (about 1 s) and the call reports PV_ERR_TIMEOUT */
-  int reserved[4];
+  int order;
+  int reserved[3];
 } pv_options;
 
 int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cloud_range[6],

@@ -47,7 +47,7 @@ class PVError(RuntimeError):
 class Options(ctypes.Structure):
     _fields_ = [("table_mode", ctypes.c_int), ("table_log2", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("test_stall_barrier", ctypes.c_int),
-                ("reserved", ctypes.c_int * 4)]
+                ("order", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 class Plan(ctypes.Structure):
@@ -111,10 +111,11 @@ def _f6(seq: Sequence[float], n: int):
     return (ctypes.c_float * n)(*vals)
 
 
-def _options(table_mode=0, table_log2=0, ctas_per_sm=0, test_stall_barrier=0) -> Options:
+def _options(table_mode=0, table_log2=0, ctas_per_sm=0, test_stall_barrier=0, unordered=False) -> Options:
     o = Options()
     o.table_mode, o.table_log2, o.ctas_per_sm = int(table_mode), int(table_log2), int(ctas_per_sm)
     o.test_stall_barrier = int(test_stall_barrier)
+    o.order = 1 if unordered else 0
     return o
 
 
@@ -162,12 +163,13 @@ def alloc_outputs(max_points: int, max_voxels: int, device):
 
 def voxelize_into(points, point_cloud_range, voxel_size, max_points: int, max_voxels: int,
                   out, stream=None, table_mode: int = 0, table_log2: int = 0, ctas_per_sm: int = 0,
-                  test_stall_barrier: int = 0) -> None:
+                  test_stall_barrier: int = 0, unordered: bool = False) -> None:
     """Enqueue one voxelization into pre-allocated outputs (no synchronization).
 
     ``out`` = (voxels [M, K, 4] f32, coords [M, 3] i32, counts [M] i32, num [1] i32),
     all CUDA tensors on the points' device.  ``num`` receives V or a negative
-    status once the stream reaches the kernel.
+    status once the stream reaches the kernel.  ``unordered`` selects the
+    page's own contract (pillars in creation order, points in arrival order).
     """
     torch = _torch()
     vox, coords, counts, num = out
@@ -192,8 +194,8 @@ def voxelize_into(points, point_cloud_range, voxel_size, max_points: int, max_vo
             _f6(point_cloud_range, 6), _f6(voxel_size, 3), int(max_points), int(max_voxels),
             ctypes.c_void_p(vox.data_ptr()), ctypes.c_void_p(coords.data_ptr()),
             ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(num.data_ptr()))
-    if table_mode or table_log2 or ctas_per_sm or test_stall_barrier:
-        o = _options(table_mode, table_log2, ctas_per_sm, test_stall_barrier)
+    if table_mode or table_log2 or ctas_per_sm or test_stall_barrier or unordered:
+        o = _options(table_mode, table_log2, ctas_per_sm, test_stall_barrier, unordered)
         st = lib.pv_voxelize_ex(*args, ctypes.byref(o), handle)
     else:
         st = lib.pv_voxelize(*args, handle)

@@ -99,7 +99,8 @@ struct Control {
   int err;              // most negative status recorded in the running launch
   unsigned int dirty;   // 1: the table may hold stale entries
   unsigned int epoch;   // launch number
-  unsigned int pad[3];
+  unsigned int created; // unordered mode: pillars created in the running launch
+  unsigned int pad[2];
 };
 
 struct KParams {
@@ -133,6 +134,8 @@ struct KParams {
   int32_t* out_coords;
   int32_t* out_counts;
   int32_t* out_num;
+  unsigned int* row_cnt;  // unordered mode: [max_voxels] points that reached each row (zero between calls)
+  size_t row_cnt_cap;
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -743,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     uint4* l4 = reinterpret_cast<uint4*>(p.lists);
     for (size_t q = gtid; q < p.list_words_cap / 2; q += gthreads) l4[q] = e4;
     for (size_t q = gtid; q < p.key_words_cap; q += gthreads) p.keys[q] = kNoKey;
+    for (size_t q = gtid; q < p.row_cnt_cap; q += gthreads) p.row_cnt[q] = 0u;  // unordered-mode counters
     alive = grid_sync(p.ctl, bar_target, &s_flag);
     bar_target += P;
   }
@@ -1153,6 +1157,180 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   }
 }
 
+// ------------------------------------------------------------ unordered mode
+
+// The page's own contract, without the canonical order ("The hash slot is
+// the output index", "Claiming a pillar and packing points", "Compaction"):
+// a pillar's row is handed out when the pillar is created, its points take
+// positions in arrival order ("atomicAdd returns each thread's write
+// position inside the pillar"), points past max_points are dropped, and
+// pillars created after max_voxels rows are taken are dropped whole.  Which
+// points and pillars survive a cap, and in what order, varies from run to
+// run, as the page says of its own kernel ("Results"); the pillar set, the
+// counts and, for pillars under the cap, the point sets do not.
+//
+// One cooperative launch and one grid barrier.  Phase U1, every point: bin,
+// find the slot (direct or hashed, as in the ordered kernel), group the
+// warp's points by slot (match), and let one leader per group claim the
+// slot's head word: free -> pending with atomicCAS; the creators of the
+// warp take consecutive row numbers with one atomicAdd and publish them;
+// other leaders wait (bounded) while the word is pending.  The leader then
+// reserves the group's positions in the row with one atomicAdd and every
+// point stores its row at its position.  A warp finishes all of its own
+// claims before any lane waits, so a wait only ever waits for a warp that
+// is past its claim.  Phase U2, after the barrier: counts (capped),
+// coordinates, zero padding, and the clean-up of every slot created
+// (recorded by creation number).
+constexpr unsigned long long kRowPending = ~1ull;  // head word 0 while its creator takes a row
+constexpr unsigned long long kRowDropped = ~2ull;  // pillar created past max_voxels
+
+__device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long* p) {
+  return *reinterpret_cast<const volatile unsigned long long*>(p);
+}
+
+__global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel(const KParams p) {
+  __shared__ int s_flag;
+  const unsigned int P = gridDim.x;
+  const unsigned int tid = threadIdx.x;
+  const unsigned int lane = tid & 31u;
+  const size_t gtid = static_cast<size_t>(blockIdx.x) * kThreads + tid;
+  const size_t gthreads = static_cast<size_t>(P) * kThreads;
+  const long long gwarp = static_cast<long long>(blockIdx.x) * kWarps + (tid >> 5);
+  const long long nwarps = static_cast<long long>(P) * kWarps;
+  const int K = p.K;
+  const unsigned int M = static_cast<unsigned int>(p.max_voxels);
+  const unsigned int epoch = ld_relaxed(&p.ctl->epoch);
+  const unsigned int dirty = ld_relaxed(&p.ctl->dirty);
+  unsigned int bar_target = P;
+  bool alive = true;
+
+  if (dirty) {  // recovery after a failed launch: empty the table and the row counters first
+    const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+    uint4* l4 = reinterpret_cast<uint4*>(p.lists);
+    for (size_t q = gtid; q < p.list_words_cap / 2; q += gthreads) l4[q] = e4;
+    for (size_t q = gtid; q < p.key_words_cap; q += gthreads) p.keys[q] = kNoKey;
+    for (size_t q = gtid; q < p.row_cnt_cap; q += gthreads) p.row_cnt[q] = 0u;
+    if (gtid == 0) p.ctl->created = 0u;
+    alive = grid_sync(p.ctl, bar_target, &s_flag);
+    bar_target += P;
+  }
+
+  // ---- phase U1.  Every lane of a warp runs the same trips (the grid stride
+  // is a multiple of 32), so the match and the shuffles see the whole warp.
+  if (alive) {
+    for (long long base = 0; base < p.n; base += static_cast<long long>(gthreads)) {
+      const long long i = base + static_cast<long long>(gtid);
+      const float4 q = i < p.n ? __ldg(p.points + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      int slot = -1, key = 0;
+      if (i < p.n) {
+        if (bin_point(q, p, &key)) {
+          slot = p.hash_mode ? claim_slot(p.keys, p.table_mask, key) : key;
+          if (slot < 0) atomicMin(&p.ctl->err, PV_ERR_CAPACITY);
+        }
+      }
+      const unsigned int peers = __match_any_sync(0xffffffffu, slot);
+      const int leader = __ffs(peers) - 1;
+      const bool lead = slot >= 0 && static_cast<int>(lane) == leader;
+      unsigned long long* const head = p.lists + static_cast<size_t>(slot < 0 ? 0 : slot) * kHead;
+      unsigned long long word = 0;
+      if (lead) word = atomicCAS(head, kEmpty64, kRowPending);
+      const bool creator = lead && word == kEmpty64;
+      const unsigned int cm = __ballot_sync(0xffffffffu, creator);
+      unsigned int cbase = 0;
+      if (cm != 0u) {
+        const int first = __ffs(cm) - 1;
+        if (static_cast<int>(lane) == first) cbase = atomicAdd(&p.ctl->created, static_cast<unsigned int>(__popc(cm)));
+        cbase = __shfl_sync(0xffffffffu, cbase, first);
+      }
+      long long row = -1;
+      if (creator) {
+        const unsigned int a = cbase + __popc(cm & lanemask_lt());
+        p.firsts[a] = slot;  // creation records (at most one per distinct slot): slot for the clean-up,
+        p.slot_of_point[a] = key;  // id for the coordinates
+        row = a < M ? static_cast<long long>(a) : -1;
+        atomicExch(head, a < M ? static_cast<unsigned long long>(a) : kRowDropped);
+      }
+      __syncwarp();
+      if (lead && !creator) {
+        if (word == kRowPending) {  // bounded wait for the creator's row
+          const unsigned long long t0 = global_timer_ns();
+          do {
+            word = ld_volatile_u64(head);
+            if (word != kRowPending) break;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              atomicMin(&p.ctl->err, PV_ERR_TIMEOUT);
+              break;
+            }
+          } while (true);
+        }
+        row = word < static_cast<unsigned long long>(M) ? static_cast<long long>(word) : -1;
+      }
+      row = __shfl_sync(0xffffffffu, row, leader);
+      unsigned int pbase = 0;
+      if (lead && row >= 0) pbase = atomicAdd(p.row_cnt + row, static_cast<unsigned int>(__popc(peers)));
+      pbase = __shfl_sync(0xffffffffu, pbase, leader);
+      const unsigned int pos = pbase + __popc(peers & lanemask_lt());
+      if (slot >= 0 && row >= 0 && pos < static_cast<unsigned int>(K))
+        p.out_voxels[static_cast<size_t>(row) * K + pos] = q;
+    }
+    alive = grid_sync(p.ctl, bar_target + p.bar_extra, &s_flag);
+  }
+
+  unsigned int V = 0;
+  if (alive) {
+    const unsigned int total = ld_relaxed(&p.ctl->created);
+    V = total < M ? total : M;
+    // ---- phase U2: one warp per row: count, coordinates, zeros past the count.
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long r = gwarp; r < static_cast<long long>(M); r += nwarps) {
+      unsigned int c = 0;
+      int key = 0;
+      if (r < static_cast<long long>(V)) {
+        c = __ldcg(p.row_cnt + r);
+        c = c < static_cast<unsigned int>(K) ? c : static_cast<unsigned int>(K);
+        key = __ldcg(p.slot_of_point + r);
+      }
+      __syncwarp();
+      for (unsigned int e = c + lane; e < static_cast<unsigned int>(K); e += 32)
+        p.out_voxels[static_cast<size_t>(r) * K + e] = z4;
+      if (lane == 0) {
+        const bool live = r < static_cast<long long>(V);
+        const int kxy = key / p.g_x;
+        p.out_counts[r] = static_cast<int32_t>(c);
+        p.out_coords[3 * r] = live ? kxy / p.g_y : 0;
+        p.out_coords[3 * r + 1] = live ? kxy % p.g_y : 0;
+        p.out_coords[3 * r + 2] = live ? key % p.g_x : 0;
+        if (live) p.row_cnt[r] = 0u;
+      }
+    }
+    // Clean-up of every created slot (rows and dropped pillars alike).
+    for (size_t a = gtid; a < total; a += gthreads) {
+      const int slot = __ldcg(p.firsts + a);
+      p.lists[static_cast<size_t>(slot) * kHead] = kEmpty64;
+      if (p.hash_mode) p.keys[slot] = kNoKey;
+    }
+  }
+
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned int prev = atomicAdd(&p.ctl->done, 1u);
+    if (prev == P - 1) {
+      __threadfence();
+      const int err = *reinterpret_cast<volatile int*>(&p.ctl->err);
+      *p.out_num = err != 0 ? err : static_cast<int32_t>(V);
+      p.ctl->dirty = err != 0 ? 1u : 0u;
+      p.ctl->err = 0;
+      p.ctl->bar = 0;
+      p.ctl->done = 0;
+      p.ctl->created = 0;
+      const unsigned int next = epoch + 1;
+      p.ctl->epoch = next == 0 ? 1u : next;
+      __threadfence();
+    }
+  }
+}
+
 // ------------------------------------------------------------ host side
 
 struct DeviceInfo {
@@ -1175,6 +1353,8 @@ struct Workspace {
   size_t list_words_cap = 0;
   int32_t* keys = nullptr;
   size_t key_words_cap = 0;
+  unsigned int* row_cnt = nullptr;  // unordered mode, [max_voxels]
+  size_t row_cnt_cap = 0;
   // Device copies used by pv_voxelize_host.
   unsigned char* staging = nullptr;
   size_t staging_cap = 0;
@@ -1186,6 +1366,7 @@ std::map<std::pair<int, pv_stream_t>, Workspace*> g_ws;
 
 struct Plan {
   unsigned int stall = 0;  // test hook (pv_options.test_stall_barrier)
+  bool unordered = false;  // pv_options.order == 1
   int64_t g[3];
   int mode;
   int64_t T;
@@ -1195,6 +1376,7 @@ struct Plan {
   unsigned int mask;
   size_t list_words;
   size_t key_words;
+  size_t row_words;   // unordered mode: per-row point counters (max_voxels)
   size_t bytes;
 };
 
@@ -1256,6 +1438,8 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   if (o.table_mode < 0 || o.table_mode > 2 || o.table_log2 < 0 || o.table_log2 > 31 || o.ctas_per_sm < 0)
     return PV_ERR_INVALID;
   pl->stall = o.test_stall_barrier ? 1u : 0u;
+  if (o.order < 0 || o.order > 1) return PV_ERR_INVALID;
+  pl->unordered = o.order == 1;
   const int64_t cells = pl->g[0] * pl->g[1] * pl->g[2];
   const int64_t distinct_bound = std::max<int64_t>(1, std::min(N, cells));
   const int64_t hashed_T = next_pow2(std::max<int64_t>(2 * distinct_bound, 1024));
@@ -1280,8 +1464,9 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   // Contiguous, tile-aligned chunks: phase 1 and phase 2 share them.
   const int64_t tiles = (N + kThreads - 1) / kThreads;
   pl->chunk = ((tiles + pl->ctas - 1) / pl->ctas) * kThreads;
+  pl->row_words = pl->unordered ? static_cast<size_t>(M) : 0;
   pl->bytes = sizeof(Control) + 4 * static_cast<size_t>(kMaxCtas) + 32 * static_cast<size_t>(N) +
-              8 * pl->list_words + 4 * pl->key_words;
+              8 * pl->list_words + 4 * pl->key_words + 4 * pl->row_words;
   return PV_OK;
 }
 
@@ -1369,6 +1554,9 @@ int reserve(Workspace* ws, const Plan& pl, int64_t N, pv_stream_t stream) {
   if (pl.key_words &&
       (st = grow(&ws->keys, &ws->key_words_cap, pl.key_words, 0xFF, stream, &synced)) != PV_OK)
     return st;
+  if (pl.row_words &&
+      (st = grow(&ws->row_cnt, &ws->row_cnt_cap, pl.row_words, 0, stream, &synced)) != PV_OK)
+    return st;
   return PV_OK;
 }
 
@@ -1449,18 +1637,20 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.out_coords = out_coords;
   kp.out_counts = out_counts;
   kp.out_num = out_num;
+  kp.row_cnt = ws->row_cnt;
+  kp.row_cnt_cap = ws->row_cnt_cap;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned int>(pl.ctas));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kDynSmem;
+  cfg.dynamicSmemBytes = pl.unordered ? 0 : kDynSmem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, pv_voxelize_kernel, kp) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, pl.unordered ? pv_unordered_kernel : pv_voxelize_kernel, kp) != cudaSuccess) {
     cudaGetLastError();
     return PV_ERR_CUDA;
   }
@@ -1740,6 +1930,7 @@ int pv_release_workspace(void) {
     cudaFree(ws->recs);
     cudaFree(ws->lists);
     cudaFree(ws->keys);
+    cudaFree(ws->row_cnt);
     cudaFree(ws->staging);
     delete ws;
   }

@@ -291,3 +291,86 @@ def voxelize_bruteforce(points: np.ndarray, pc_range, voxel_size, max_points: in
             coords[rank] = k
     V = min(len(first), max_voxels)
     return vox, coords, counts, V
+
+
+# --------------------------------------------------------------------------
+# Order-insensitive check of an unordered result (the page's own contract).
+# --------------------------------------------------------------------------
+
+def check_unordered(points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int,
+                    voxels: np.ndarray, coords: np.ndarray, counts: np.ndarray, V: int,
+                    three_d: bool = False):
+    """Failures (a list of strings, empty if valid) of a result produced under
+    the page's unordered contract ("Claiming a pillar and packing points":
+    pillars in slot order, points in atomicAdd arrival order, "keep the
+    first K"; "Results": compared after sorting by the (z, y, x) key).
+
+    What is unique is compared exactly: V = min(#pillars, max_voxels); every
+    row's coordinates name a distinct occupied pillar (all of them when the
+    budget does not bind); every count is min(points of the pillar,
+    max_points).  The rest is checked for validity: the rows of a pillar are,
+    as a multiset of bit patterns, contained in that pillar's points (so a
+    pillar under the cap holds exactly its points), and every other byte is
+    zero.
+    """
+    fails = []
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    ok, cx, cy, cz, g = cells_numpy(pts, pc_range, voxel_size)
+    if not three_d:
+        cz = np.zeros_like(cz)
+    key = (cz * g[1] + cy) * g[0] + cx
+    idx = np.flatnonzero(ok)
+    pk = key[idx]
+    uniq, n_of = np.unique(pk, return_counts=True)
+    exp_V = int(min(uniq.size, max_voxels))
+    if V != exp_V:
+        return [f"V {V} != {exp_V}"]
+    K, M = max_points, max_voxels
+    c = np.asarray(coords, dtype=np.int64)[:V]
+    rkey = (c[:, 0] * g[1] + c[:, 1]) * g[0] + c[:, 2]
+    if V and (np.any(c < 0) or np.any(c[:, 2] >= g[0]) or np.any(c[:, 1] >= g[1]) or np.any(c[:, 0] >= g[2])):
+        fails.append("coordinates out of the grid")
+        return fails
+    if np.unique(rkey).size != V:
+        fails.append("two rows name the same pillar")
+    pos = np.searchsorted(uniq, rkey)
+    pos = np.minimum(pos, max(uniq.size - 1, 0))
+    if V and not np.all(uniq[pos] == rkey):
+        fails.append("a row names an empty pillar")
+        return fails
+    if uniq.size <= M and V and not np.array_equal(np.sort(rkey), uniq):
+        fails.append("pillar set differs")
+    exp_cnt = np.minimum(n_of[pos], K) if V else np.zeros(0, dtype=np.int64)
+    got_cnt = np.asarray(counts)[:V].astype(np.int64)
+    if not np.array_equal(got_cnt, exp_cnt):
+        bad = int(np.flatnonzero(got_cnt != exp_cnt)[0])
+        fails.append(f"row {bad}: count {got_cnt[bad]} != {exp_cnt[bad]}")
+        return fails
+    # Padding: positions >= count of live rows, and every row >= V, all zero bits.
+    vb = np.ascontiguousarray(voxels).view(np.uint32).reshape(M, K, 4)
+    live = np.zeros((M, K), dtype=bool)
+    if V:
+        live[:V] = np.arange(K)[None, :] < got_cnt[:, None]
+    if np.any(vb[~live] != 0):
+        fails.append("nonzero padding in voxels")
+    if np.any(np.asarray(coords)[V:] != 0) or np.any(np.asarray(counts)[V:] != 0):
+        fails.append("nonzero padding in coords or counts")
+    # Multiset containment of the stored rows in their pillar's points.
+    rec = np.dtype([("k", "<i8"), ("a", "<u4"), ("b", "<u4"), ("c", "<u4"), ("d", "<u4")])
+    pb = pts.view(np.uint32)[idx]
+    have = np.empty(idx.size, dtype=rec)
+    have["k"], have["a"], have["b"], have["c"], have["d"] = pk, pb[:, 0], pb[:, 1], pb[:, 2], pb[:, 3]
+    rr, ee = np.nonzero(live[:V]) if V else (np.zeros(0, int), np.zeros(0, int))
+    got = np.empty(rr.size, dtype=rec)
+    gb = vb[rr, ee]
+    got["k"], got["a"], got["b"], got["c"], got["d"] = rkey[rr] if V else 0, gb[:, 0], gb[:, 1], gb[:, 2], gb[:, 3]
+    hu, hc = np.unique(have, return_counts=True)
+    gu, gc = np.unique(got, return_counts=True)
+    at = np.searchsorted(hu, gu)
+    at = np.minimum(at, max(hu.size - 1, 0))
+    found = (hu[at] == gu) if hu.size else np.zeros(gu.size, dtype=bool)
+    if not np.all(found):
+        fails.append("a stored row is not a point of its pillar")
+    elif np.any(gc > hc[at]):
+        fails.append("a point is stored more often than it occurs")
+    return fails
