@@ -374,3 +374,88 @@ def check_unordered(points: np.ndarray, pc_range, voxel_size, max_points: int, m
     elif np.any(gc > hc[at]):
         fails.append("a point is stored more often than it occurs")
     return fails
+
+
+# --------------------------------------------------------------------------
+# Batches of frames: each frame voxelized on its own.
+# --------------------------------------------------------------------------
+
+def voxelize_batch(points: np.ndarray, frame_offsets, pc_range, voxel_size, max_points: int,
+                   max_voxels: int, three_d: bool = False, lib=None):
+    """B frames, frame b = points[frame_offsets[b]:frame_offsets[b + 1]], each
+    voxelized exactly as one cloud (same grid, caps per frame).  Returns
+    (status, voxels [B, M, K, 4], coords [B, M, 4] = (b, z, y, x), counts
+    [B, M], V [B]); coordinate rows past V_b are zero, batch index included.
+    The batch index in the coordinates follows the batched PointPillars
+    layout (one (batch, z, y, x) row per voxel)."""
+    off = [int(o) for o in frame_offsets]
+    B = len(off) - 1
+    vox = np.zeros((B, max_voxels, max_points, 4), dtype=np.float32)
+    coords = np.zeros((B, max_voxels, 4), dtype=np.int32)
+    counts = np.zeros((B, max_voxels), dtype=np.int32)
+    Vs = np.zeros(B, dtype=np.int32)
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    for b in range(B):
+        st, v, c, n, V = voxelize(pts[off[b]:off[b + 1]], pc_range, voxel_size, max_points, max_voxels, lib,
+                                  three_d=three_d)
+        if st != OK:
+            return st, vox, coords, counts, Vs
+        vox[b], counts[b], Vs[b] = v, n, V
+        coords[b, :V, 0] = b
+        coords[b, :, 1:] = c
+    return OK, vox, coords, counts, Vs
+
+
+def voxelize_batch_numpy(points: np.ndarray, frame_offsets, pc_range, voxel_size, max_points: int,
+                         max_voxels: int, three_d: bool = False):
+    """Restatement over the whole concatenated cloud: the grouping key is
+    (frame, voxel id), voxels are ordered by their first point inside each
+    frame and the budget applies per frame.  Same return values as
+    :func:`voxelize_batch` without the status."""
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    off = np.asarray(frame_offsets, dtype=np.int64)
+    B = off.size - 1
+    K, M = max_points, max_voxels
+    ok, cx, cy, cz, g = cells_numpy(pts, pc_range, voxel_size)
+    if not three_d:
+        cz = np.zeros_like(cz)
+    frame = np.searchsorted(off, np.arange(pts.shape[0]), side="right") - 1
+    cells = g[0] * g[1] * g[2]
+    key = frame * cells + (cz * g[1] + cy) * g[0] + cx
+    vox = np.zeros((B, M, K, 4), dtype=np.float32)
+    coords = np.zeros((B, M, 4), dtype=np.int32)
+    counts = np.zeros((B, M), dtype=np.int32)
+    Vs = np.zeros(B, dtype=np.int32)
+    idx = np.flatnonzero(ok)
+    if idx.size == 0:
+        return vox, coords, counts, Vs
+    uniq, first_pos, inverse = np.unique(key[idx], return_index=True, return_inverse=True)
+    first_idx = idx[first_pos]
+    order = np.argsort(first_idx, kind="stable")        # voxels by first point (frames in order)
+    ufr = uniq[order] // cells                           # frame of each voxel, ascending
+    start_of_frame = np.searchsorted(ufr, np.arange(B), side="left")
+    rank_global = np.empty_like(order)
+    rank_global[order] = np.arange(order.size)
+    ufr_by_uniq = uniq // cells
+    local = rank_global - start_of_frame[ufr_by_uniq]    # rank inside its frame
+    p_local = local[inverse.reshape(-1)]
+    p_frame = ufr_by_uniq[inverse.reshape(-1)]
+    p_rank = rank_global[inverse.reshape(-1)]
+    s = np.argsort(p_rank, kind="stable")
+    rs = p_rank[s]
+    st = np.searchsorted(rs, rs, side="left")
+    pos = np.empty_like(s)
+    pos[s] = np.arange(s.size) - st
+    keep = (p_local < M) & (pos < K)
+    vox.view(np.uint32)[p_frame[keep], p_local[keep], pos[keep]] = pts.view(np.uint32)[idx[keep]]
+    n_of = np.bincount(inverse.reshape(-1), minlength=uniq.size)
+    live = local < M
+    counts[ufr_by_uniq[live], local[live]] = np.minimum(n_of[live], K)
+    per_frame = np.bincount(ufr_by_uniq, minlength=B)
+    Vs[:] = np.minimum(per_frame, M)
+    vid = uniq[live] % cells
+    coords[ufr_by_uniq[live], local[live], 0] = ufr_by_uniq[live]
+    coords[ufr_by_uniq[live], local[live], 1] = vid // (g[0] * g[1])
+    coords[ufr_by_uniq[live], local[live], 2] = (vid // g[0]) % g[1]
+    coords[ufr_by_uniq[live], local[live], 3] = vid % g[0]
+    return vox, coords, counts, Vs

@@ -141,17 +141,17 @@ def exact_cell(coord_bits: int, lo: float, v: float, cells: int):
 # Random tiny clouds for the brute-force comparison.
 # --------------------------------------------------------------------------
 
-def random_tiny_case(rng: np.random.Generator, gz_max: int = 1):
-    """A tiny cloud with both caps likely to bind; gz_max > 1 draws a z extent
-    of up to gz_max cells (true 3-D voxels)."""
+def _tiny_params(rng: np.random.Generator, gz_max: int):
     g = [int(rng.integers(1, 7)), int(rng.integers(1, 7)), int(rng.integers(1, gz_max + 1))]
     v = [float(np.float32(rng.choice([0.25, 0.5, 1.0, 0.16, 0.1, 0.3]))) for _ in range(2)]
     v.append(float(np.float32(rng.choice([1.0, 2.0, 4.0] if gz_max == 1 else [0.25, 0.5, 0.3, 1.0]))))
     lo = [float(np.float32(rng.uniform(-5, 5))), float(np.float32(rng.uniform(-5, 5))),
           float(np.float32(rng.uniform(-3, 0)))]
     hi = [float(np.float32(lo[a] + g[a] * v[a])) for a in range(3)]
-    pc_range = tuple(lo + hi)
-    n = int(rng.integers(0, 260))
+    return g, v, lo, hi
+
+
+def _tiny_points(rng: np.random.Generator, n: int, g, v, lo, hi) -> np.ndarray:
     pts = np.zeros((n, 4), dtype=np.float32)
     hot = [[lo[a] + (rng.integers(0, g[a]) + 0.5) * v[a] for a in range(3)] for _ in range(2)]
     for i in range(n):
@@ -184,7 +184,27 @@ def random_tiny_case(rng: np.random.Generator, gz_max: int = 1):
             for a in range(3):
                 p[a] = h[a] + rng.uniform(-0.3, 0.3) * v[a]
         pts[i] = np.array(p, dtype=np.float32)
-    return pts, pc_range, tuple(v), int(rng.integers(1, 5)), int(rng.integers(1, 10))
+    return pts
+
+
+def random_tiny_case(rng: np.random.Generator, gz_max: int = 1):
+    """A tiny cloud with both caps likely to bind; gz_max > 1 draws a z extent
+    of up to gz_max cells (true 3-D voxels)."""
+    g, v, lo, hi = _tiny_params(rng, gz_max)
+    n = int(rng.integers(0, 260))
+    pts = _tiny_points(rng, n, g, v, lo, hi)
+    return pts, tuple(lo + hi), tuple(v), int(rng.integers(1, 5)), int(rng.integers(1, 10))
+
+
+def random_tiny_batch(rng: np.random.Generator, gz_max: int = 1, max_frames: int = 6):
+    """A batch of tiny frames on one grid: (points, frame offsets, range, voxel, K, M).
+    Frames may be empty."""
+    g, v, lo, hi = _tiny_params(rng, gz_max)
+    B = int(rng.integers(1, max_frames + 1))
+    frames = [_tiny_points(rng, int(rng.integers(0, 120)), g, v, lo, hi) for _ in range(B)]
+    off = np.concatenate([[0], np.cumsum([f.shape[0] for f in frames])]).astype(np.int64)
+    pts = np.concatenate(frames) if off[-1] else np.zeros((0, 4), dtype=np.float32)
+    return pts, off, tuple(lo + hi), tuple(v), int(rng.integers(1, 5)), int(rng.integers(1, 10))
 
 
 # --------------------------------------------------------------------------
