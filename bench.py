@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--workload", default="kitti")
     ap.add_argument("--order", default="canonical", choices=["canonical", "unordered"],
                     help="canonical order (default) or the page's own unordered contract")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="frames per launch (pv_voxelize_batch when > 1; different frames of the workload)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample length")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -190,15 +192,25 @@ def run_reference(args, rank, world):
 
     if rank != 0:
         return
-    pts, P = synth.make(args.workload)
     import oracle
 
     lib = oracle.load()
+    if args.batch > 1:
+        pts, frame_off, P = synth.make_batch(args.workload, args.batch)
+        frames = [pts[frame_off[b]:frame_off[b + 1]] for b in range(args.batch)]
+    else:
+        pts, P = synth.make(args.workload)
+        frames = [pts]
+
+    def one_step():
+        for f in frames:
+            oracle_frame(f, P, lib)
+
     for _ in range(args.warmup):
-        oracle_frame(pts, P, lib)
+        one_step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_frame(pts, P, lib)
+        one_step()
     el = time.perf_counter() - t0
     n = pts.shape[0]
     value = n * args.steps / el / 1e6
@@ -207,10 +219,11 @@ def run_reference(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * el / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {synth.WORKLOADS[args.workload]}", "N": n,
-                   "max_points": P.max_points, "max_voxels": P.max_voxels},
+        "config": {"workload": (f"{args.workload} x{args.batch} frames per launch: " if args.batch > 1 else
+                                f"{args.workload}: ") + synth.WORKLOADS[args.workload], "N": n,
+                   "max_points": P.max_points, "max_voxels": P.max_voxels, "frames_per_launch": args.batch},
         "cpu_baseline": {"value": round(value, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
-                         "sample": f"one full frame per step, {args.steps} steps, single-threaded C++ std::map oracle"},
+                         "sample": f"{args.batch} full frame(s) per step, {args.steps} steps, single-threaded C++ std::map oracle"},
         "e2e": {"value": round(value, 3), "unit": "Mpoints/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -225,29 +238,40 @@ def run_gb300(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    pts, P = synth.make(args.workload)
+    Bf = args.batch
+    if Bf > 1:
+        pts, frame_off, P = synth.make_batch(args.workload, Bf)
+    else:
+        pts, P = synth.make(args.workload)
+        frame_off = [0, pts.shape[0]]
     n, K, M = pts.shape[0], P.max_points, P.max_voxels
     plan = pv.query_plan(n, P.point_cloud_range, P.voxel_size, K, M)
-    bytes_launch = algorithmic_bytes(n, K, M)
-    frame_bytes = 16 * n + M * (16 * K + 16) + 4
+    bytes_launch = 16 * n + Bf * (M * (16 * K + 16) + 4)  # input once, every output byte of every frame once
+    frame_bytes = bytes_launch
     R = max(2, -(-2 * L2_BYTES // frame_bytes))
     src = torch.from_numpy(pts).to(dev)
     inputs = [src.clone() for _ in range(R)]
-    outs = [pv.alloc_outputs(K, M, dev) for _ in range(R)]
+    outs = [(pv.alloc_batch_outputs(Bf, K, M, dev) if Bf > 1 else pv.alloc_outputs(K, M, dev)) for _ in range(R)]
     stream = torch.cuda.current_stream(dev)
 
     unordered = args.order == "unordered"
+    if unordered and Bf > 1:
+        raise SystemExit("--order unordered takes one frame per launch")
     kernel = "pv_unordered_kernel" if unordered else "pv_voxelize_kernel"
 
     def step(k):
-        pv.voxelize_into(inputs[k % R], P.point_cloud_range, P.voxel_size, K, M, outs[k % R], stream=stream,
-                         unordered=unordered)
+        if Bf > 1:
+            pv.voxelize_batch_into(inputs[k % R], frame_off, P.point_cloud_range, P.voxel_size, K, M, outs[k % R],
+                                   stream=stream)
+        else:
+            pv.voxelize_into(inputs[k % R], P.point_cloud_range, P.voxel_size, K, M, outs[k % R], stream=stream,
+                             unordered=unordered)
 
     for k in range(args.warmup):
         step(k)
     torch.cuda.synchronize(dev)
     # Correctness guard on the last warm-up output (cheap: V only).
-    v_dev = int(outs[(args.warmup - 1) % R][3].item()) if args.warmup else 0
+    v_dev = int(outs[(args.warmup - 1) % R][3].min().item()) if args.warmup else 0
     if v_dev < 0:
         raise RuntimeError(f"device status {v_dev}")
 
@@ -291,7 +315,7 @@ def run_gb300(args, rank, world, local_rank):
     region_ms = max_over_ranks(region_ms, device=dev)
     # Result check after timing: the last timed output against the first.
     last = outs[(args.warmup + args.steps - 1) % R]
-    V = int(last[3].item())
+    V = int(last[3].sum().item())
 
     if rank != 0:
         return
@@ -302,11 +326,19 @@ def run_gb300(args, rank, world, local_rank):
 
     # End to end through the C ABI with host buffers (pinned), rank 0 only.
     pin_pts = torch.from_numpy(pts).pin_memory().numpy()
-    host_out = (torch.empty((M, K, 4), dtype=torch.float32).pin_memory().numpy(),
-                torch.empty((M, 3), dtype=torch.int32).pin_memory().numpy(),
-                torch.empty((M,), dtype=torch.int32).pin_memory().numpy(),
-                torch.empty((1,), dtype=torch.int32).pin_memory().numpy())
-    if unordered:  # Python API: pinned host -> device, voxelize_into, device -> pinned host
+    host_out = tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory().numpy() for o in outs[0])
+    if Bf > 1:  # Python API: pinned host -> device, voxelize_batch_into, device -> pinned host
+        host_t = [torch.from_numpy(a) for a in host_out]
+        pin_t = torch.from_numpy(pin_pts)
+
+        def e2e_step():
+            d_pts = pin_t.to(dev, non_blocking=True)
+            pv.voxelize_batch_into(d_pts, frame_off, P.point_cloud_range, P.voxel_size, K, M, outs[0], stream=stream)
+            for h, d in zip(host_t, outs[0]):
+                h.copy_(d, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        api = f"voxelize_batch_into ({Bf} frames) with pinned host copies in and out, synchronous"
+    elif unordered:  # Python API: pinned host -> device, voxelize_into, device -> pinned host
         host_t = [torch.from_numpy(a) for a in host_out]
         pin_t = torch.from_numpy(pin_pts)
 
@@ -328,14 +360,16 @@ def run_gb300(args, rank, world, local_rank):
         e2e_step()
     e2e_s = time.perf_counter() - t0
     e2e = {"value": round(n * args.e2e_steps / e2e_s / 1e6, 3), "unit": "Mpoints/s",
-           "h2d_bytes_per_step": 16 * n, "d2h_bytes_per_step": M * (16 * K + 16) + 4,
+           "h2d_bytes_per_step": 16 * n, "d2h_bytes_per_step": sum(int(o.numel()) * 4 for o in outs[0]),
            "api": api, "steps": args.e2e_steps}
 
     cpu = None
     if not args.no_cpu_baseline:
-        rate, frames, el = cpu_oracle_rate(pts, P, args.cpu_seconds)
+        one = pts[:frame_off[1]] if Bf > 1 else pts
+        rate, frames, el = cpu_oracle_rate(one, P, args.cpu_seconds)
         cpu = {"value": round(rate, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
-               "sample": f"{frames} repetitions of the full frame ({el:.1f} s), single-threaded C++ std::map oracle"}
+               "sample": f"{frames} repetitions of {'the first frame' if Bf > 1 else 'the full frame'} ({el:.1f} s), "
+                         "single-threaded C++ std::map oracle"}
 
     line = {
         "metric": METRIC,
@@ -351,9 +385,11 @@ def run_gb300(args, rank, world, local_rank):
         "dtype": "f32",
         "data": "synthetic",
         "config": {
-            "workload": f"{args.workload}: {synth.WORKLOADS[args.workload]}",
-            "N": n, "V": V, "grid": list(plan["grid"]), "max_points": K, "max_voxels": M,
-            "table": f"{plan['table_mode']}, {plan['table_slots']} slots",
+            "workload": (f"{args.workload} x{Bf} frames per launch: " if Bf > 1 else f"{args.workload}: ")
+                        + synth.WORKLOADS[args.workload],
+            "N": n, "V": V, "frames_per_launch": Bf, "grid": list(plan["grid"]), "max_points": K, "max_voxels": M,
+            "table": (f"{plan['table_mode']}, {plan['table_slots']} slots" if Bf == 1 else
+                      f"one key space per frame, {Bf} x {int(np.prod(plan['grid']))} voxel ids"),
             "launch": f"1 cooperative kernel per step, {plan['ctas']} blocks x {plan['threads']} threads",
             "l2": f"inputs+outputs rotate over {R} frame buffers ({R * frame_bytes / 2**20:.0f} MiB > 2x L2)",
             "parallelism": f"replicas x{world}",
@@ -361,7 +397,8 @@ def run_gb300(args, rank, world, local_rank):
         },
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload, kernel),
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(args.workload + (f"_x{Bf}" if Bf > 1 else ""), kernel),
             "peak_source": f"{peak_src} (hbm_gbs)", "kernel": kernel,
             "bytes_per_launch": bytes_launch, "avg_launch_us": round(avg_kernel_s * 1e6, 3),
         },

@@ -142,6 +142,33 @@ typedef struct pv_options {
   int reserved[3];
 } pv_options;
 
+/*
+ * A batch of frames in one launch.  Frame b is points[frame_offsets[b] ..
+ * frame_offsets[b + 1]) and is voxelized exactly as pv_voxelize voxelizes it
+ * alone (same grid, max_points and max_voxels per frame; canonical order
+ * inside the frame).  Batching spreads one launch and its grid barriers over
+ * many small frames; the page measures that a frame's cost is dominated by
+ * that fixed overhead ("voxelize latency vs point count", Tab. 2).
+ *   points          device, [frame_offsets[num_frames], 4] float32, 16-byte aligned.
+ *   frame_offsets   HOST, [num_frames + 1] int64: 0, then never decreasing (empty
+ *                   frames allowed); read before the call returns.
+ *   num_frames      1 .. PV_MAX_FRAMES.
+ *   out_voxels      device, [num_frames, max_voxels, max_points, 4] float32.
+ *   out_coords      device, [num_frames, max_voxels, 4] int32, (batch, z, y, x):
+ *                   the batched PointPillars layout; rows past a frame's V are zero.
+ *   out_counts      device, [num_frames, max_voxels] int32.
+ *   out_num_voxels  device, [num_frames] int32: V of each frame, or the (same)
+ *                   negative status in every entry.
+ * num_frames * (grid voxels) must stay below 2^31, and num_frames *
+ * max_voxels * max_points below 2^31.  Errors, ownership and streams as for
+ * pv_voxelize.
+ */
+#define PV_MAX_FRAMES 256
+int pv_voxelize_batch(const float* points, const int64_t* frame_offsets, int num_frames,
+                      const float point_cloud_range[6], const float voxel_size[3], int max_points, int max_voxels,
+                      float* out_voxels, int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels,
+                      pv_stream_t stream);
+
 int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cloud_range[6],
                    const float voxel_size[3], int max_points, int max_voxels, float* out_voxels,
                    int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels,

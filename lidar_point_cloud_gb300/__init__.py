@@ -7,7 +7,9 @@ package is its thin Python binding plus seeded synthetic inputs
 
 from ._binding import (  # noqa: F401
     EXPORTS,
+    MAX_FRAMES,
     PVError,
+    alloc_batch_outputs,
     alloc_outputs,
     grid_size,
     lib_path,
@@ -15,6 +17,8 @@ from ._binding import (  # noqa: F401
     query_plan,
     release_workspace,
     voxelize,
+    voxelize_batch,
+    voxelize_batch_into,
     voxelize_host,
     voxelize_into,
 )

@@ -30,9 +30,11 @@ STATUS = {
 }
 
 EXPORTS = (
-    "pv_voxelize", "pv_voxelize_ex", "pv_voxelize_host", "pv_voxelize_static", "pv_grid_size", "pv_query_plan",
-    "pv_release_workspace", "pv_status_string", "pv_version",
+    "pv_voxelize", "pv_voxelize_ex", "pv_voxelize_host", "pv_voxelize_static", "pv_voxelize_batch", "pv_grid_size",
+    "pv_query_plan", "pv_release_workspace", "pv_status_string", "pv_version",
 )
+
+MAX_FRAMES = 256  # PV_MAX_FRAMES
 
 
 class PVError(RuntimeError):
@@ -89,6 +91,8 @@ def load(path: Optional[str] = None):
         lib.pv_voxelize_host.restype = ci
         lib.pv_voxelize_static.argtypes = dev_args + [vp]
         lib.pv_voxelize_static.restype = ci
+        lib.pv_voxelize_batch.argtypes = [vp, ctypes.POINTER(ctypes.c_int64), ci, f, f, ci, ci, vp, vp, vp, vp, vp]
+        lib.pv_voxelize_batch.restype = ci
         lib.pv_grid_size.argtypes = [f, f, ctypes.POINTER(ctypes.c_int64)]
         lib.pv_grid_size.restype = ci
         lib.pv_query_plan.argtypes = [i64, f, f, ci, ci, ctypes.POINTER(Options), ctypes.POINTER(Plan)]
@@ -248,3 +252,63 @@ def voxelize_host(points, point_cloud_range, voxel_size, max_points: int = 32, m
     if st != 0:
         raise PVError(st, "pv_voxelize_host")
     return vox, coords, counts, int(num[0])
+
+
+def alloc_batch_outputs(num_frames: int, max_points: int, max_voxels: int, device):
+    """Outputs of a batched call: voxels [B, M, K, 4], coords [B, M, 4] (batch, z, y, x),
+    counts [B, M], num [B]."""
+    torch = _torch()
+    return (torch.empty((num_frames, max_voxels, max_points, 4), dtype=torch.float32, device=device),
+            torch.empty((num_frames, max_voxels, 4), dtype=torch.int32, device=device),
+            torch.empty((num_frames, max_voxels), dtype=torch.int32, device=device),
+            torch.empty((num_frames,), dtype=torch.int32, device=device))
+
+
+def voxelize_batch_into(points, frame_offsets, point_cloud_range, voxel_size, max_points: int, max_voxels: int,
+                        out, stream=None) -> None:
+    """Enqueue one batched voxelization (frame b = points[off[b]:off[b+1]]) into
+    pre-allocated outputs (see :func:`alloc_batch_outputs`); no synchronization."""
+    torch = _torch()
+    off = [int(o) for o in frame_offsets]
+    B = len(off) - 1
+    vox, coords, counts, num = out
+    if not isinstance(points, torch.Tensor) or points.dtype != torch.float32 or not points.is_cuda:
+        raise TypeError("points must be a float32 CUDA tensor")
+    if points.dim() != 2 or points.shape[1] != 4 or not points.is_contiguous():
+        raise ValueError("points must be a contiguous [N, 4] tensor")
+    if B < 1 or off[-1] != points.shape[0]:
+        raise ValueError("frame_offsets must hold num_frames + 1 offsets ending at N")
+    for t, dt, shape in ((vox, torch.float32, (B, max_voxels, max_points, 4)),
+                         (coords, torch.int32, (B, max_voxels, 4)),
+                         (counts, torch.int32, (B, max_voxels)), (num, torch.int32, (B,))):
+        if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous() or t.device != points.device:
+            raise ValueError("output tensor has the wrong dtype, shape, layout or device")
+    if stream is None:
+        stream = torch.cuda.current_stream(points.device)
+    handle = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    offs = (ctypes.c_int64 * (B + 1))(*off)
+    st = load().pv_voxelize_batch(
+        ctypes.c_void_p(points.data_ptr() if points.shape[0] else 0), offs, B,
+        _f6(point_cloud_range, 6), _f6(voxel_size, 3), int(max_points), int(max_voxels),
+        ctypes.c_void_p(vox.data_ptr()), ctypes.c_void_p(coords.data_ptr()),
+        ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(num.data_ptr()), handle)
+    if st != 0:
+        raise PVError(st, "pv_voxelize_batch")
+
+
+def voxelize_batch(points, frame_offsets, point_cloud_range, voxel_size, max_points: int = 32,
+                   max_voxels: int = 16000, stream=None):
+    """Voxelize a batch of frames in one launch.  Returns the batched
+    PointPillars tensors, frames concatenated: voxels [sum V, K, 4], coords
+    [sum V, 4] (batch, z, y, x), counts [sum V]."""
+    torch = _torch()
+    B = len(frame_offsets) - 1
+    with torch.no_grad():
+        out = alloc_batch_outputs(B, max_points, max_voxels, points.device)
+        voxelize_batch_into(points, frame_offsets, point_cloud_range, voxel_size, max_points, max_voxels, out, stream)
+        Vs = out[3].tolist()
+        if any(v < 0 for v in Vs):
+            raise PVError(min(Vs), "pv_voxelize_batch (device)")
+        return (torch.cat([out[0][b, :v] for b, v in enumerate(Vs)]),
+                torch.cat([out[1][b, :v] for b, v in enumerate(Vs)]),
+                torch.cat([out[2][b, :v] for b, v in enumerate(Vs)]))

@@ -136,7 +136,38 @@ struct KParams {
   int32_t* out_num;
   unsigned int* row_cnt;  // unordered mode: [max_voxels] points that reached each row (zero between calls)
   size_t row_cnt_cap;
+  int frames;             // frames in the call (1 but for pv_voxelize_batch)
+  int cells;              // voxels of one frame's grid; a batched id is frame * cells + id
+  unsigned int* frame_cnt;  // batched: [frames + 1] first points of a frame start's block before it
 };
+
+// Frame start offsets of a batched call, passed by value with the launch
+// (frame b is points [off[b], off[b + 1])).
+constexpr int kMaxFrames = PV_MAX_FRAMES;
+template <int NF>
+struct Frames {
+  long long off[NF + 1];
+};
+
+// Frame holding point i: the largest b < B with off[b] <= i (empty frames skipped).
+__device__ __forceinline__ int frame_of(const long long* off, int B, long long i) {
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= i) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Largest b < B with cum[b] <= k, for a non-decreasing cum.
+__device__ __forceinline__ int slot_in_cum(const unsigned int* cum, int B, unsigned int k) {
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cum[mid] <= k) lo = mid; else hi = mid;
+  }
+  return lo;
+}
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -711,9 +742,18 @@ __device__ unsigned int emit_groups(const KParams& p, const ListRef& L, float4* 
 
 // ------------------------------------------------------------ the kernel
 
-__global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(const KParams p) {
+// NF = 1: one cloud (pv_voxelize); NF = kMaxFrames: a batch of up to NF
+// frames (pv_voxelize_batch), where a voxel's id carries its frame, each
+// frame keeps its own first max_voxels voxels and writes its own rows.
+template <int NF>
+__global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(const KParams p, const Frames<NF> fr) {
+  constexpr bool kBatched = NF > 1;
   extern __shared__ __align__(16) unsigned char s_dyn[];
   __shared__ unsigned int s_prefix[kMaxCtas + 1];
+  __shared__ long long s_off[NF + 1];
+  __shared__ unsigned int s_fpre[NF + 1];  // batched: first points before each frame start (global)
+  __shared__ unsigned int s_vcum[NF + 1];  // batched: rows emitted by earlier frames
+  __shared__ unsigned int s_dcum[NF + 1];  // batched: voxels past the budget in earlier frames
   __shared__ unsigned int s_tile[kFlagUnroll][kWarps];
   __shared__ unsigned int s_tmp[kWarps + 1];
   __shared__ int s_flag;
@@ -738,6 +778,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   unsigned int bar_target = P;
   bool alive = true;
   (void)epoch;
+  const int B = kBatched ? p.frames : 1;
+  if (kBatched)
+    for (int b = static_cast<int>(tid); b <= B; b += kThreads) s_off[b] = fr.off[b];  // read after a block barrier
   PV_STAMP(0);
 
   // Recovery after a failed launch: empty the whole table first.
@@ -809,6 +852,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       if (i < end) {
         int key;
         if (bin_point(q, p, &key)) {
+          if (kBatched) key += frame_of(s_off, B, i) * p.cells;
           slot = p.hash_mode ? claim_slot(p.keys, p.table_mask, key) : key;
           if (slot < 0) atomicMin(&p.ctl->err, PV_ERR_CAPACITY);
         }
@@ -995,8 +1039,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       unsigned int run = local;
 #pragma unroll
       for (int u = 0; u < kFlagUnroll; ++u) {
-        if ((ball[u] >> lane) & 1u)
-          p.firsts[begin + run + s_tile[u][warp] + __popc(ball[u] & lanemask_lt())] = s[u];
+        const unsigned int before = run + s_tile[u][warp] + __popc(ball[u] & lanemask_lt());
+        if ((ball[u] >> lane) & 1u) p.firsts[begin + before] = s[u];
+        if (kBatched) {  // a frame start at i records this block's first points before it
+          const long long i = base + u * kThreads + tid;
+          if (i < end)
+            for (int b = frame_of(s_off, B, i); b >= 1 && s_off[b] == i; --b) p.frame_cnt[b] = before;
+        }
       }
       run += s_tmp[kWarps];
       local = run;
@@ -1017,17 +1066,50 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     if (tid < P) s_prefix[tid] = excl;
     if (tid == 0) s_prefix[P] = total;
     __syncthreads();
-    V = total < M ? total : M;
+    if (kBatched) {
+      // Per frame: voxels (first points between its start and the next), rows
+      // kept (at most max_voxels) and voxels past its budget, as exclusive sums.
+      for (int b = static_cast<int>(tid); b <= B; b += kThreads) {
+        const long long o = s_off[b];
+        unsigned int pre = 0;
+        if (b > 0) pre = o >= p.n ? total : s_prefix[o / p.chunk] + __ldcg(p.frame_cnt + b);
+        s_fpre[b] = pre;
+      }
+      __syncthreads();
+      const unsigned int cnt_b = static_cast<int>(tid) < B ? s_fpre[tid + 1] - s_fpre[tid] : 0u;
+      const unsigned int keep = cnt_b < M ? cnt_b : M;
+      unsigned int vt = 0, dt = 0;
+      const unsigned int ve = block_exclusive_scan(keep, s_tmp, &vt);
+      const unsigned int de = block_exclusive_scan(cnt_b - keep, s_tmp, &dt);
+      if (static_cast<int>(tid) < B) {
+        s_vcum[tid] = ve;
+        s_dcum[tid] = de;
+      }
+      if (tid == 0) {
+        s_vcum[B] = vt;
+        s_dcum[B] = dt;
+      }
+      __syncthreads();
+      V = vt;  // rows written over all frames
+    } else {
+      V = total < M ? total : M;
+    }
     PV_STAMP(4);
 
-    // ---- phase 2c: empty the slots of pillars past the budget (ranks M..total-1),
-    // before the output rows load the memory system with writes:
-    // a list known to end inside positions 0..3 loses those, any other list
-    // every position.
-    for (long long r0 = static_cast<long long>(M) + gwarp * 32; r0 < total; r0 += nwarps * 32) {
-      const long long r = r0 + lane;
-      const bool valid = r < total;
-      const int slot = valid ? slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r)) : 0;
+    // ---- phase 2c: empty the slots of pillars past the budget (ranks M..total-1;
+    // per frame in a batch), before the output rows load the memory system
+    // with writes: a list known to end inside positions 0..3 loses those, any
+    // other list every position.
+    const long long dropped = kBatched ? static_cast<long long>(s_dcum[B]) : static_cast<long long>(total - V);
+    for (long long j0 = gwarp * 32; j0 < dropped; j0 += nwarps * 32) {
+      const long long j = j0 + lane;
+      const bool valid = j < dropped;
+      unsigned int rank = static_cast<unsigned int>(M + j);
+      if (kBatched && valid) {
+        const int b = slot_in_cum(s_dcum, B, static_cast<unsigned int>(j));
+        rank = s_fpre[b] + M + static_cast<unsigned int>(j - s_dcum[b]);
+      }
+      const int slot = valid ? slot_of_rank(p, s_prefix, P, rank) : 0;
       unsigned long long* L = p.lists + static_cast<size_t>(slot) * kHead;  // head row
       const Head hd = read_head(p, L, valid);
       const bool short_list = valid && hd.few && !hd.filled;
@@ -1057,17 +1139,25 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     const long long rw0 = gwarp * per_warp;
     const long long rw1 = rw0 + per_warp < static_cast<long long>(V) ? rw0 + per_warp : static_cast<long long>(V);
     for (long long r0 = rw0; r0 < rw1; r0 += 32) {
-      const long long r = r0 + lane;
-      const bool valid = r < rw1;
+      const long long k = r0 + lane;  // the k-th row written (frames one after the other)
+      const bool valid = k < rw1;
+      long long row = k;              // output row: frame * max_voxels + rank inside the frame
+      unsigned int rank = static_cast<unsigned int>(k);
+      int fb = 0;
+      if (kBatched && valid) {
+        fb = slot_in_cum(s_vcum, B, static_cast<unsigned int>(k));
+        const unsigned int loc = static_cast<unsigned int>(k) - s_vcum[fb];
+        rank = s_fpre[fb] + loc;
+        row = static_cast<long long>(fb) * M + loc;
+      }
       int slot = 0;
-      if (valid) slot = slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r));
+      if (valid) slot = slot_of_rank(p, s_prefix, P, rank);
       unsigned long long* L = p.lists + static_cast<size_t>(slot) * kHead;  // head row
       Head hd = read_head(p, L, valid);
       int key = slot;
       if (valid && p.hash_mode) key = __ldcg(p.keys + slot);
       const bool few = valid && hd.few;
       const unsigned int cnt0 = few ? hd.n : 0u;
-      float4* const orow0 = p.out_voxels + static_cast<size_t>(r0) * K;
       unsigned int cnt = cnt0;
       const unsigned int fmask = __ballot_sync(0xffffffffu, few);
       // Pillars served by their first groups, kEmitUnroll at a time: lane e copies position e.
@@ -1080,16 +1170,21 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           v[j] = src >= 0 ? __ldcg(p.tile_rows + src) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int j = 0; j < kEmitUnroll; ++j)
-          if (((fmask >> (u0 + j)) & 1u) && static_cast<int>(lane) < K) orow0[static_cast<size_t>(u0 + j) * K + lane] = v[j];
+        for (int j = 0; j < kEmitUnroll; ++j) {
+          const long long row_u = __shfl_sync(0xffffffffu, row, u0 + j);
+          if (((fmask >> (u0 + j)) & 1u) && static_cast<int>(lane) < K)
+            p.out_voxels[static_cast<size_t>(row_u) * K + lane] = v[j];
+        }
         if (K > 32) {  // positions 32 .. K-1 (every lane runs the same trips: head_source shuffles)
           const unsigned int k32 = (static_cast<unsigned int>(K) + 31u) & ~31u;
           for (int j = 0; j < kEmitUnroll; ++j) {
             if (!((fmask >> (u0 + j)) & 1u)) continue;
+            const long long row_u = __shfl_sync(0xffffffffu, row, u0 + j);
             for (unsigned int e = lane + 32; e < k32; e += 32) {
               const long long src = head_source(hd, u0 + j, e);
               if (e < static_cast<unsigned int>(K))
-                orow0[static_cast<size_t>(u0 + j) * K + e] = src >= 0 ? __ldcg(p.tile_rows + src) : make_float4(0.f, 0.f, 0.f, 0.f);
+                p.out_voxels[static_cast<size_t>(row_u) * K + e] =
+                    src >= 0 ? __ldcg(p.tile_rows + src) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
         }
@@ -1104,7 +1199,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       for (unsigned int m = __ballot_sync(0xffffffffu, valid && !few); m != 0u; m &= m - 1u) {
         const int u = __ffs(m) - 1;
         const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, u));
-        const unsigned int w = emit_groups(p, Lu, orow0 + static_cast<size_t>(u) * K, K, lane, &stale);
+        const long long row_u = __shfl_sync(0xffffffffu, row, u);
+        const unsigned int w = emit_groups(p, Lu, p.out_voxels + static_cast<size_t>(row_u) * K, K, lane, &stale);
         if (static_cast<int>(lane) == u) cnt = w;
       }
       if (valid) {
@@ -1114,26 +1210,32 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           reinterpret_cast<uint4*>(L)[0] = e4;
           reinterpret_cast<uint4*>(L)[1] = e4;
         }
-        const int kxy = key / p.g_x;
-        p.out_coords[3 * static_cast<size_t>(r)] = kxy / p.g_y;  // 0 on a pillar grid
-        p.out_coords[3 * static_cast<size_t>(r) + 1] = kxy % p.g_y;
-        p.out_coords[3 * static_cast<size_t>(r) + 2] = key % p.g_x;
-        p.out_counts[static_cast<size_t>(r)] = static_cast<int32_t>(cnt);
+        const int id = kBatched ? key % p.cells : key;  // the frame is the row's, not the id's
+        const int kxy = id / p.g_x;
+        constexpr int cw = kBatched ? 4 : 3;  // (batch,) z, y, x
+        int32_t* co = p.out_coords + cw * static_cast<size_t>(row);
+        if (kBatched) co[0] = fb;
+        co[cw - 3] = kxy / p.g_y;  // 0 on a pillar grid
+        co[cw - 2] = kxy % p.g_y;
+        co[cw - 1] = id % p.g_x;
+        p.out_counts[static_cast<size_t>(row)] = static_cast<int32_t>(cnt);
         if (p.hash_mode) p.keys[slot] = kNoKey;
       }
     }
     if (stale) atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
     PV_STAMP(6);
 
-    // ---- phase 2e: zero rows V .. max_voxels-1 (all blocks share it).
+    // ---- phase 2e: zero rows V .. max_voxels-1 (of every frame; all blocks share it).
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     const size_t Kz = static_cast<size_t>(K);
-    for (size_t q = static_cast<size_t>(V) * Kz + gtid; q < static_cast<size_t>(M) * Kz; q += gthreads)
-      p.out_voxels[q] = z4;
-    for (size_t q = 3 * static_cast<size_t>(V) + gtid; q < 3 * static_cast<size_t>(M); q += gthreads)
-      p.out_coords[q] = 0;
-    for (size_t q = static_cast<size_t>(V) + gtid; q < static_cast<size_t>(M); q += gthreads)
-      p.out_counts[q] = 0;
+    constexpr size_t cw = kBatched ? 4 : 3;
+    for (int b = 0; b < B; ++b) {
+      const unsigned int Vb = kBatched ? s_vcum[b + 1] - s_vcum[b] : V;
+      const size_t lo = static_cast<size_t>(b) * M + Vb, hi = static_cast<size_t>(b + 1) * M;
+      for (size_t q = lo * Kz + gtid; q < hi * Kz; q += gthreads) p.out_voxels[q] = z4;
+      for (size_t q = cw * lo + gtid; q < cw * hi; q += gthreads) p.out_coords[q] = 0;
+      for (size_t q = lo + gtid; q < hi; q += gthreads) p.out_counts[q] = 0;
+    }
   }
 
   // ---- the last block to finish publishes the status and rearms the control block.
@@ -1145,7 +1247,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     if (prev == P - 1) {
       __threadfence();
       const int err = *reinterpret_cast<volatile int*>(&p.ctl->err);
-      *p.out_num = err != 0 ? err : static_cast<int32_t>(V);
+      if (kBatched) {
+        for (int b = 0; b < B; ++b)
+          p.out_num[b] = err != 0 ? err : static_cast<int32_t>(s_vcum[b + 1] - s_vcum[b]);
+      } else {
+        *p.out_num = err != 0 ? err : static_cast<int32_t>(V);
+      }
       p.ctl->dirty = err != 0 ? 1u : 0u;
       p.ctl->err = 0;
       p.ctl->bar = 0;
@@ -1366,6 +1473,9 @@ std::map<std::pair<int, pv_stream_t>, Workspace*> g_ws;
 
 struct Plan {
   unsigned int stall = 0;  // test hook (pv_options.test_stall_barrier)
+  int frames = 1;
+  bool batched = false;    // pv_voxelize_batch (any frame count): batched layout of the outputs
+  int64_t cells = 0;       // voxels of one frame's grid
   bool unordered = false;  // pv_options.order == 1
   int64_t g[3];
   int mode;
@@ -1402,6 +1512,24 @@ int grid_extents(const float r[6], const float v[3], int64_t g[3]) {
   return PV_OK;
 }
 
+// Dynamic shared memory opt-in for both instantiations of the ordered kernel;
+// returns the resident blocks per SM of the smaller one (0 on failure).
+int prepare_kernels() {
+  int single = 0, batched = 0;
+  if (cudaFuncSetAttribute(pv_voxelize_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(pv_voxelize_kernel<kMaxFrames>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&single, pv_voxelize_kernel<1>, kThreads, kDynSmem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&batched, pv_voxelize_kernel<kMaxFrames>, kThreads, kDynSmem) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return std::min(single, batched);
+}
+
 int device_info(int dev, DeviceInfo* out) {
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_devices.find(dev);
@@ -1413,12 +1541,7 @@ int device_info(int dev, DeviceInfo* out) {
   int coop = 0;
   if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PV_ERR_CUDA;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) return PV_ERR_CUDA;
-  if (cudaFuncSetAttribute(pv_voxelize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
-      cudaSuccess)
-    return PV_ERR_CUDA;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.blocks_per_sm, pv_voxelize_kernel, kThreads, kDynSmem) !=
-      cudaSuccess)
-    return PV_ERR_CUDA;
+  d.blocks_per_sm = prepare_kernels();
   d.cooperative = coop != 0;
   if (d.blocks_per_sm < 1 || !d.cooperative) return PV_ERR_CUDA;
   g_devices[dev] = d;
@@ -1427,7 +1550,7 @@ int device_info(int dev, DeviceInfo* out) {
 }
 
 int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int M, const pv_options* opt,
-              const DeviceInfo& dev, Plan* pl) {
+              const DeviceInfo& dev, Plan* pl, int frames = 1) {
   if (N < 0 || N >= (int64_t(1) << 29)) return PV_ERR_INVALID;
   if (K < 1 || K > PV_MAX_POINTS_LIMIT || M < 1) return PV_ERR_INVALID;
   if (static_cast<int64_t>(K) * M >= (int64_t(1) << 31)) return PV_ERR_INVALID;
@@ -1440,7 +1563,11 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   pl->stall = o.test_stall_barrier ? 1u : 0u;
   if (o.order < 0 || o.order > 1) return PV_ERR_INVALID;
   pl->unordered = o.order == 1;
-  const int64_t cells = pl->g[0] * pl->g[1] * pl->g[2];
+  pl->cells = pl->g[0] * pl->g[1] * pl->g[2];
+  pl->frames = frames;
+  if (frames < 1 || frames > kMaxFrames) return PV_ERR_INVALID;
+  if (pl->cells * frames >= (int64_t(1) << 31)) return PV_ERR_INVALID;  // batched ids stay int32
+  const int64_t cells = pl->cells * frames;  // one key space per frame
   const int64_t distinct_bound = std::max<int64_t>(1, std::min(N, cells));
   const int64_t hashed_T = next_pow2(std::max<int64_t>(2 * distinct_bound, 1024));
   pl->KT = std::max(0, ((K + 3) & ~3) - kHead);
@@ -1521,7 +1648,7 @@ int get_workspace(int dev, pv_stream_t stream, Workspace** out) {
   }
   ws->ctl = static_cast<Control*>(ctl);
   void* cnt = nullptr;
-  if (cudaMalloc(&cnt, sizeof(unsigned int) * kMaxCtas) != cudaSuccess) {
+  if (cudaMalloc(&cnt, sizeof(unsigned int) * (kMaxCtas + kMaxFrames + 1)) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(ctl);
     delete ws;
@@ -1595,7 +1722,7 @@ class DeviceGuard {
 
 int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const float range[6],
            const float vsize[3], int K, int M, float* out_voxels, int32_t* out_coords, int32_t* out_counts,
-           int32_t* out_num, pv_stream_t stream) {
+           int32_t* out_num, pv_stream_t stream, const int64_t* frame_offsets = nullptr) {
   KParams kp;
   kp.points = reinterpret_cast<const float4*>(points);
   kp.n = N;
@@ -1639,6 +1766,9 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.out_num = out_num;
   kp.row_cnt = ws->row_cnt;
   kp.row_cnt_cap = ws->row_cnt_cap;
+  kp.frames = pl.frames;
+  kp.cells = static_cast<int>(pl.cells);
+  kp.frame_cnt = ws->counts + kMaxCtas;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned int>(pl.ctas));
@@ -1650,7 +1780,20 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, pl.unordered ? pv_unordered_kernel : pv_voxelize_kernel, kp) != cudaSuccess) {
+  cudaError_t e;
+  if (pl.unordered) {
+    e = cudaLaunchKernelEx(&cfg, pv_unordered_kernel, kp);
+  } else if (!pl.batched) {
+    Frames<1> fr;
+    fr.off[0] = 0;
+    fr.off[1] = N;
+    e = cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1>, kp, fr);
+  } else {
+    Frames<kMaxFrames> fr;  // copied into the launch: the caller's array may go at once
+    for (int b = 0; b <= kMaxFrames; ++b) fr.off[b] = b <= pl.frames ? frame_offsets[b] : N;
+    e = cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<kMaxFrames>, kp, fr);
+  }
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return PV_ERR_CUDA;
   }
@@ -1659,7 +1802,8 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
 
 int voxelize_impl(const float* points, int64_t N, const float range[6], const float vsize[3], int K, int M,
                   float* out_voxels, int32_t* out_coords, int32_t* out_counts, int32_t* out_num,
-                  const pv_options* opt, pv_stream_t stream) {
+                  const pv_options* opt, pv_stream_t stream, const int64_t* frame_offsets = nullptr,
+                  int frames = 1) {
   if (!range || !vsize) return PV_ERR_INVALID;
   if (!out_voxels || !out_coords || !out_counts || !out_num) return PV_ERR_INVALID;
   if (N > 0 && !points) return PV_ERR_INVALID;
@@ -1677,12 +1821,28 @@ int voxelize_impl(const float* points, int64_t N, const float range[6], const fl
   int st = device_info(dev, &di);
   if (st != PV_OK) return st;
   Plan pl;
-  if ((st = make_plan(N, range, vsize, K, M, opt, di, &pl)) != PV_OK) return st;
+  if ((st = make_plan(N, range, vsize, K, M, opt, di, &pl, frames)) != PV_OK) return st;
+  pl.batched = frame_offsets != nullptr;
   Workspace* ws = nullptr;
   if ((st = get_workspace(dev, stream, &ws)) != PV_OK) return st;
   std::lock_guard<std::mutex> lk(ws->mu);
   if ((st = reserve(ws, pl, N, stream)) != PV_OK) return st;
-  return launch(ws, pl, points, N, range, vsize, K, M, out_voxels, out_coords, out_counts, out_num, stream);
+  return launch(ws, pl, points, N, range, vsize, K, M, out_voxels, out_coords, out_counts, out_num, stream,
+                frame_offsets);
+}
+
+// A batch of frames: offsets on the host, checked here (first 0, never
+// decreasing); the total is the last offset.
+int voxelize_batch_impl(const float* points, const int64_t* frame_offsets, int frames, const float range[6],
+                        const float vsize[3], int K, int M, float* out_voxels, int32_t* out_coords,
+                        int32_t* out_counts, int32_t* out_num, pv_stream_t stream) {
+  if (!frame_offsets || frames < 1 || frames > kMaxFrames) return PV_ERR_INVALID;
+  if (frame_offsets[0] != 0) return PV_ERR_INVALID;
+  for (int b = 0; b < frames; ++b)
+    if (frame_offsets[b + 1] < frame_offsets[b]) return PV_ERR_INVALID;
+  if (static_cast<int64_t>(frames) * M * K >= (int64_t(1) << 31)) return PV_ERR_INVALID;  // output rows
+  return voxelize_impl(points, frame_offsets[frames], range, vsize, K, M, out_voxels, out_coords, out_counts,
+                       out_num, nullptr, stream, frame_offsets, frames);
 }
 
 // ------------------------------------------------------------ allocation-free variant
@@ -1739,14 +1899,11 @@ int static_setup(int dev, pv_stream_t stream, StaticDevice** out) {
     DeviceInfo d;
     int coop = 0;
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(pv_voxelize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.blocks_per_sm, pv_voxelize_kernel, kThreads, kDynSmem) !=
-            cudaSuccess) {
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) {
       cudaGetLastError();
       return PV_ERR_CUDA;
     }
+    d.blocks_per_sm = prepare_kernels();
     d.cooperative = coop != 0;
     if (d.blocks_per_sm < 1 || !d.cooperative) return PV_ERR_CUDA;
     unsigned char* base = static_cast<unsigned char*>(ptr);
@@ -1826,6 +1983,14 @@ int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cl
                    pv_stream_t stream) {
   return voxelize_impl(points, num_points, point_cloud_range, voxel_size, max_points, max_voxels, out_voxels,
                        out_coords, out_counts, out_num_voxels, options, stream);
+}
+
+int pv_voxelize_batch(const float* points, const int64_t* frame_offsets, int num_frames,
+                      const float point_cloud_range[6], const float voxel_size[3], int max_points, int max_voxels,
+                      float* out_voxels, int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels,
+                      pv_stream_t stream) {
+  return voxelize_batch_impl(points, frame_offsets, num_frames, point_cloud_range, voxel_size, max_points,
+                             max_voxels, out_voxels, out_coords, out_counts, out_num_voxels, stream);
 }
 
 int pv_voxelize_host(const float* points_host, int64_t num_points, const float point_cloud_range[6],

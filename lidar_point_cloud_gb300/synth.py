@@ -310,6 +310,22 @@ def make(name: str) -> Tuple[np.ndarray, Params]:
     raise KeyError(name)
 
 
+def make_batch(name: str, frames: int) -> Tuple[np.ndarray, np.ndarray, Params]:
+    """(points, frame offsets [frames + 1], params): `frames` different frames of
+    a named workload (the generator run with consecutive seeds), concatenated."""
+    gens = {"kitti": (kitti, 1), "kitti3d": (kitti, 1), "second": (kitti, 1), "dense": (dense, 7),
+            "dense3d": (dense, 7), "adversarial": (adversarial, 8), "tiny": (tiny, 0)}
+    _, P = make(name)
+    if name.startswith("uniform_"):
+        n = int(name.split("_", 1)[1])
+        parts = [uniform(n, 300 + 7 * b + n % 997) for b in range(frames)]
+    else:
+        gen, seed0 = gens[name]
+        parts = [gen(seed0 + 1000 * b) if b else gen(seed0) for b in range(frames)]
+    off = np.concatenate([[0], np.cumsum([p.shape[0] for p in parts])]).astype(np.int64)
+    return np.concatenate(parts), off, P
+
+
 WORKLOADS: Dict[str, str] = {
     "tiny": "4,096 uniform + 16 boundary points, 432x496 grid, 16,000 pillars",
     "kitti": "122,880-return 64-beam frame, 432x496 grid, 16,000 pillars",
