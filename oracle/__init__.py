@@ -459,3 +459,82 @@ def voxelize_batch_numpy(points: np.ndarray, frame_offsets, pc_range, voxel_size
     coords[ufr_by_uniq[live], local[live], 2] = (vid // g[0]) % g[1]
     coords[ufr_by_uniq[live], local[live], 3] = vid % g[0]
     return vox, coords, counts, Vs
+
+
+# --------------------------------------------------------------------------
+# Voxel-grid centroid downsampling.
+# --------------------------------------------------------------------------
+
+def _bind_downsample(lib):
+    if not hasattr(lib, "pv_oracle_downsample"):
+        return None
+    f = ctypes.POINTER(ctypes.c_float)
+    i32 = ctypes.POINTER(ctypes.c_int32)
+    fn = lib.pv_oracle_downsample
+    fn.argtypes = [f, ctypes.c_int64, f, f, ctypes.c_int, f, i32, i32, i32]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def downsample(points: np.ndarray, pc_range, voxel_size, max_voxels: int, lib=None):
+    """The C++ oracle of centroid downsampling.  Returns (status, centroids
+    [M, 4] float32, coords [M, 3] int32 (z, y, x), counts [M] int32, V)."""
+    lib = lib or load()
+    fn = _bind_downsample(lib)
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    r, v = _f32(pc_range), _f32(voxel_size)
+    cen = np.empty((max_voxels, 4), dtype=np.float32)
+    coords = np.empty((max_voxels, 3), dtype=np.int32)
+    counts = np.empty((max_voxels,), dtype=np.int32)
+    num = np.zeros(1, dtype=np.int32)
+    i32 = ctypes.POINTER(ctypes.c_int32)
+    st = fn(_fptr(pts) if pts.size else None, pts.shape[0], _fptr(r), _fptr(v), int(max_voxels), _fptr(cen),
+            coords.ctypes.data_as(i32), counts.ctypes.data_as(i32), num.ctypes.data_as(i32))
+    return st, cen, coords, counts, int(num[0])
+
+
+def downsample_exact(points: np.ndarray, pc_range, voxel_size, max_voxels: int):
+    """Restatement with exact sums: each voxel's mean is the exact rational sum
+    of its points' fields over the count (math.fsum is exact for these sums
+    of float32 values), then rounded to float32.  Returns (centroids, coords,
+    counts, V)."""
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    ok, cx, cy, cz, g = cells_numpy(pts, pc_range, voxel_size)
+    key = (cz * g[1] + cy) * g[0] + cx
+    M = max_voxels
+    cen = np.zeros((M, 4), dtype=np.float32)
+    coords = np.zeros((M, 3), dtype=np.int32)
+    counts = np.zeros((M,), dtype=np.int32)
+    idx = np.flatnonzero(ok)
+    if idx.size == 0:
+        return cen, coords, counts, 0
+    uniq, first_pos, inverse = np.unique(key[idx], return_index=True, return_inverse=True)
+    order = np.argsort(idx[first_pos], kind="stable")
+    V = int(min(uniq.size, M))
+    inverse = inverse.reshape(-1)
+    for r in range(V):
+        u = order[r]
+        members = idx[inverse == u]
+        n = members.size
+        counts[r] = n
+        k = int(uniq[u])
+        coords[r] = (k // (g[0] * g[1]), (k // g[0]) % g[1], k % g[0])
+        for c in range(4):
+            vals = pts[members, c].astype(np.float64)
+            if not np.all(np.isfinite(vals)):
+                cen[r, c] = np.float32(np.nan if np.any(np.isnan(vals)) or np.ptp(vals[np.isinf(vals)]) > 0
+                                       else vals[np.isinf(vals)][0])
+            else:
+                cen[r, c] = np.float32(math.fsum(vals) / n)
+    return cen, coords, counts, V
+
+
+def ulp_distance32(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Units in the last place between float32 arrays (NaN == NaN counts 0)."""
+    ai = np.ascontiguousarray(a, dtype=np.float32).view(np.int32).astype(np.int64)
+    bi = np.ascontiguousarray(b, dtype=np.float32).view(np.int32).astype(np.int64)
+    ai = np.where(ai < 0, -(ai & 0x7FFFFFFF), ai)  # a monotone integer line through +-0
+    bi = np.where(bi < 0, -(bi & 0x7FFFFFFF), bi)
+    d = np.abs(ai - bi)
+    both_nan = np.isnan(a) & np.isnan(b)
+    return np.where(both_nan, 0, d)

@@ -37,6 +37,7 @@
 #include <cstdint>
 #include <cstring>
 #include <map>
+#include <vector>
 
 namespace {
 
@@ -237,6 +238,64 @@ int pv_oracle_voxelize3d(const float* points, int64_t N, const float range[6],
   if (st != kOk) return st;
   return voxelize_pass(points, N, range, voxel_size, grid, max_points, max_voxels,
                        out_voxels, out_coords, out_counts, out_num, true);
+}
+
+// Voxel-grid centroid downsampling: the cuda-kdtree ICP page ("4.4",
+// voxel_downsample) replaces PCL's voxel-grid filter: every occupied voxel
+// becomes one point, the centroid of the points that fall in it
+// ("accumulate into the voxel centre", then a reduce by key).  Read here
+// with the Voxelize binning rule on all three axes (floorf, strict upper
+// bound, NaN/Inf dropped; the page's integer truncation would put points
+// just below the origin in cell 0, which "Binning a point" on the Voxelize
+// page rules out) and the canonical order (voxels by their first point, the
+// first max_voxels kept).  Every point of a kept voxel counts (no per-voxel
+// cap).  Per voxel: the four fields (x, y, z, intensity) summed in double
+// precision in point-index order, each sum divided by the count in double,
+// the quotient rounded to float.
+//   out_centroids [max_voxels, 4] float32, out_coords [max_voxels, 3] int32
+//   (z, y, x), out_counts [max_voxels] int32, out_num the voxel count V;
+//   zeros past V.
+int pv_oracle_downsample(const float* points, int64_t N, const float range[6],
+                         const float voxel_size[3], int max_voxels,
+                         float* out_centroids, int32_t* out_coords,
+                         int32_t* out_counts, int32_t* out_num) {
+  int st = check_args(points, N, 1, max_voxels, out_centroids, out_coords, out_counts, out_num);
+  if (st != kOk) return st;
+  int64_t grid[3];
+  st = pv_oracle_grid3d(range, voxel_size, grid);
+  if (st != kOk) return st;
+  std::memset(out_centroids, 0, sizeof(float) * 4 * static_cast<size_t>(max_voxels));
+  std::memset(out_coords, 0, sizeof(int32_t) * 3 * static_cast<size_t>(max_voxels));
+  std::memset(out_counts, 0, sizeof(int32_t) * static_cast<size_t>(max_voxels));
+  std::map<int64_t, int32_t> voxel;  // voxel id -> output row
+  std::vector<double> sum(4 * static_cast<size_t>(max_voxels), 0.0);
+  int32_t V = 0;
+  for (int64_t i = 0; i < N; ++i) {
+    const float* p = points + 4 * i;
+    int64_t cell[3];
+    if (!pv_oracle_bin_point(p, range, voxel_size, grid, cell)) continue;
+    const int64_t id = (cell[2] * grid[1] + cell[1]) * grid[0] + cell[0];
+    auto it = voxel.find(id);
+    int32_t r;
+    if (it == voxel.end()) {
+      if (V >= max_voxels) continue;  // budget spent: this voxel is dropped
+      r = V++;
+      voxel.emplace(id, r);
+      out_coords[3 * r + 0] = static_cast<int32_t>(cell[2]);
+      out_coords[3 * r + 1] = static_cast<int32_t>(cell[1]);
+      out_coords[3 * r + 2] = static_cast<int32_t>(cell[0]);
+    } else {
+      r = it->second;
+    }
+    for (int c = 0; c < 4; ++c) sum[4 * static_cast<size_t>(r) + c] += static_cast<double>(p[c]);
+    out_counts[r] += 1;
+  }
+  for (int32_t r = 0; r < V; ++r)
+    for (int c = 0; c < 4; ++c)
+      out_centroids[4 * static_cast<size_t>(r) + c] =
+          static_cast<float>(sum[4 * static_cast<size_t>(r) + c] / static_cast<double>(out_counts[r]));
+  *out_num = V;
+  return kOk;
 }
 
 }  // extern "C"
