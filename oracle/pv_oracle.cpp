@@ -281,9 +281,7 @@ int pv_oracle_downsample(const float* points, int64_t N, const float range[6],
       if (V >= max_voxels) continue;  // budget spent: this voxel is dropped
       r = V++;
       voxel.emplace(id, r);
-      out_coords[3 * r + 0] = static_cast<int32_t>(cell[2]);
-      out_coords[3 * r + 1] = static_cast<int32_t>(cell[1]);
-      out_coords[3 * r + 2] = static_cast<int32_t>(cell[0]);
+      for (int a = 0; a < 3; ++a) out_coords[3 * r + a] = static_cast<int32_t>(cell[2 - a]);  // (z, y, x)
     } else {
       r = it->second;
     }
