@@ -274,7 +274,7 @@ int pv_oracle_downsample(const float* points, int64_t N, const float range[6],
     const float* p = points + 4 * i;
     int64_t cell[3];
     if (!pv_oracle_bin_point(p, range, voxel_size, grid, cell)) continue;
-    const int64_t id = (cell[2] * grid[1] + cell[1]) * grid[0] + cell[0];
+    const int64_t id = cell[0] + grid[0] * (cell[1] + grid[1] * cell[2]);  // (cz * gy + cy) * gx + cx
     auto it = voxel.find(id);
     int32_t r;
     if (it == voxel.end()) {

@@ -125,8 +125,7 @@ MUTANTS = {
                    "sum[4 * static_cast<size_t>(r) + c]) + p[c]);"),
     "count_plus_one": ("/ static_cast<double>(out_counts[r]));", "/ static_cast<double>(out_counts[r] + 1));"),
     "intensity_not_averaged": ("for (int c = 0; c < 4; ++c) sum[", "for (int c = 0; c < 3; ++c) sum["),
-    "voxel_id_without_z": ("const int64_t id = (cell[2] * grid[1] + cell[1]) * grid[0] + cell[0];\n    auto it = voxel.find(id);",
-                           "const int64_t id = cell[1] * grid[0] + cell[0];\n    auto it = voxel.find(id);"),
+    "voxel_id_without_z": ("cell[0] + grid[0] * (cell[1] + grid[1] * cell[2]);", "cell[0] + grid[0] * cell[1];"),
 }
 
 
