@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--workload", default="kitti")
     ap.add_argument("--order", default="canonical", choices=["canonical", "unordered"],
                     help="canonical order (default) or the page's own unordered contract")
+    ap.add_argument("--op", default="voxelize", choices=["voxelize", "downsample"],
+                    help="voxelize (PointPillars tensors) or voxel-grid centroid downsampling")
     ap.add_argument("--batch", type=int, default=1,
                     help="frames per launch (pv_voxelize_batch when > 1; different frames of the workload)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample length")
@@ -161,25 +163,28 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(busy)}
 
 
-def oracle_frame(pts, P, lib):
+def oracle_frame(pts, P, lib, op="voxelize"):
     """One frame through the C++ oracle (the 3-D pass when the grid has layers)."""
     import oracle
+
+    if op == "downsample":
+        return oracle.downsample(pts, P.point_cloud_range, P.voxel_size, P.max_voxels, lib)
 
     three_d = oracle.grid3d(P.point_cloud_range, P.voxel_size, lib)[1][2] > 1
     return oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib,
                            three_d=three_d)
 
 
-def cpu_oracle_rate(pts, P, seconds):
+def cpu_oracle_rate(pts, P, seconds, op="voxelize"):
     """Single-threaded C++ oracle on the host: (Mpoints/s, frames, seconds)."""
     import oracle
 
     lib = oracle.load()
     n = pts.shape[0]
-    oracle_frame(pts, P, lib)  # warm
+    oracle_frame(pts, P, lib, op)  # warm
     frames, t0 = 0, time.perf_counter()
     while True:
-        oracle_frame(pts, P, lib)
+        oracle_frame(pts, P, lib, op)
         frames += 1
         el = time.perf_counter() - t0
         if el >= seconds or frames >= 100000:
@@ -204,7 +209,7 @@ def run_reference(args, rank, world):
 
     def one_step():
         for f in frames:
-            oracle_frame(f, P, lib)
+            oracle_frame(f, P, lib, args.op)
 
     for _ in range(args.warmup):
         one_step()
@@ -245,22 +250,31 @@ def run_gb300(args, rank, world, local_rank):
         pts, P = synth.make(args.workload)
         frame_off = [0, pts.shape[0]]
     n, K, M = pts.shape[0], P.max_points, P.max_voxels
+    ds = args.op == "downsample"
+    if ds and (Bf > 1 or args.order != "canonical"):
+        raise SystemExit("--op downsample takes one frame per launch in the canonical order")
     plan = pv.query_plan(n, P.point_cloud_range, P.voxel_size, K, M)
-    bytes_launch = 16 * n + Bf * (M * (16 * K + 16) + 4)  # input once, every output byte of every frame once
+    if ds:  # input once; centroid (16 B), coordinates (12 B) and count (4 B) of every row, V
+        bytes_launch = 16 * n + M * 32 + 4
+    else:   # input once, every output byte of every frame once
+        bytes_launch = 16 * n + Bf * (M * (16 * K + 16) + 4)
     frame_bytes = bytes_launch
     R = max(2, -(-2 * L2_BYTES // frame_bytes))
     src = torch.from_numpy(pts).to(dev)
     inputs = [src.clone() for _ in range(R)]
-    outs = [(pv.alloc_batch_outputs(Bf, K, M, dev) if Bf > 1 else pv.alloc_outputs(K, M, dev)) for _ in range(R)]
+    outs = [(pv.alloc_downsample_outputs(M, dev) if ds else
+             pv.alloc_batch_outputs(Bf, K, M, dev) if Bf > 1 else pv.alloc_outputs(K, M, dev)) for _ in range(R)]
     stream = torch.cuda.current_stream(dev)
 
     unordered = args.order == "unordered"
     if unordered and Bf > 1:
         raise SystemExit("--order unordered takes one frame per launch")
-    kernel = "pv_unordered_kernel" if unordered else "pv_voxelize_kernel"
+    kernel = "pv_downsample_kernel" if ds else "pv_unordered_kernel" if unordered else "pv_voxelize_kernel"
 
     def step(k):
-        if Bf > 1:
+        if ds:
+            pv.downsample_into(inputs[k % R], P.point_cloud_range, P.voxel_size, M, outs[k % R], stream=stream)
+        elif Bf > 1:
             pv.voxelize_batch_into(inputs[k % R], frame_off, P.point_cloud_range, P.voxel_size, K, M, outs[k % R],
                                    stream=stream)
         else:
@@ -327,7 +341,18 @@ def run_gb300(args, rank, world, local_rank):
     # End to end through the C ABI with host buffers (pinned), rank 0 only.
     pin_pts = torch.from_numpy(pts).pin_memory().numpy()
     host_out = tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory().numpy() for o in outs[0])
-    if Bf > 1:  # Python API: pinned host -> device, voxelize_batch_into, device -> pinned host
+    if ds:  # Python API: pinned host -> device, downsample_into, device -> pinned host
+        host_t = [torch.from_numpy(a) for a in host_out]
+        pin_t = torch.from_numpy(pin_pts)
+
+        def e2e_step():
+            d_pts = pin_t.to(dev, non_blocking=True)
+            pv.downsample_into(d_pts, P.point_cloud_range, P.voxel_size, M, outs[0], stream=stream)
+            for h, d in zip(host_t, outs[0]):
+                h.copy_(d, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        api = "downsample_into with pinned host copies in and out, synchronous"
+    elif Bf > 1:  # Python API: pinned host -> device, voxelize_batch_into, device -> pinned host
         host_t = [torch.from_numpy(a) for a in host_out]
         pin_t = torch.from_numpy(pin_pts)
 
@@ -366,7 +391,7 @@ def run_gb300(args, rank, world, local_rank):
     cpu = None
     if not args.no_cpu_baseline:
         one = pts[:frame_off[1]] if Bf > 1 else pts
-        rate, frames, el = cpu_oracle_rate(one, P, args.cpu_seconds)
+        rate, frames, el = cpu_oracle_rate(one, P, args.cpu_seconds, args.op)
         cpu = {"value": round(rate, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
                "sample": f"{frames} repetitions of {'the first frame' if Bf > 1 else 'the full frame'} ({el:.1f} s), "
                          "single-threaded C++ std::map oracle"}
@@ -394,6 +419,7 @@ def run_gb300(args, rank, world, local_rank):
             "l2": f"inputs+outputs rotate over {R} frame buffers ({R * frame_bytes / 2**20:.0f} MiB > 2x L2)",
             "parallelism": f"replicas x{world}",
             "order": args.order,
+            "op": args.op,
         },
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

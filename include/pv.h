@@ -169,6 +169,27 @@ int pv_voxelize_batch(const float* points, const int64_t* frame_offsets, int num
                       float* out_voxels, int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels,
                       pv_stream_t stream);
 
+/*
+ * Voxel-grid centroid downsampling.  The cuda-kdtree ICP page ("4.4",
+ * voxel_downsample) replaces the voxel-grid filter: every occupied voxel
+ * becomes one point, the centroid of the points in it.  Cells follow the
+ * binning rule above on all three axes (any grid_z); voxels are in the
+ * canonical order (first point), the first max_voxels kept.  Every point of a
+ * kept voxel counts (no per-voxel cap).  A centroid is (mean x, mean y,
+ * mean z, mean intensity): double-precision sums divided by the count in
+ * double, rounded to float.  The sums are accumulated in parallel, so a mean
+ * may differ from the sequential index-order sum by one float32 unit in the
+ * last place; counts, coordinates, V and the order are exact.
+ *   out_centroids   device, [max_voxels, 4] float32, 16-byte aligned.
+ *   out_coords      device, [max_voxels, 3] int32, (z, y, x).
+ *   out_counts      device, [max_voxels] int32, points per voxel.
+ *   out_num_voxels  device, one int32: V or a negative status.
+ * Rows past V are zero.  Errors, ownership and streams as for pv_voxelize.
+ */
+int pv_voxel_downsample(const float* points, int64_t num_points, const float point_cloud_range[6],
+                        const float voxel_size[3], int max_voxels, float* out_centroids, int32_t* out_coords,
+                        int32_t* out_counts, int32_t* out_num_voxels, pv_stream_t stream);
+
 int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cloud_range[6],
                    const float voxel_size[3], int max_points, int max_voxels, float* out_voxels,
                    int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels,

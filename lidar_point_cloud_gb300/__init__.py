@@ -10,7 +10,10 @@ from ._binding import (  # noqa: F401
     MAX_FRAMES,
     PVError,
     alloc_batch_outputs,
+    alloc_downsample_outputs,
     alloc_outputs,
+    downsample,
+    downsample_into,
     grid_size,
     lib_path,
     load,

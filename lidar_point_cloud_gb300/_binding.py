@@ -30,8 +30,8 @@ STATUS = {
 }
 
 EXPORTS = (
-    "pv_voxelize", "pv_voxelize_ex", "pv_voxelize_host", "pv_voxelize_static", "pv_voxelize_batch", "pv_grid_size",
-    "pv_query_plan", "pv_release_workspace", "pv_status_string", "pv_version",
+    "pv_voxelize", "pv_voxelize_ex", "pv_voxelize_host", "pv_voxelize_static", "pv_voxelize_batch",
+    "pv_voxel_downsample", "pv_grid_size", "pv_query_plan", "pv_release_workspace", "pv_status_string", "pv_version",
 )
 
 MAX_FRAMES = 256  # PV_MAX_FRAMES
@@ -93,6 +93,8 @@ def load(path: Optional[str] = None):
         lib.pv_voxelize_static.restype = ci
         lib.pv_voxelize_batch.argtypes = [vp, ctypes.POINTER(ctypes.c_int64), ci, f, f, ci, ci, vp, vp, vp, vp, vp]
         lib.pv_voxelize_batch.restype = ci
+        lib.pv_voxel_downsample.argtypes = [vp, i64, f, f, ci, vp, vp, vp, vp, vp]
+        lib.pv_voxel_downsample.restype = ci
         lib.pv_grid_size.argtypes = [f, f, ctypes.POINTER(ctypes.c_int64)]
         lib.pv_grid_size.restype = ci
         lib.pv_query_plan.argtypes = [i64, f, f, ci, ci, ctypes.POINTER(Options), ctypes.POINTER(Plan)]
@@ -312,3 +314,49 @@ def voxelize_batch(points, frame_offsets, point_cloud_range, voxel_size, max_poi
         return (torch.cat([out[0][b, :v] for b, v in enumerate(Vs)]),
                 torch.cat([out[1][b, :v] for b, v in enumerate(Vs)]),
                 torch.cat([out[2][b, :v] for b, v in enumerate(Vs)]))
+
+
+def alloc_downsample_outputs(max_voxels: int, device):
+    """Outputs of a downsampling call: centroids [M, 4] f32, coords [M, 3] i32, counts [M] i32, num [1] i32."""
+    torch = _torch()
+    return (torch.empty((max_voxels, 4), dtype=torch.float32, device=device),
+            torch.empty((max_voxels, 3), dtype=torch.int32, device=device),
+            torch.empty((max_voxels,), dtype=torch.int32, device=device),
+            torch.empty((1,), dtype=torch.int32, device=device))
+
+
+def downsample_into(points, point_cloud_range, voxel_size, max_voxels: int, out, stream=None) -> None:
+    """Enqueue one voxel-grid centroid downsampling into pre-allocated outputs."""
+    torch = _torch()
+    cen, coords, counts, num = out
+    if not isinstance(points, torch.Tensor) or points.dtype != torch.float32 or not points.is_cuda:
+        raise TypeError("points must be a float32 CUDA tensor")
+    if points.dim() != 2 or points.shape[1] != 4 or not points.is_contiguous():
+        raise ValueError("points must be a contiguous [N, 4] tensor")
+    for t, dt, shape in ((cen, torch.float32, (max_voxels, 4)), (coords, torch.int32, (max_voxels, 3)),
+                         (counts, torch.int32, (max_voxels,)), (num, torch.int32, (1,))):
+        if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous() or t.device != points.device:
+            raise ValueError("output tensor has the wrong dtype, shape, layout or device")
+    if stream is None:
+        stream = torch.cuda.current_stream(points.device)
+    handle = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    st = load().pv_voxel_downsample(
+        ctypes.c_void_p(points.data_ptr() if points.shape[0] else 0), int(points.shape[0]),
+        _f6(point_cloud_range, 6), _f6(voxel_size, 3), int(max_voxels), ctypes.c_void_p(cen.data_ptr()),
+        ctypes.c_void_p(coords.data_ptr()), ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(num.data_ptr()),
+        handle)
+    if st != 0:
+        raise PVError(st, "pv_voxel_downsample")
+
+
+def downsample(points, point_cloud_range, voxel_size, max_voxels: int = 1 << 20, stream=None):
+    """Voxel-grid centroid downsampling on the points' GPU.  Returns
+    (centroids [V, 4], coords [V, 3], counts [V])."""
+    torch = _torch()
+    with torch.no_grad():
+        out = alloc_downsample_outputs(max_voxels, points.device)
+        downsample_into(points, point_cloud_range, voxel_size, max_voxels, out, stream)
+        V = int(out[3].item())
+        if V < 0:
+            raise PVError(V, "pv_voxel_downsample (device)")
+        return out[0][:V], out[1][:V], out[2][:V]

@@ -139,7 +139,20 @@ struct KParams {
   int frames;             // frames in the call (1 but for pv_voxelize_batch)
   int cells;              // voxels of one frame's grid; a batched id is frame * cells + id
   unsigned int* frame_cnt;  // batched: [frames + 1] first points of a frame start's block before it
+  struct VoxAcc* acc;     // downsampling: [T] per-voxel sums (zero between calls)
+  size_t acc_cap;
 };
+
+// Downsampling accumulator of one voxel (48 bytes, one L2 line half): the
+// four fields summed in double, the point count, and the complement of the
+// lowest point index (all-zero bytes = empty, so atomicMax finds the minimum).
+struct VoxAcc {
+  double s[4];
+  unsigned int count;
+  unsigned int first_c;
+  unsigned int pad[2];
+};
+static_assert(sizeof(VoxAcc) == 48, "three 16-byte words");
 
 // Frame start offsets of a batched call, passed by value with the launch
 // (frame b is points [off[b], off[b + 1])).
@@ -740,6 +753,21 @@ __device__ unsigned int emit_groups(const KParams& p, const ListRef& L, float4* 
   return written;
 }
 
+// Recovery after a failed launch (the control block's dirty flag): every
+// table a launch of any kind fills is emptied whole, since the next launch
+// may be of another kind: lists, hashed keys, unordered-mode row counters,
+// downsampling accumulators.  A grid barrier must follow.
+__device__ void reset_tables(const KParams& p, size_t gtid, size_t gthreads) {
+  const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+  uint4* l4 = reinterpret_cast<uint4*>(p.lists);
+  for (size_t q = gtid; q < p.list_words_cap / 2; q += gthreads) l4[q] = e4;
+  for (size_t q = gtid; q < p.key_words_cap; q += gthreads) p.keys[q] = kNoKey;
+  for (size_t q = gtid; q < p.row_cnt_cap; q += gthreads) p.row_cnt[q] = 0u;
+  uint4* a4 = reinterpret_cast<uint4*>(p.acc);
+  for (size_t q = gtid; q < 3 * p.acc_cap; q += gthreads) a4[q] = z4;
+}
+
 // ------------------------------------------------------------ the kernel
 
 // NF = 1: one cloud (pv_voxelize); NF = kMaxFrames: a batch of up to NF
@@ -785,11 +813,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
 
   // Recovery after a failed launch: empty the whole table first.
   if (dirty) {
-    const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-    uint4* l4 = reinterpret_cast<uint4*>(p.lists);
-    for (size_t q = gtid; q < p.list_words_cap / 2; q += gthreads) l4[q] = e4;
-    for (size_t q = gtid; q < p.key_words_cap; q += gthreads) p.keys[q] = kNoKey;
-    for (size_t q = gtid; q < p.row_cnt_cap; q += gthreads) p.row_cnt[q] = 0u;  // unordered-mode counters
+    reset_tables(p, gtid, gthreads);
     alive = grid_sync(p.ctl, bar_target, &s_flag);
     bar_target += P;
   }
@@ -1311,12 +1335,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel
   unsigned int bar_target = P;
   bool alive = true;
 
-  if (dirty) {  // recovery after a failed launch: empty the table and the row counters first
-    const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-    uint4* l4 = reinterpret_cast<uint4*>(p.lists);
-    for (size_t q = gtid; q < p.list_words_cap / 2; q += gthreads) l4[q] = e4;
-    for (size_t q = gtid; q < p.key_words_cap; q += gthreads) p.keys[q] = kNoKey;
-    for (size_t q = gtid; q < p.row_cnt_cap; q += gthreads) p.row_cnt[q] = 0u;
+  if (dirty) {  // recovery after a failed launch: empty every table first
+    reset_tables(p, gtid, gthreads);
     if (gtid == 0) p.ctl->created = 0u;
     alive = grid_sync(p.ctl, bar_target, &s_flag);
     bar_target += P;
@@ -1438,6 +1458,260 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel
   }
 }
 
+// ------------------------------------------------------------ centroid downsampling
+
+// Voxel-grid downsampling (the cuda-kdtree ICP page, "4.4": voxel_downsample
+// replaces the voxel-grid filter, accumulating every point into its voxel,
+// then a reduce by key): every occupied voxel becomes the mean of its points
+// (x, y, z, intensity), in the canonical voxel order (first point), the first
+// max_voxels voxels kept; cells by the Voxelize binning rule.  Sums are
+// double; the order of the additions differs from the sequential oracle,
+// which can move a mean by one float32 unit in the last place at most (see
+// the tests).  Counts, coordinates and the order are exact.
+//
+// One cooperative launch, two grid barriers, the ordered kernel's skeleton:
+// phase D1 per 1024-point tile of the block's chunk: bin, find the slot,
+// sum each warp's points of one voxel by pointer jumping along the group
+// (five shuffle rounds at most, none for single points), add the warp sums
+// into a shared-memory map of the tile's voxels, then flush the map with one
+// set of global atomics per voxel (4 double adds, the count, the first
+// index).  Phase D2: a point is its voxel's first iff it is a warp-group
+// leader whose index the accumulator holds; blocks compact their first
+// points in index order; counts, barrier, scan.  Phase D3: rank r reads its
+// voxel's accumulator, writes the centroid (double quotient rounded to
+// float), coordinates and count, and empties the accumulator.
+constexpr int kDsHash = 2 * kThreads;  // tile map positions
+constexpr int kDsSmem = kDsHash * (4 + 32 + 4 + 4);
+
+__global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kernel(const KParams p) {
+  extern __shared__ __align__(16) unsigned char s_dyn[];
+  __shared__ unsigned int s_prefix[kMaxCtas + 1];
+  __shared__ unsigned int s_tile[kFlagUnroll][kWarps];
+  __shared__ unsigned int s_tmp[kWarps + 1];
+  __shared__ int s_flag;
+  double* m_sum = reinterpret_cast<double*>(s_dyn);                        // [4][kDsHash]
+  int* m_key = reinterpret_cast<int*>(s_dyn + 32 * kDsHash);               // [kDsHash], -1 = free
+  unsigned int* m_cnt = reinterpret_cast<unsigned int*>(m_key + kDsHash);  // [kDsHash]
+  unsigned int* m_first = m_cnt + kDsHash;                                 // [kDsHash]
+
+  const unsigned int P = gridDim.x;
+  const unsigned int cta = blockIdx.x;
+  const unsigned int tid = threadIdx.x;
+  const unsigned int lane = tid & 31u;
+  const unsigned int warp = tid >> 5;
+  const size_t gtid = static_cast<size_t>(cta) * kThreads + tid;
+  const size_t gthreads = static_cast<size_t>(P) * kThreads;
+  const long long gwarp = static_cast<long long>(cta) * kWarps + warp;
+  const long long nwarps = static_cast<long long>(P) * kWarps;
+  const long long begin = lmin(p.n, static_cast<long long>(cta) * p.chunk);
+  const long long end = lmin(p.n, begin + p.chunk);
+  const unsigned int M = static_cast<unsigned int>(p.max_voxels);
+  const unsigned int epoch = ld_relaxed(&p.ctl->epoch);
+  const unsigned int dirty = ld_relaxed(&p.ctl->dirty);
+  unsigned int bar_target = P;
+  bool alive = true;
+
+  if (dirty) {
+    reset_tables(p, gtid, gthreads);
+    alive = grid_sync(p.ctl, bar_target, &s_flag);
+    bar_target += P;
+  }
+
+  if (alive) {
+    for (int h = static_cast<int>(tid); h < kDsHash; h += kThreads) {
+      m_key[h] = -1;
+      m_cnt[h] = 0u;
+      m_first[h] = 0xFFFFFFFFu;
+      for (int c = 0; c < 4; ++c) m_sum[c * kDsHash + h] = 0.0;
+    }
+    __syncthreads();
+    // ---- phase D1
+    for (long long tb = begin; tb < end; tb += kThreads) {
+      const long long i = tb + tid;
+      const float4 q = i < end ? __ldg(p.points + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      int slot = -1;
+      if (i < end) {
+        int key;
+        if (bin_point(q, p, &key)) {
+          slot = p.hash_mode ? claim_slot(p.keys, p.table_mask, key) : key;
+          if (slot < 0) atomicMin(&p.ctl->err, PV_ERR_CAPACITY);
+        }
+      }
+      const unsigned int peers = __match_any_sync(0xffffffffu, slot);
+      const int leader = __ffs(peers) - 1;
+      // Suffix sums along the group by pointer jumping: nxt is the next member above this lane.
+      double v0 = q.x, v1 = q.y, v2 = q.z, v3 = q.w;
+      int nxt = __ffs(peers & ~((2u << lane) - 1u)) - 1;  // -1: last member (2 << 31 wraps to 0: no member above)
+      if (lane == 31u) nxt = -1;
+      while (__any_sync(0xffffffffu, nxt >= 0)) {
+        const int src = nxt >= 0 ? nxt : static_cast<int>(lane);
+        const double o0 = __shfl_sync(0xffffffffu, v0, src);
+        const double o1 = __shfl_sync(0xffffffffu, v1, src);
+        const double o2 = __shfl_sync(0xffffffffu, v2, src);
+        const double o3 = __shfl_sync(0xffffffffu, v3, src);
+        const int onext = __shfl_sync(0xffffffffu, nxt, src);
+        if (nxt >= 0) {
+          v0 += o0;
+          v1 += o1;
+          v2 += o2;
+          v3 += o3;
+          nxt = onext;
+        }
+      }
+      const bool lead = slot >= 0 && static_cast<int>(lane) == leader;
+      if (i < end) p.slot_of_point[i] = slot < 0 ? -1 : (lead ? (slot | kLeaderBit) : slot);
+      if (lead) {
+        unsigned int h = mix32(static_cast<unsigned int>(slot)) & (kDsHash - 1);
+        for (int probe = 0; probe < kDsHash; ++probe) {  // at most kThreads keys: never full
+          const int cur = atomicCAS(m_key + h, -1, slot);
+          if (cur == -1 || cur == slot) break;
+          h = (h + 1) & (kDsHash - 1);
+        }
+        atomicAdd(m_sum + h, v0);
+        atomicAdd(m_sum + kDsHash + h, v1);
+        atomicAdd(m_sum + 2 * kDsHash + h, v2);
+        atomicAdd(m_sum + 3 * kDsHash + h, v3);
+        atomicAdd(m_cnt + h, static_cast<unsigned int>(__popc(peers)));
+        atomicMin(m_first + h, static_cast<unsigned int>(i));
+      }
+      __syncthreads();  // the tile's voxels are in the map
+      for (int h = static_cast<int>(tid); h < kDsHash; h += kThreads) {
+        const int key = m_key[h];
+        if (key < 0) continue;
+        VoxAcc* A = p.acc + key;
+        for (int c = 0; c < 4; ++c) {
+          atomicAdd(&A->s[c], m_sum[c * kDsHash + h]);
+          m_sum[c * kDsHash + h] = 0.0;
+        }
+        atomicAdd(&A->count, m_cnt[h]);
+        atomicMax(&A->first_c, ~m_first[h]);
+        m_key[h] = -1;
+        m_cnt[h] = 0u;
+        m_first[h] = 0xFFFFFFFFu;
+      }
+      __syncthreads();  // the map is empty again
+    }
+    alive = grid_sync(p.ctl, bar_target + p.bar_extra, &s_flag);
+  }
+
+  unsigned int V = 0;
+  if (alive) {
+    // ---- phase D2: first points of this block's range, compacted in index order.
+    unsigned int local = 0;
+    for (long long base = begin; base < end; base += static_cast<long long>(kFlagUnroll) * kThreads) {
+      int s[kFlagUnroll];
+      unsigned int fc[kFlagUnroll];
+#pragma unroll
+      for (int u = 0; u < kFlagUnroll; ++u) {
+        const long long i = base + u * kThreads + tid;
+        s[u] = i < end ? __ldcg(p.slot_of_point + i) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kFlagUnroll; ++u) {
+        fc[u] = (s[u] >= 0 && (s[u] & kLeaderBit)) ? __ldcg(&p.acc[s[u] & ~kLeaderBit].first_c) : 0u;
+        s[u] = s[u] >= 0 ? (s[u] & ~kLeaderBit) : -1;
+      }
+      unsigned int ball[kFlagUnroll];
+#pragma unroll
+      for (int u = 0; u < kFlagUnroll; ++u) {
+        const long long i = base + u * kThreads + tid;
+        ball[u] = __ballot_sync(0xffffffffu, s[u] >= 0 && fc[u] == ~static_cast<unsigned int>(i));
+        if (lane == 0) s_tile[u][warp] = __popc(ball[u]);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        unsigned int carry = 0;
+#pragma unroll
+        for (int u = 0; u < kFlagUnroll; ++u) {
+          const unsigned int c = lane < static_cast<unsigned int>(kWarps) ? s_tile[u][lane] : 0u;
+          unsigned int incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= static_cast<unsigned int>(o)) incl += y;
+          }
+          if (lane < static_cast<unsigned int>(kWarps)) s_tile[u][lane] = carry + incl - c;
+          carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) s_tmp[kWarps] = carry;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < kFlagUnroll; ++u)
+        if ((ball[u] >> lane) & 1u)
+          p.firsts[begin + local + s_tile[u][warp] + __popc(ball[u] & lanemask_lt())] = s[u];
+      local += s_tmp[kWarps];
+      __syncthreads();
+    }
+    if (tid == 0) p.counts[cta] = local;
+    alive = grid_sync(p.ctl, bar_target + P, &s_flag);
+  }
+
+  if (alive) {
+    unsigned int total = 0;
+    const unsigned int c = tid < P ? __ldcg(p.counts + tid) : 0u;
+    const unsigned int excl = block_exclusive_scan(c, s_tmp, &total);
+    if (tid < P) s_prefix[tid] = excl;
+    if (tid == 0) s_prefix[P] = total;
+    __syncthreads();
+    V = total < M ? total : M;
+    // ---- phase D3: one voxel per thread, ranks in order across the grid;
+    // voxels past the budget only have their accumulators emptied.
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+    for (size_t r = gtid; r < total; r += gthreads) {
+      const int slot = slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r));
+      uint4* a4 = reinterpret_cast<uint4*>(p.acc + slot);
+      if (r < V) {
+        VoxAcc A;  // written by other blocks' atomics: read from L2
+        reinterpret_cast<uint4*>(&A)[0] = __ldcg(a4);
+        reinterpret_cast<uint4*>(&A)[1] = __ldcg(a4 + 1);
+        reinterpret_cast<uint4*>(&A)[2] = __ldcg(a4 + 2);
+        const double n = static_cast<double>(A.count);
+        p.out_voxels[r] = make_float4(static_cast<float>(A.s[0] / n), static_cast<float>(A.s[1] / n),
+                                      static_cast<float>(A.s[2] / n), static_cast<float>(A.s[3] / n));
+        const int key = p.hash_mode ? __ldcg(p.keys + slot) : slot;
+        const int kxy = key / p.g_x;
+        p.out_coords[3 * r] = kxy / p.g_y;
+        p.out_coords[3 * r + 1] = kxy % p.g_y;
+        p.out_coords[3 * r + 2] = key % p.g_x;
+        p.out_counts[r] = static_cast<int32_t>(A.count);
+      }
+      a4[0] = z4;
+      a4[1] = z4;
+      a4[2] = z4;
+      if (p.hash_mode) p.keys[slot] = kNoKey;
+    }
+    // Rows V .. max_voxels-1 are zero.
+    for (size_t r = static_cast<size_t>(V) + gtid; r < M; r += gthreads) {
+      p.out_voxels[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      p.out_coords[3 * r] = 0;
+      p.out_coords[3 * r + 1] = 0;
+      p.out_coords[3 * r + 2] = 0;
+      p.out_counts[r] = 0;
+    }
+  }
+
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned int prev = atomicAdd(&p.ctl->done, 1u);
+    if (prev == P - 1) {
+      __threadfence();
+      const int err = *reinterpret_cast<volatile int*>(&p.ctl->err);
+      *p.out_num = err != 0 ? err : static_cast<int32_t>(V);
+      p.ctl->dirty = err != 0 ? 1u : 0u;
+      p.ctl->err = 0;
+      p.ctl->bar = 0;
+      p.ctl->done = 0;
+      const unsigned int next = epoch + 1;
+      p.ctl->epoch = next == 0 ? 1u : next;
+      __threadfence();
+    }
+  }
+  (void)gwarp;
+  (void)nwarps;
+}
+
 // ------------------------------------------------------------ host side
 
 struct DeviceInfo {
@@ -1462,6 +1736,8 @@ struct Workspace {
   size_t key_words_cap = 0;
   unsigned int* row_cnt = nullptr;  // unordered mode, [max_voxels]
   size_t row_cnt_cap = 0;
+  VoxAcc* acc = nullptr;            // downsampling, [T]
+  size_t acc_cap = 0;
   // Device copies used by pv_voxelize_host.
   unsigned char* staging = nullptr;
   size_t staging_cap = 0;
@@ -1475,6 +1751,7 @@ struct Plan {
   unsigned int stall = 0;  // test hook (pv_options.test_stall_barrier)
   int frames = 1;
   bool batched = false;    // pv_voxelize_batch (any frame count): batched layout of the outputs
+  bool downsample = false; // pv_voxel_downsample: per-voxel accumulators instead of lists
   int64_t cells = 0;       // voxels of one frame's grid
   bool unordered = false;  // pv_options.order == 1
   int64_t g[3];
@@ -1487,6 +1764,7 @@ struct Plan {
   size_t list_words;
   size_t key_words;
   size_t row_words;   // unordered mode: per-row point counters (max_voxels)
+  size_t acc_slots = 0;  // downsampling: accumulators (T)
   size_t bytes;
 };
 
@@ -1523,6 +1801,8 @@ int prepare_kernels() {
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&single, pv_voxelize_kernel<1>, kThreads, kDynSmem) !=
           cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&batched, pv_voxelize_kernel<kMaxFrames>, kThreads, kDynSmem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(pv_downsample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDsSmem) !=
           cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -1676,8 +1956,10 @@ int reserve(Workspace* ws, const Plan& pl, int64_t N, pv_stream_t stream) {
     if ((st = grow(&ws->recs, &cap_d, want, 0, stream, &synced)) != PV_OK) return st;
     ws->points_cap = want;
   }
-  if ((st = grow(&ws->lists, &ws->list_words_cap, round_up(pl.list_words, 2), 0xFF, stream, &synced)) != PV_OK)
+  if (pl.list_words &&
+      (st = grow(&ws->lists, &ws->list_words_cap, round_up(pl.list_words, 2), 0xFF, stream, &synced)) != PV_OK)
     return st;
+  if (pl.acc_slots && (st = grow(&ws->acc, &ws->acc_cap, pl.acc_slots, 0, stream, &synced)) != PV_OK) return st;
   if (pl.key_words &&
       (st = grow(&ws->keys, &ws->key_words_cap, pl.key_words, 0xFF, stream, &synced)) != PV_OK)
     return st;
@@ -1769,6 +2051,8 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.frames = pl.frames;
   kp.cells = static_cast<int>(pl.cells);
   kp.frame_cnt = ws->counts + kMaxCtas;
+  kp.acc = ws->acc;
+  kp.acc_cap = ws->acc_cap;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned int>(pl.ctas));
@@ -1781,7 +2065,10 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (pl.unordered) {
+  if (pl.downsample) {
+    cfg.dynamicSmemBytes = kDsSmem;
+    e = cudaLaunchKernelEx(&cfg, pv_downsample_kernel, kp);
+  } else if (pl.unordered) {
     e = cudaLaunchKernelEx(&cfg, pv_unordered_kernel, kp);
   } else if (!pl.batched) {
     Frames<1> fr;
@@ -1829,6 +2116,39 @@ int voxelize_impl(const float* points, int64_t N, const float range[6], const fl
   if ((st = reserve(ws, pl, N, stream)) != PV_OK) return st;
   return launch(ws, pl, points, N, range, vsize, K, M, out_voxels, out_coords, out_counts, out_num, stream,
                 frame_offsets);
+}
+
+// Centroid downsampling: the same checks and workspace, accumulators in
+// place of lists.
+int downsample_impl(const float* points, int64_t N, const float range[6], const float vsize[3], int M,
+                    float* out_centroids, int32_t* out_coords, int32_t* out_counts, int32_t* out_num,
+                    pv_stream_t stream) {
+  if (!range || !vsize) return PV_ERR_INVALID;
+  if (!out_centroids || !out_coords || !out_counts || !out_num) return PV_ERR_INVALID;
+  if (N > 0 && !points) return PV_ERR_INVALID;
+  if (!aligned(out_centroids, 16) || !aligned(out_coords, 4) || !aligned(out_counts, 4) || !aligned(out_num, 4))
+    return PV_ERR_INVALID;
+  if (N > 0 && !aligned(points, 16)) return PV_ERR_INVALID;
+  const int dev = device_of(out_centroids);
+  if (dev < 0) return PV_ERR_INVALID;
+  if (device_of(out_coords) != dev || device_of(out_counts) != dev || device_of(out_num) != dev)
+    return PV_ERR_INVALID;
+  if (N > 0 && device_of(points) != dev) return PV_ERR_INVALID;
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return PV_ERR_CUDA;
+  DeviceInfo di;
+  int st = device_info(dev, &di);
+  if (st != PV_OK) return st;
+  Plan pl;
+  if ((st = make_plan(N, range, vsize, 1, M, nullptr, di, &pl)) != PV_OK) return st;
+  pl.downsample = true;
+  pl.list_words = 0;
+  pl.acc_slots = static_cast<size_t>(pl.T);
+  Workspace* ws = nullptr;
+  if ((st = get_workspace(dev, stream, &ws)) != PV_OK) return st;
+  std::lock_guard<std::mutex> lk(ws->mu);
+  if ((st = reserve(ws, pl, N, stream)) != PV_OK) return st;
+  return launch(ws, pl, points, N, range, vsize, 1, M, out_centroids, out_coords, out_counts, out_num, stream);
 }
 
 // A batch of frames: offsets on the host, checked here (first 0, never
@@ -1993,6 +2313,13 @@ int pv_voxelize_batch(const float* points, const int64_t* frame_offsets, int num
                              max_voxels, out_voxels, out_coords, out_counts, out_num_voxels, stream);
 }
 
+int pv_voxel_downsample(const float* points, int64_t num_points, const float point_cloud_range[6],
+                        const float voxel_size[3], int max_voxels, float* out_centroids, int32_t* out_coords,
+                        int32_t* out_counts, int32_t* out_num_voxels, pv_stream_t stream) {
+  return downsample_impl(points, num_points, point_cloud_range, voxel_size, max_voxels, out_centroids, out_coords,
+                         out_counts, out_num_voxels, stream);
+}
+
 int pv_voxelize_host(const float* points_host, int64_t num_points, const float point_cloud_range[6],
                      const float voxel_size[3], int max_points, int max_voxels, float* out_voxels_host,
                      int32_t* out_coords_host, int32_t* out_counts_host, int32_t* out_num_voxels_host,
@@ -2096,6 +2423,7 @@ int pv_release_workspace(void) {
     cudaFree(ws->lists);
     cudaFree(ws->keys);
     cudaFree(ws->row_cnt);
+    cudaFree(ws->acc);
     cudaFree(ws->staging);
     delete ws;
   }

@@ -32,7 +32,7 @@ def _worker(rank, world, port, q):
     try:
         region = 10.0 + 5.0 * rank  # rank 1 is the slow one
         worst = bench.max_over_ranks(region)
-        args = type("A", (), {"workload": "tiny", "steps": 2, "warmup": 1, "gpus": world, "batch": 1})()
+        args = type("A", (), {"workload": "tiny", "steps": 2, "warmup": 1, "gpus": world, "batch": 1, "op": "voxelize"})()
         buf = io.StringIO()
         with redirect_stdout(buf):
             bench.run_reference(args, rank, world)
