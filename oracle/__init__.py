@@ -538,3 +538,39 @@ def ulp_distance32(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     d = np.abs(ai - bi)
     both_nan = np.isnan(a) & np.isnan(b)
     return np.where(both_nan, 0, d)
+
+
+# --------------------------------------------------------------------------
+# Farthest point sampling.
+# --------------------------------------------------------------------------
+
+def fps(points: np.ndarray, num_samples: int, start: int = 0, lib=None):
+    """The C++ oracle of farthest point sampling.  Returns (status, indices [M] int32)."""
+    lib = lib or load()
+    fn = lib.pv_oracle_fps
+    fn.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.POINTER(ctypes.c_int32)]
+    fn.restype = ctypes.c_int
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    out = np.zeros(max(int(num_samples), 0), dtype=np.int32)
+    st = fn(_fptr(pts) if pts.size else None, pts.shape[0], int(num_samples), int(start),
+            out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+    return st, out
+
+
+def fps_numpy(points: np.ndarray, num_samples: int, start: int = 0):
+    """Vectorised restatement: one NumPy float32 pass per sample (the same
+    operation order, elementwise, so every distance has the same bits), and
+    np.argmax, which returns the first maximum."""
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    x, y, z = pts[:, 0], pts[:, 1], pts[:, 2]
+    dist = np.full(pts.shape[0], np.inf, dtype=np.float32)
+    out = np.zeros(num_samples, dtype=np.int32)
+    sel = int(start)
+    for k in range(num_samples):
+        out[k] = sel
+        dx, dy, dz = x - x[sel], y - y[sel], z - z[sel]
+        d = (dx * dx + dy * dy) + dz * dz
+        np.minimum(dist, d, out=dist)
+        sel = int(np.argmax(dist))
+    return out

@@ -296,4 +296,47 @@ int pv_oracle_downsample(const float* points, int64_t N, const float range[6],
   return kOk;
 }
 
+// Farthest point sampling, the operation RadiusFPS accelerates (the RadiusFPS
+// page: "Baseline: classic GPU FPS"; its spherical-voxel pruning skips only
+// work that cannot change the result, so the samples are those of plain
+// FPS).  Start at point `start`; every point keeps its smallest squared
+// distance to the samples so far (the page's min_dist, starting above every
+// distance); the next sample is the point with the largest such distance.
+// Ties go to the lowest index (the page leaves tie-breaking open and notes
+// it; fixing it makes the result unique).  The squared distance of the page's
+// baseline kernel, (px-qx)^2 + (py-qy)^2 + (pz-qz)^2, is evaluated in float
+// as ((dx * dx) + (dy * dy)) + (dz * dz), every operation rounded to nearest.
+// Intensity is ignored.  Points must be finite (status kErrInvalid if not).
+//   points [N, 4] float32; out_idx [M] int32.
+int pv_oracle_fps(const float* points, int64_t N, int64_t M, int64_t start,
+                  int32_t* out_idx) {
+  if (N < 1 || N >= (int64_t(1) << 31) || M < 1 || start < 0 || start >= N)
+    return kErrInvalid;
+  if (!points || !out_idx) return kErrInvalid;
+  for (int64_t i = 0; i < N; ++i)
+    for (int c = 0; c < 3; ++c)
+      if (!is_finite_bits(points[4 * i + c])) return kErrInvalid;
+  std::vector<float> min_dist(static_cast<size_t>(N), INFINITY);
+  int64_t sel = start;
+  for (int64_t k = 0; k < M; ++k) {
+    out_idx[k] = static_cast<int32_t>(sel);
+    const float qx = points[4 * sel], qy = points[4 * sel + 1], qz = points[4 * sel + 2];
+    int64_t best = 0;
+    float best_d = -1.0f;  // below every distance: index 0 wins if all are zero
+    for (int64_t i = 0; i < N; ++i) {
+      const float dx = points[4 * i] - qx;
+      const float dy = points[4 * i + 1] - qy;
+      const float dz = points[4 * i + 2] - qz;
+      const float d = (dx * dx + dy * dy) + dz * dz;
+      if (d < min_dist[i]) min_dist[i] = d;
+      if (min_dist[i] > best_d) {  // strict: the first (lowest-index) maximum stays
+        best_d = min_dist[i];
+        best = i;
+      }
+    }
+    sel = best;
+  }
+  return kOk;
+}
+
 }  // extern "C"
