@@ -48,8 +48,9 @@ def parse():
     ap.add_argument("--workload", default="kitti")
     ap.add_argument("--order", default="canonical", choices=["canonical", "unordered"],
                     help="canonical order (default) or the page's own unordered contract")
-    ap.add_argument("--op", default="voxelize", choices=["voxelize", "downsample"],
-                    help="voxelize (PointPillars tensors) or voxel-grid centroid downsampling")
+    ap.add_argument("--op", default="voxelize", choices=["voxelize", "downsample", "fps"],
+                    help="voxelize (PointPillars tensors), voxel-grid centroid downsampling, or farthest point "
+                         "sampling (workload lidar65k)")
     ap.add_argument("--batch", type=int, default=1,
                     help="frames per launch (pv_voxelize_batch when > 1; different frames of the workload)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample length")
@@ -200,6 +201,24 @@ def run_reference(args, rank, world):
     import oracle
 
     lib = oracle.load()
+    if args.op == "fps":
+        B = max(1, args.batch)
+        clouds = [synth.fps_cloud(1 + b) for b in range(B)]
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            for c in clouds:
+                oracle.fps(c, synth.FPS_SAMPLES, 0, lib)
+        el = time.perf_counter() - t0
+        value = synth.FPS_POINTS * B * args.steps / el / 1e6
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "Mpoints/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": 0, "ms_per_step": round(1e3 * el / args.steps, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": f"lidar65k: {synth.WORKLOADS['lidar65k']}", "op": "fps", "clouds_per_launch": B},
+                "cpu_baseline": {"value": round(value, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{B} full sampling(s) per step, {args.steps} steps, C++ O(N*M) loop"},
+                "e2e": {"value": round(value, 3), "unit": "Mpoints/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     if args.batch > 1:
         pts, frame_off, P = synth.make_batch(args.workload, args.batch)
         frames = [pts[frame_off[b]:frame_off[b + 1]] for b in range(args.batch)]
@@ -230,6 +249,120 @@ def run_reference(args, rank, world):
         "cpu_baseline": {"value": round(value, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
                          "sample": f"{args.batch} full frame(s) per step, {args.steps} steps, single-threaded C++ std::map oracle"},
         "e2e": {"value": round(value, 3), "unit": "Mpoints/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# Plain fp32 lanes of the GPU (no multiply-add is used by the FPS distances):
+# 152 SMs x 128 lanes x 2.07 GHz maximum SM clock.
+FP32_LANES_PER_SM = 128
+
+
+def run_fps(args, rank, world, local_rank):
+    """Farthest point sampling: B clouds of 65,536 points, 4,096 samples each."""
+    import numpy as np
+    import torch
+
+    import lidar_point_cloud_gb300 as pv
+    from lidar_point_cloud_gb300 import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B, N, M = max(1, args.batch), synth.FPS_POINTS, synth.FPS_SAMPLES
+    clouds = np.stack([synth.fps_cloud(1 + b) for b in range(B)])
+    src = torch.from_numpy(clouds).to(dev)
+    pts = src if B > 1 else src[0]
+    lead = (B,) if B > 1 else ()
+    idx = torch.empty(lead + (M,), dtype=torch.int32, device=dev)
+    smp = torch.empty(lead + (M, 4), dtype=torch.float32, device=dev)
+    status = torch.zeros((1,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pv.fps_into(pts, M, idx, smp, status, 0, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status")
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for k in range(args.steps):
+        starts[k].record(stream)
+        step()
+        ends[k].record(stream)
+    r1.record(stream)
+    torch.cuda.synchronize(dev)
+    region_ms = max_over_ranks(r0.elapsed_time(r1), device=dev)
+    kernel_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    t_soak = time.perf_counter()
+    while sampler and time.perf_counter() - t_soak < 1.5:
+        step()
+        torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+    if rank != 0:
+        return
+    value = whole_job_rate(B * N, args.steps, world, region_ms)
+    ops = 8.0 * N * (M - 1) * B  # 3 subtractions, 3 products, 2 sums per point per sample
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak_ops = sms * FP32_LANES_PER_SM * 2.07e9
+    achieved = ops / (kernel_ms * 1e-3)
+    # End to end: pinned host clouds in, indices and samples out.
+    pin = torch.from_numpy(clouds).pin_memory()
+    pin_in = pin if B > 1 else pin[0]
+    h_idx = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
+    h_smp = torch.empty(smp.shape, dtype=torch.float32).pin_memory()
+    e_steps = max(3, args.e2e_steps // 10)
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        d = pin_in.to(dev, non_blocking=True)
+        pv.fps_into(d, M, idx, smp, status, 0, stream)
+        h_idx.copy_(idx, non_blocking=True)
+        h_smp.copy_(smp, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = time.perf_counter() - t0
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        lib = oracle.load()
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds or reps == 0:
+            oracle.fps(clouds[0], M, 0, lib)
+            reps += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": round(N * reps / el / 1e6, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
+               "sample": f"{reps} full sampling(s) of one cloud ({el:.1f} s), single-threaded C++ O(N*M) loop"}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "Mpoints/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(region_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"lidar65k: {synth.WORKLOADS['lidar65k']}", "op": "fps", "clouds_per_launch": B,
+                   "N": N, "samples": M, "launch": f"{B} cluster(s) of 8 CTAs x 1024 threads, cloud in shared memory",
+                   "l2": "the cloud is read once per launch into shared memory; no L2 reuse between samples",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "alu", "achieved": round(achieved / 1e9, 1), "peak": round(peak_ops / 1e9, 1),
+                     "unit": "Gop/s", "frac": round(achieved / peak_ops, 4), "traffic": None,
+                     "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2.07 GHz",
+                     "kernel": "pv_fps_kernel", "ops_per_launch": ops,
+                     "avg_launch_us": round(kernel_ms * 1e3, 3)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(N * B * e_steps / e2e_s / 1e6, 3), "unit": "Mpoints/s",
+                "h2d_bytes_per_step": 16 * N * B, "d2h_bytes_per_step": 4 * M * B + 16 * M * B,
+                "api": "fps_into with pinned host copies in and out, synchronous", "steps": e_steps},
+        "gpu_launches": args.steps, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
 
@@ -451,7 +584,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        run_gb300(args, rank, world, local_rank)
+        if args.op == "fps":
+            run_fps(args, rank, world, local_rank)
+        else:
+            run_gb300(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

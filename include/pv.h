@@ -190,6 +190,32 @@ int pv_voxel_downsample(const float* points, int64_t num_points, const float poi
                         const float voxel_size[3], int max_voxels, float* out_centroids, int32_t* out_coords,
                         int32_t* out_counts, int32_t* out_num_voxels, pv_stream_t stream);
 
+/*
+ * Farthest point sampling, the operation the RadiusFPS page accelerates
+ * ("Baseline: classic GPU FPS"; its spherical-voxel pruning skips only
+ * updates that cannot change a distance, so the samples are those of plain
+ * FPS).  From point `start`, every point keeps its smallest squared distance
+ * to the samples so far, ((dx*dx) + (dy*dy)) + (dz*dz) in float rounded to
+ * nearest (intensity ignored); the next sample is the point with the largest
+ * one, ties to the lowest index.  The result is unique and bit-reproducible.
+ *   points        device, [num_clouds, num_points, 4] float32, 16-byte aligned;
+ *                 x, y, z finite (else *out_status = PV_ERR_INVALID).
+ *   num_points    points per cloud, 1 .. PV_FPS_MAX_POINTS.
+ *   num_samples   samples per cloud, >= 1 (past the distinct points the
+ *                 remaining distances are 0 and the lowest index repeats).
+ *   start         first sample, 0 .. num_points - 1 (PointNet++ takes 0).
+ *   out_indices   device, [num_clouds, num_samples] int32, indices inside each cloud.
+ *   out_samples   device, [num_clouds, num_samples, 4] float32 copies of the
+ *                 sampled points, or NULL.
+ *   out_status    device, one int32: 0, or a negative status found on the device.
+ * Returns PV_OK or a negative status found on the host (nothing enqueued).
+ * Each cloud runs in one cluster of 8 CTAs holding it in distributed shared
+ * memory; clouds run side by side.
+ */
+#define PV_FPS_MAX_POINTS 106496
+int pv_fps(const float* points, int num_clouds, int64_t num_points, int64_t num_samples, int64_t start,
+           int32_t* out_indices, float* out_samples, int32_t* out_status, pv_stream_t stream);
+
 int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cloud_range[6],
                    const float voxel_size[3], int max_points, int max_voxels, float* out_voxels,
                    int32_t* out_coords, int32_t* out_counts, int32_t* out_num_voxels,

@@ -7,6 +7,7 @@ package is its thin Python binding plus seeded synthetic inputs
 
 from ._binding import (  # noqa: F401
     EXPORTS,
+    FPS_MAX_POINTS,
     MAX_FRAMES,
     PVError,
     alloc_batch_outputs,
@@ -14,6 +15,8 @@ from ._binding import (  # noqa: F401
     alloc_outputs,
     downsample,
     downsample_into,
+    fps,
+    fps_into,
     grid_size,
     lib_path,
     load,

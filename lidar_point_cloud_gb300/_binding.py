@@ -31,8 +31,11 @@ STATUS = {
 
 EXPORTS = (
     "pv_voxelize", "pv_voxelize_ex", "pv_voxelize_host", "pv_voxelize_static", "pv_voxelize_batch",
-    "pv_voxel_downsample", "pv_grid_size", "pv_query_plan", "pv_release_workspace", "pv_status_string", "pv_version",
+    "pv_voxel_downsample", "pv_fps", "pv_grid_size", "pv_query_plan", "pv_release_workspace", "pv_status_string",
+    "pv_version",
 )
+
+FPS_MAX_POINTS = 106496  # PV_FPS_MAX_POINTS
 
 MAX_FRAMES = 256  # PV_MAX_FRAMES
 
@@ -95,6 +98,8 @@ def load(path: Optional[str] = None):
         lib.pv_voxelize_batch.restype = ci
         lib.pv_voxel_downsample.argtypes = [vp, i64, f, f, ci, vp, vp, vp, vp, vp]
         lib.pv_voxel_downsample.restype = ci
+        lib.pv_fps.argtypes = [vp, ci, i64, i64, i64, vp, vp, vp, vp]
+        lib.pv_fps.restype = ci
         lib.pv_grid_size.argtypes = [f, f, ctypes.POINTER(ctypes.c_int64)]
         lib.pv_grid_size.restype = ci
         lib.pv_query_plan.argtypes = [i64, f, f, ci, ci, ctypes.POINTER(Options), ctypes.POINTER(Plan)]
@@ -360,3 +365,53 @@ def downsample(points, point_cloud_range, voxel_size, max_voxels: int = 1 << 20,
         if V < 0:
             raise PVError(V, "pv_voxel_downsample (device)")
         return out[0][:V], out[1][:V], out[2][:V]
+
+
+def fps_into(points, num_samples: int, out_indices, out_samples=None, out_status=None, start: int = 0,
+             stream=None) -> None:
+    """Enqueue farthest point sampling of one cloud [N, 4] or a batch [B, N, 4]
+    into out_indices ([M] or [B, M] int32) and optionally out_samples
+    ([.., M, 4] float32).  out_status (one int32, device) receives 0 or a
+    negative status; it is allocated and checked by :func:`fps` when not given."""
+    torch = _torch()
+    if not isinstance(points, torch.Tensor) or points.dtype != torch.float32 or not points.is_cuda:
+        raise TypeError("points must be a float32 CUDA tensor")
+    if points.dim() not in (2, 3) or points.shape[-1] != 4 or not points.is_contiguous():
+        raise ValueError("points must be a contiguous [N, 4] or [B, N, 4] tensor")
+    B = 1 if points.dim() == 2 else int(points.shape[0])
+    N = int(points.shape[-2])
+    M = int(num_samples)
+    want = (M,) if points.dim() == 2 else (B, M)
+    if out_indices.dtype != torch.int32 or tuple(out_indices.shape) != want or not out_indices.is_contiguous():
+        raise ValueError("out_indices has the wrong dtype, shape or layout")
+    if out_samples is not None and (out_samples.dtype != torch.float32 or tuple(out_samples.shape) != want + (4,)
+                                    or not out_samples.is_contiguous()):
+        raise ValueError("out_samples has the wrong dtype, shape or layout")
+    if out_status is None or out_status.dtype != torch.int32 or out_status.numel() != 1:
+        raise ValueError("out_status must be one int32 on the device")
+    if stream is None:
+        stream = torch.cuda.current_stream(points.device)
+    handle = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    st = load().pv_fps(ctypes.c_void_p(points.data_ptr()), B, N, M, int(start),
+                       ctypes.c_void_p(out_indices.data_ptr()),
+                       ctypes.c_void_p(out_samples.data_ptr() if out_samples is not None else 0),
+                       ctypes.c_void_p(out_status.data_ptr()), handle)
+    if st != 0:
+        raise PVError(st, "pv_fps")
+
+
+def fps(points, num_samples: int, start: int = 0, return_samples: bool = False, stream=None):
+    """Farthest point sampling (exact; ties to the lowest index).  Returns the
+    sample indices ([M] or [B, M] int32) and, if asked, the sampled points."""
+    torch = _torch()
+    with torch.no_grad():
+        lead = () if points.dim() == 2 else (int(points.shape[0]),)
+        idx = torch.empty(lead + (int(num_samples),), dtype=torch.int32, device=points.device)
+        smp = (torch.empty(lead + (int(num_samples), 4), dtype=torch.float32, device=points.device)
+               if return_samples else None)
+        status = torch.empty((1,), dtype=torch.int32, device=points.device)
+        fps_into(points, num_samples, idx, smp, status, start, stream)
+        st = int(status.item())
+        if st != 0:
+            raise PVError(st, "pv_fps (device)")
+        return (idx, smp) if return_samples else idx

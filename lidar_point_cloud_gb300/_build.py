@@ -8,7 +8,8 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "pv_voxelize.cu")
+SRC = os.path.join(PKG, "csrc", "pv_voxelize.cu")  # voxelizer, downsampling and their C ABI
+SRCS = [SRC, os.path.join(PKG, "csrc", "pv_fps.cu")]  # every translation unit of libpv.so
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libpv.so")
 
@@ -20,6 +21,7 @@ NVCC_FLAGS = [
     "-ftz=false", "-prec-div=true", "-prec-sqrt=true", "-fmad=false",
     "-Xcompiler", "-fPIC", "-shared",
 ]
+COMPILE_FLAGS = [f for f in NVCC_FLAGS if f != "-shared"]
 
 
 def nvcc_path() -> str:
@@ -33,7 +35,7 @@ def nvcc_path() -> str:
 
 
 def sources():
-    return [SRC, os.path.join(INCLUDE, "pv.h")]
+    return [*SRCS, os.path.join(INCLUDE, "pv.h")]
 
 
 def is_stale(lib: str = LIB) -> bool:
@@ -44,13 +46,29 @@ def is_stale(lib: str = LIB) -> bool:
 
 
 def build(out: str = LIB, extra=(), verbose: bool = False) -> str:
-    """Compile the library; returns its path."""
+    """Compile every translation unit (in parallel) and link the library; returns its path."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    objs = [f"{out}.{os.path.splitext(os.path.basename(src))[0]}.o" for src in SRCS]
+
+    def compile_one(src, obj):
+        cmd = [nvcc_path(), *COMPILE_FLAGS, *extra, "-I", INCLUDE, "-c", src, "-o", obj]
+        return subprocess.run(cmd, capture_output=True, text=True)
+
+    with ThreadPoolExecutor(max_workers=len(SRCS)) as ex:
+        results = list(ex.map(compile_one, SRCS, objs))
+    for res in results:
+        if res.returncode != 0:
+            raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
+        if verbose:
+            print(res.stdout + res.stderr)
     tmp = out + ".tmp"
-    cmd = [nvcc_path(), *NVCC_FLAGS, *extra, "-I", INCLUDE, SRC, "-o", tmp]
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
-    if verbose:
-        print(res.stdout + res.stderr)
+    link = subprocess.run([nvcc_path(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", *objs, "-o", tmp],
+                          capture_output=True, text=True)
+    for o in objs:
+        if os.path.exists(o):
+            os.remove(o)
+    if link.returncode != 0:
+        raise RuntimeError("nvcc link failed:\n" + link.stdout + link.stderr)
     os.replace(tmp, out)
     return out

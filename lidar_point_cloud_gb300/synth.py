@@ -326,6 +326,18 @@ def make_batch(name: str, frames: int) -> Tuple[np.ndarray, np.ndarray, Params]:
     return np.concatenate(parts), off, P
 
 
+FPS_POINTS = 65_536   # the RadiusFPS page's benchmark: N = 65,536 points,
+FPS_SAMPLES = 4_096   # M = 4,096 samples
+
+
+def fps_cloud(seed: int = 1, n: int = FPS_POINTS) -> np.ndarray:
+    """A LiDAR-shaped cloud for farthest point sampling: the first n returns
+    of the KITTI-shaped frame of this seed whose x, y, z are finite."""
+    pts = kitti(seed)
+    ok = np.all(np.isfinite(pts[:, :3]), axis=1)
+    return np.ascontiguousarray(pts[ok][:n])
+
+
 WORKLOADS: Dict[str, str] = {
     "tiny": "4,096 uniform + 16 boundary points, 432x496 grid, 16,000 pillars",
     "kitti": "122,880-return 64-beam frame, 432x496 grid, 16,000 pillars",
@@ -335,4 +347,5 @@ WORKLOADS: Dict[str, str] = {
     "kitti3d": "122,880-return 64-beam frame, 432x496x16 voxels (0.25 m layers), 40,000 voxels",
     "second": "122,880-return 64-beam frame, 1408x1600x40 voxels (0.05x0.05x0.1 m), 5 points, 40,000 voxels",
     "dense3d": "1,048,576-return 128-beam frame, 1024x1024x4 voxels (2 m layers), 60,000 voxels",
+    "lidar65k": "farthest point sampling: 65,536 returns of the 64-beam frame, 4,096 samples",
 }

@@ -1,0 +1,100 @@
+"""GPU parity of farthest point sampling: sample indices bit-identical to the
+oracle's (the distances are the same float operations in the same order, and
+ties go to the lowest index on both sides).
+
+Covers the page's benchmark size (65,536 points, 4,096 samples), the largest
+cloud one launch holds, clouds of a few points (CTAs of the cluster without
+points), exact ties on a lattice, several start points, more samples than
+distinct points, batches of clouds, the sampled-point copies, and
+non-finite input reported on the device.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+
+torch = pytest.importorskip("torch")
+pv = pytest.importorskip("lidar_point_cloud_gb300")
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pv.load()
+    yield
+
+
+def cloud(n, seed, scale=50.0):
+    rng = np.random.default_rng(seed)
+    return (rng.random((n, 4)) * scale).astype(np.float32)
+
+
+def check(pts, m, start=0):
+    st, ref = oracle.fps(pts, m, start)
+    assert st == 0
+    got = pv.fps(torch.from_numpy(pts).to(DEV), m, start).cpu().numpy()
+    assert np.array_equal(got, ref), f"first difference at sample {int(np.argmax(got != ref))}"
+
+
+def test_page_benchmark_size():
+    check(cloud(65_536, 1), 4096)
+
+
+def test_largest_cloud():
+    check(cloud(pv.FPS_MAX_POINTS, 2), 1024, start=777)
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 8, 9, 100, 8193])
+def test_small_and_ragged_clouds(n):
+    check(cloud(n, 3 + n), min(3 * n, 300))
+
+
+def test_lattice_ties():
+    g = np.stack(np.meshgrid(np.arange(20), np.arange(20), np.arange(5), indexing="ij"), -1).reshape(-1, 3)
+    pts = np.concatenate([g, np.zeros((g.shape[0], 1))], 1).astype(np.float32)
+    check(pts, 1200)
+    check(pts, 700, start=1234)
+
+
+def test_duplicates_and_more_samples_than_points():
+    pts = cloud(300, 5)
+    pts = np.concatenate([pts, pts[:100]])  # exact duplicates
+    check(pts, 600)
+
+
+def test_batch_of_clouds_and_samples():
+    B, N, M = 12, 20_000, 512
+    pts = np.stack([cloud(N, 100 + b) for b in range(B)])
+    idx, smp = pv.fps(torch.from_numpy(pts).to(DEV), M, start=3, return_samples=True)
+    idx, smp = idx.cpu().numpy(), smp.cpu().numpy()
+    for b in range(B):
+        st, ref = oracle.fps(pts[b], M, 3)
+        assert np.array_equal(idx[b], ref)
+        assert smp[b].tobytes() == pts[b][ref].tobytes()
+
+
+def test_non_finite_input_is_reported():
+    pts = cloud(1000, 6)
+    pts[500, 2] = np.inf
+    with pytest.raises(pv.PVError):
+        pv.fps(torch.from_numpy(pts).to(DEV), 10)
+    check(cloud(1000, 7), 50)  # and the next call is clean
+
+
+def test_fps_argument_errors():
+    t = torch.zeros((10, 4), dtype=torch.float32, device=DEV)
+    with pytest.raises(pv.PVError):
+        pv.fps(t, 0)
+    with pytest.raises(pv.PVError):
+        pv.fps(t, 5, start=10)
+    big = torch.zeros((pv.FPS_MAX_POINTS + 1, 4), dtype=torch.float32, device=DEV)
+    with pytest.raises(pv.PVError):
+        pv.fps(big, 5)
