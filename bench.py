@@ -94,8 +94,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sha():
-    src = os.path.join(ROOT, "lidar_point_cloud_gb300", "csrc", "pv_voxelize.cu")
+def kernel_sha(kernel="pv_voxelize_kernel"):
+    """SHA-256 of the source file that holds the kernel."""
+    name = "pv_fps.cu" if kernel == "pv_fps_kernel" else "pv_voxelize.cu"
+    src = os.path.join(ROOT, "lidar_point_cloud_gb300", "csrc", name)
     with open(src, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
 
@@ -111,7 +113,7 @@ def profiled_traffic(workload, kernel="pv_voxelize_kernel"):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256") != kernel_sha():
+    if vals.get("kernel_source_sha256") != kernel_sha(kernel):
         return None
     try:
         return int(vals["dram_bytes_per_launch"])
@@ -356,7 +358,8 @@ def run_fps(args, rank, world, local_rank):
                    "l2": "the cloud is read once per launch into shared memory; no L2 reuse between samples",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "alu", "achieved": round(achieved / 1e9, 1), "peak": round(peak_ops / 1e9, 1),
-                     "unit": "Gop/s", "frac": round(achieved / peak_ops, 4), "traffic": None,
+                     "unit": "Gop/s", "frac": round(achieved / peak_ops, 4),
+                     "traffic": profiled_traffic("lidar65k" + (f"_x{B}" if B > 1 else ""), "pv_fps_kernel"),
                      "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2.07 GHz",
                      "kernel": "pv_fps_kernel", "ops_per_launch": ops,
                      "avg_launch_us": round(kernel_ms * 1e3, 3)},
