@@ -1120,64 +1120,74 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     }
     PV_STAMP(4);
 
-    // ---- phase 2c: empty the slots of pillars past the budget (ranks M..total-1;
-    // per frame in a batch), before the output rows load the memory system
-    // with writes: a list known to end inside positions 0..3 loses those, any
-    // other list every position.
-    const long long dropped = kBatched ? static_cast<long long>(s_dcum[B]) : static_cast<long long>(total - V);
-    for (long long j0 = gwarp * 32; j0 < dropped; j0 += nwarps * 32) {
-      const long long j = j0 + lane;
-      const bool valid = j < dropped;
-      unsigned int rank = static_cast<unsigned int>(M + j);
-      if (kBatched && valid) {
-        const int b = slot_in_cum(s_dcum, B, static_cast<unsigned int>(j));
-        rank = s_fpre[b] + M + static_cast<unsigned int>(j - s_dcum[b]);
-      }
-      const int slot = valid ? slot_of_rank(p, s_prefix, P, rank) : 0;
-      unsigned long long* L = p.lists + static_cast<size_t>(slot) * kHead;  // head row
-      const Head hd = read_head(p, L, valid);
-      const bool short_list = valid && hd.few && !hd.filled;
-      if (short_list) {
-        const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-        reinterpret_cast<uint4*>(L)[0] = e4;
-        reinterpret_cast<uint4*>(L)[1] = e4;
-      }
-      if (valid && p.hash_mode) p.keys[slot] = kNoKey;
-      for (unsigned int m = __ballot_sync(0xffffffffu, valid && !short_list); m != 0u; m &= m - 1u) {
-        const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, __ffs(m) - 1));
-        for (int e = static_cast<int>(lane); e < K; e += 32) *Lu.at(e) = kEmpty64;
-      }
-    }
     PV_STAMP(5);
 
-    // ---- phase 2d: output rows.  Every warp of the grid takes a contiguous
-    // range of ranks (so its output rows are contiguous) and works through
-    // it 32 ranks at a time.  Lane l finds the slot of rank r0 + l and reads
-    // list positions 0..3 (one round trip each for 32 pillars).  A pillar
-    // whose points all come from those groups (its list ends inside them, or
-    // they already hold max_points points) is copied by the warp kEmitUnroll
-    // pillars at a time; the others are emitted one by one from their whole
-    // list.
+    // ---- phase 2c+2d: every ranked pillar, kept or past the budget.  Every
+    // warp of the grid takes an equal contiguous share of the kept rows (so
+    // its output rows are contiguous) and an equal contiguous share of the
+    // pillars past the budget (which only have their lists emptied), and
+    // works through both together, 32 at a time.  Lane l finds the slot of
+    // its pillar and reads list positions 0..3 (one round trip each for 32
+    // pillars).  Past the budget (its frame's, in a batch): a list known to
+    // end inside positions 0..3 loses those, any other list every position.
+    // Kept: a pillar whose points all come from those groups (its list ends
+    // inside them, or they already hold max_points points) is copied by the
+    // warp kEmitUnroll pillars at a time; the others are emitted one by one
+    // from their whole list.
     bool stale = false;
-    const long long per_warp = (static_cast<long long>(V) + nwarps - 1) / nwarps;
-    const long long rw0 = gwarp * per_warp;
-    const long long rw1 = rw0 + per_warp < static_cast<long long>(V) ? rw0 + per_warp : static_cast<long long>(V);
-    for (long long r0 = rw0; r0 < rw1; r0 += 32) {
-      const long long k = r0 + lane;  // the k-th row written (frames one after the other)
-      const bool valid = k < rw1;
-      long long row = k;              // output row: frame * max_voxels + rank inside the frame
-      unsigned int rank = static_cast<unsigned int>(k);
+    // (Counts of pillars and warps fit 32 bits: N < 2^29, at most 1024 x 32 warps.)
+    const unsigned int dropped = kBatched ? s_dcum[B] : total - V;
+    const unsigned int nw = static_cast<unsigned int>(nwarps), gw = static_cast<unsigned int>(gwarp);
+    const unsigned int pk = (V + nw - 1) / nw;
+    const unsigned int kw0 = gw * pk < V ? gw * pk : V;
+    const unsigned int nk = (kw0 + pk < V ? kw0 + pk : V) - kw0;
+    const unsigned int pd = (dropped + nw - 1) / nw;
+    const unsigned int dw0 = gw * pd < dropped ? gw * pd : dropped;
+    const unsigned int nd = (dw0 + pd < dropped ? dw0 + pd : dropped) - dw0;
+    for (unsigned int t0 = 0; t0 < nk + nd; t0 += 32) {
+      const unsigned int t = t0 + lane;
+      const bool valid = t < nk;                  // kept: an output row
+      const bool drop = !valid && t < nk + nd;    // past the budget
+      const bool in_range = valid || drop;
+      long long row = 0;
+      unsigned int rank = 0;
       int fb = 0;
-      if (kBatched && valid) {
-        fb = slot_in_cum(s_vcum, B, static_cast<unsigned int>(k));
-        const unsigned int loc = static_cast<unsigned int>(k) - s_vcum[fb];
-        rank = s_fpre[fb] + loc;
-        row = static_cast<long long>(fb) * M + loc;
+      if (valid) {
+        const unsigned int k = kw0 + t;  // the k-th row written (frames one after the other)
+        rank = k;
+        row = k;
+        if (kBatched) {
+          fb = slot_in_cum(s_vcum, B, k);
+          const unsigned int loc = k - s_vcum[fb];
+          rank = s_fpre[fb] + loc;
+          row = static_cast<long long>(fb) * M + loc;
+        }
+      } else if (drop) {
+        const unsigned int j = dw0 + (t - nk);  // the j-th pillar past a budget
+        rank = M + j;
+        if (kBatched) {
+          const int b = slot_in_cum(s_dcum, B, j);
+          rank = s_fpre[b] + M + (j - s_dcum[b]);
+        }
       }
       int slot = 0;
-      if (valid) slot = slot_of_rank(p, s_prefix, P, rank);
+      if (in_range) slot = slot_of_rank(p, s_prefix, P, rank);
       unsigned long long* L = p.lists + static_cast<size_t>(slot) * kHead;  // head row
-      Head hd = read_head(p, L, valid);
+      Head hd = read_head(p, L, in_range);
+      {  // past the budget: empty the list
+        const bool short_drop = drop && hd.few && !hd.filled;
+        if (short_drop) {
+          const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
+          reinterpret_cast<uint4*>(L)[0] = e4;
+          reinterpret_cast<uint4*>(L)[1] = e4;
+        }
+        if (drop && p.hash_mode) p.keys[slot] = kNoKey;
+        for (unsigned int m = __ballot_sync(0xffffffffu, drop && !short_drop); m != 0u; m &= m - 1u) {
+          const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, __ffs(m) - 1));
+          for (int e = static_cast<int>(lane); e < K; e += 32) *Lu.at(e) = kEmpty64;
+        }
+      }
+
       int key = slot;
       if (valid && p.hash_mode) key = __ldcg(p.keys + slot);
       const bool few = valid && hd.few;
