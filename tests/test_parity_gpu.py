@@ -232,3 +232,16 @@ def test_sliced_python_entry_point():
     st, ov, oc, on, oV = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, 32, 16000)
     assert vox.shape == (oV, 32, 4) and coords.shape == (oV, 3) and counts.shape == (oV,)
     assert same_bits(vox.cpu().numpy(), ov[:oV])
+
+
+def test_large_cloud_64m_points():
+    # 64 M points (1 GiB of input): chunks of about 440,000 points a block, so
+    # the chunk map overflows and the per-block loops run hundreds of tiles.
+    rng = np.random.Generator(np.random.PCG64(64))
+    n = 64 * 1024 * 1024
+    pts = np.empty((n, 4), np.float32)
+    pts[:, 0] = rng.random(n, dtype=np.float32) * np.float32(69.12)
+    pts[:, 1] = rng.random(n, dtype=np.float32) * np.float32(79.36) - np.float32(39.68)
+    pts[:, 2] = rng.random(n, dtype=np.float32) * np.float32(4.0) - np.float32(3.0)
+    pts[:, 3] = rng.random(n, dtype=np.float32)
+    assert_parity(pts, KR, KV, 32, 16_000)
