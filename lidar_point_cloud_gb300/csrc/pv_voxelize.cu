@@ -1120,6 +1120,20 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     }
     PV_STAMP(4);
 
+    // ---- phase 2e, issued first: zero rows V .. max_voxels-1 (of every
+    // frame; all blocks share it).  These stores depend on nothing else, so
+    // they overlap the gather's load latencies instead of trailing it.
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const size_t Kz = static_cast<size_t>(K);
+    constexpr size_t cw = kBatched ? 4 : 3;
+    for (int b = 0; b < B; ++b) {
+      const unsigned int Vb = kBatched ? s_vcum[b + 1] - s_vcum[b] : V;
+      const size_t lo = static_cast<size_t>(b) * M + Vb, hi = static_cast<size_t>(b + 1) * M;
+      for (size_t q = lo * Kz + gtid; q < hi * Kz; q += gthreads) p.out_voxels[q] = z4;
+      for (size_t q = cw * lo + gtid; q < cw * hi; q += gthreads) p.out_coords[q] = 0;
+      for (size_t q = lo + gtid; q < hi; q += gthreads) p.out_counts[q] = 0;
+    }
+
     PV_STAMP(5);
 
     // ---- phase 2c+2d: every ranked pillar, kept or past the budget.  Every
@@ -1259,17 +1273,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     if (stale) atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
     PV_STAMP(6);
 
-    // ---- phase 2e: zero rows V .. max_voxels-1 (of every frame; all blocks share it).
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const size_t Kz = static_cast<size_t>(K);
-    constexpr size_t cw = kBatched ? 4 : 3;
-    for (int b = 0; b < B; ++b) {
-      const unsigned int Vb = kBatched ? s_vcum[b + 1] - s_vcum[b] : V;
-      const size_t lo = static_cast<size_t>(b) * M + Vb, hi = static_cast<size_t>(b + 1) * M;
-      for (size_t q = lo * Kz + gtid; q < hi * Kz; q += gthreads) p.out_voxels[q] = z4;
-      for (size_t q = cw * lo + gtid; q < cw * hi; q += gthreads) p.out_coords[q] = 0;
-      for (size_t q = lo + gtid; q < hi; q += gthreads) p.out_counts[q] = 0;
-    }
   }
 
   // ---- the last block to finish publishes the status and rearms the control block.
