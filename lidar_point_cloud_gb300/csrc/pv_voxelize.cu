@@ -204,6 +204,12 @@ __device__ __forceinline__ unsigned int ld_relaxed(const unsigned int* p) {
 
 __device__ __forceinline__ long long lmin(long long a, long long b) { return a < b ? a : b; }
 
+__device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ unsigned int lanemask_lt() {
   unsigned int m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -260,7 +266,9 @@ __device__ bool grid_sync(Control* ctl, unsigned int target, int* s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    // No separate fences: the release reduction covers the block's earlier
+    // writes (ordered before it by the CTA barrier above) and the acquire
+    // load, with the CTA barrier below, passes the other blocks' writes on.
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&ctl->bar) : "memory");
     unsigned int v = ld_acquire(&ctl->bar);
     if (v < target) {
@@ -271,10 +279,10 @@ __device__ bool grid_sync(Control* ctl, unsigned int target, int* s_flag) {
           ok = 0;
           break;
         }
-        v = ld_acquire(&ctl->bar);
+        v = ld_relaxed(&ctl->bar);  // relaxed polls; the count is acquired once it is reached
       } while (v < target);
+      if (ok) v = ld_acquire(&ctl->bar);
     }
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     *s_flag = ok;
   }
   __syncthreads();
@@ -1279,10 +1287,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   PV_STAMP(7);
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    const unsigned int prev = atomicAdd(&p.ctl->done, 1u);
+    // Acquire-release count of finished blocks: the last one sees every
+    // block's writes (their error words included) before it reads them.
+    const unsigned int prev = atom_add_acq_rel(&p.ctl->done, 1u);
     if (prev == P - 1) {
-      __threadfence();
       const int err = *reinterpret_cast<volatile int*>(&p.ctl->err);
       if (kBatched) {
         for (int b = 0; b < B; ++b)
@@ -1296,7 +1304,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       p.ctl->done = 0;
       const unsigned int next = epoch + 1;
       p.ctl->epoch = next == 0 ? 1u : next;
-      __threadfence();
     }
   }
 }
@@ -1453,10 +1460,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel
 
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    const unsigned int prev = atomicAdd(&p.ctl->done, 1u);
+    // Acquire-release count of finished blocks: the last one sees every
+    // block's writes (their error words included) before it reads them.
+    const unsigned int prev = atom_add_acq_rel(&p.ctl->done, 1u);
     if (prev == P - 1) {
-      __threadfence();
       const int err = *reinterpret_cast<volatile int*>(&p.ctl->err);
       *p.out_num = err != 0 ? err : static_cast<int32_t>(V);
       p.ctl->dirty = err != 0 ? 1u : 0u;
@@ -1466,7 +1473,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel
       p.ctl->created = 0;
       const unsigned int next = epoch + 1;
       p.ctl->epoch = next == 0 ? 1u : next;
-      __threadfence();
     }
   }
 }
@@ -1706,10 +1712,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
 
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    const unsigned int prev = atomicAdd(&p.ctl->done, 1u);
+    // Acquire-release count of finished blocks: the last one sees every
+    // block's writes (their error words included) before it reads them.
+    const unsigned int prev = atom_add_acq_rel(&p.ctl->done, 1u);
     if (prev == P - 1) {
-      __threadfence();
       const int err = *reinterpret_cast<volatile int*>(&p.ctl->err);
       *p.out_num = err != 0 ? err : static_cast<int32_t>(V);
       p.ctl->dirty = err != 0 ? 1u : 0u;
@@ -1718,7 +1724,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
       p.ctl->done = 0;
       const unsigned int next = epoch + 1;
       p.ctl->epoch = next == 0 ? 1u : next;
-      __threadfence();
     }
   }
   (void)gwarp;
