@@ -260,8 +260,9 @@ __device__ __forceinline__ void pv_wait_reg(unsigned int v) {
 // past the time limit (PV_ERR_TIMEOUT is then recorded).  `target` counts
 // arrivals since the launch began (P for the first barrier, 2P for the next).
 // Thread 0 arrives with a release reduction (the block's earlier writes are
-// ordered before it by the CTA barrier), polls with acquire loads, and the
-// closing CTA barrier passes the acquired view to the rest of the block.
+// ordered before it by the CTA barrier), polls with relaxed loads, acquires
+// the count once it is reached, and the closing CTA barrier passes the
+// acquired view to the rest of the block.
 __device__ bool grid_sync(Control* ctl, unsigned int target, int* s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
