@@ -354,8 +354,8 @@ def run_fps(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(region_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"lidar65k: {synth.WORKLOADS['lidar65k']}", "op": "fps", "clouds_per_launch": B,
-                   "N": N, "samples": M, "launch": f"{B} cluster(s) of 8 CTAs x 1024 threads, cloud in shared memory",
-                   "l2": "the cloud is read once per launch into shared memory; no L2 reuse between samples",
+                   "N": N, "samples": M, "launch": f"{B} cluster(s), one a cloud: 16 CTAs x 256 threads (16 points a thread in registers) while the clouds fit on the GPU at once, else 8 CTAs x 256 (32 points a thread)",
+                   "l2": "the cloud is read once per launch into registers; no memory traffic between samples",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "alu", "achieved": round(achieved / 1e9, 1), "peak": round(peak_ops / 1e9, 1),
                      "unit": "Gop/s", "frac": round(achieved / peak_ops, 4),

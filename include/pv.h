@@ -209,8 +209,9 @@ int pv_voxel_downsample(const float* points, int64_t num_points, const float poi
  *                 sampled points, or NULL.
  *   out_status    device, one int32: 0, or a negative status found on the device.
  * Returns PV_OK or a negative status found on the host (nothing enqueued).
- * Each cloud runs in one cluster of 8 CTAs holding it in distributed shared
- * memory; clouds run side by side.
+ * Each cloud runs in one thread-block cluster holding it on chip (16 CTAs
+ * while the launch's clouds fit on the GPU at once in such clusters, else 8);
+ * clouds run side by side.
  */
 #define PV_FPS_MAX_POINTS 106496
 int pv_fps(const float* points, int num_clouds, int64_t num_points, int64_t num_samples, int64_t start,

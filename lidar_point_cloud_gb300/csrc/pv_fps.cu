@@ -8,23 +8,31 @@
 // theorem) skips only updates that cannot change a distance, so it never
 // changes the samples.
 //
-// How: one thread-block cluster of 8 CTAs per cloud keeps the whole cloud in
-// registers (8 points a thread: clouds up to 65,536 points) or in shared
-// memory (16 bytes a point, up to 13,312 points a CTA), so an iteration never
-// touches global memory.  Iteration k: every thread updates its running
-// minima against the last sample and keeps its farthest point as one 64-bit
-// key (distance bits high, complement of the index low: a larger key is a
-// larger distance, then a lower index); warps, then warp 0, reduce the keys,
-// and warp 0 pushes the CTA's best (key and coordinates) into every CTA of
-// the cluster through distributed shared memory, into slots kept by
-// iteration parity; one cluster barrier; then every warp picks the winner
-// among the 8 CTA bests from its own shared memory: the next query.  One
-// block barrier and one cluster barrier per sample; nothing waits on
-// another cluster.
+// How: one thread-block cluster per cloud keeps the whole cloud on chip, so
+// an iteration never touches global memory: 16 CTAs of 256 threads with 16
+// points a thread in registers, or 8 CTAs of 256 threads with 32 points a
+// thread when a launch has more clouds than the GPU holds 16-CTA clusters
+// (clouds up to 65,536 points); 8 CTAs of 1024 threads with the points in
+// shared memory (16 bytes a point, up to 13,312 points a CTA) beyond.
+// Iteration k: every thread updates its running minima against the last
+// sample and takes its farthest point (largest distance, then lowest index);
+// each warp reduces (distance bits, index) with two redux instructions, one
+// block barrier, and warp 0 reduces the warps' bests, reads the winner's
+// coordinates from the CTA's shared copy and stores (distance bits, index,
+// coordinates) into this CTA's slot in every CTA of the cluster (st.async
+// into distributed shared memory, slots and barriers kept by iteration
+// parity), each store counting its bytes on the receiving CTA's mbarrier.
+// When a CTA's barrier has seen every CTA's entry, each of its warps picks
+// the winner from its own shared memory: the next query.  No cluster barrier
+// inside the loop; nothing waits on another cluster.
 //
 // Distances: ((dx * dx) + (dy * dy)) + (dz * dz) in float, each operation
-// rounded to nearest and none contracted, as in the oracle, so the keys and
-// therefore the samples are bit-identical.
+// rounded to nearest and none contracted, as in the oracle, so the samples
+// are bit-identical.  The scalar intrinsics are used on purpose: the paired
+// fp32 instructions (sub/mul/add.rn.f32x2) were fused by the code generator
+// into a multiply-add in this kernel's context despite the explicit rounding
+// mode, which changed about one distance in five by an ulp and with it, on
+// LiDAR-shaped clouds full of near-ties, the samples.
 
 #include "pv.h"
 
@@ -38,12 +46,30 @@ namespace cg = cooperative_groups;
 
 namespace {
 
-constexpr int kCluster = 8;
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
-constexpr int kCapPerCta = PV_FPS_MAX_POINTS / kCluster;  // points held by one CTA
+// Clouds up to 65,536 points live in registers: in clusters of 16 CTAs (the
+// non-portable cluster size) while a launch's clouds all fit on the GPU at
+// once in such clusters, else in clusters of 8 CTAs.  Larger clouds (up to
+// PV_FPS_MAX_POINTS) take clusters of 8 CTAs of 1024 threads with the points
+// in shared memory.  Measured on the 65,536-point LiDAR-shaped cloud with
+// 4,096 samples: 16 CTAs x 256 threads 2.51 ms (x 512: 2.77, x 128: 2.52);
+// 8 CTAs x 256 threads 3.9 ms, and 6.5-6.8 ms for 19 clouds at once.
+constexpr int kRegsPoints = 65536;
+constexpr int kWideCluster = 16;
+constexpr int kWideThreads = 256;
+constexpr int kWidePer = kRegsPoints / (kWideCluster * kWideThreads);
+constexpr int kNarrowCluster = 8;
+constexpr int kNarrowThreads = 256;
+constexpr int kNarrowPer = kRegsPoints / (kNarrowCluster * kNarrowThreads);
+constexpr int kClusterSmem = 8;
+constexpr int kThreadsSmem = 1024;
+constexpr int kCapPerCta = PV_FPS_MAX_POINTS / kClusterSmem;  // points held by one CTA
 constexpr int kSmemBytes = kCapPerCta * 16;
-static_assert(kSmemBytes + 2048 <= 227 * 1024, "a CTA's share of the cloud and the exchange slots fit");
+// One CTA a SM: a cluster spread over as many SMs as it has CTAs.
+constexpr int kSmemFloor = 120 * 1024;
+static_assert(kWidePer * kWideCluster * kWideThreads == kRegsPoints && kNarrowPer * kNarrowCluster * kNarrowThreads == kRegsPoints,
+              "65,536 points fill the registers");
+static_assert(kSmemBytes + 2 * kClusterSmem * (kThreadsSmem / 32) * 24 + 256 <= 227 * 1024,
+              "a CTA's share of the cloud and the exchange slots fit");
 
 struct FpsParams {
   const float4* points;  // [B][n]
@@ -54,17 +80,6 @@ struct FpsParams {
   float4* out_samples;   // [B][m] or null
   int32_t* status;       // one int32: 0 or a negative status
 };
-
-// A best point of an iteration: distance bits (a non-negative float orders
-// like its bits), index, coordinates.  Larger distance wins, then the lower
-// index.
-struct Best {
-  unsigned int dbits;
-  unsigned int idx;
-  float x, y, z;
-  unsigned int pad[3];
-};
-static_assert(sizeof(Best) == 32, "two 16-byte stores");
 
 __device__ __forceinline__ bool finite3(const float4& v) {
   return ((__float_as_uint(v.x) & 0x7f800000u) != 0x7f800000u) &&
@@ -80,28 +95,6 @@ __device__ __forceinline__ float dist2(float px, float py, float pz, float qx, f
   return __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)), __fmul_rn(dz, dz));
 }
 
-// The same for two points at once with the paired fp32 instructions (each
-// half rounded to nearest on its own, as the scalar operations).
-__device__ __forceinline__ unsigned long long f32x2(float lo, float hi) {
-  return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
-}
-
-__device__ __forceinline__ void dist2_x2(unsigned long long px, unsigned long long py, unsigned long long pz,
-                                         unsigned long long qx, unsigned long long qy, unsigned long long qz,
-                                         float* d0, float* d1) {
-  unsigned long long dx, dy, dz, sx, sy, sz, s;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dx) : "l"(px), "l"(qx));
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dy) : "l"(py), "l"(qy));
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dz) : "l"(pz), "l"(qz));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(sx) : "l"(dx), "l"(dx));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(sy) : "l"(dy), "l"(dy));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(sz) : "l"(dz), "l"(dz));
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(sx), "l"(sy));
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(s), "l"(sz));
-  *d0 = __uint_as_float(static_cast<unsigned int>(s));
-  *d1 = __uint_as_float(static_cast<unsigned int>(s >> 32));
-}
-
 // Warp argmax of (dbits, idx): the largest distance, then the lowest index.
 // Returns both to every lane.
 __device__ __forceinline__ void warp_best(unsigned int dbits, unsigned int idx, unsigned int* bd, unsigned int* bi) {
@@ -110,83 +103,167 @@ __device__ __forceinline__ void warp_best(unsigned int dbits, unsigned int idx, 
   *bd = d;
 }
 
-// kRegs: the thread's kPerThread points live in registers (clouds of up to
-// kCluster * kThreads * kPerThread points), with a copy of the coordinates in
-// shared memory to look the winner up; otherwise the points live in shared
-// memory.
-constexpr int kPerThread = 8;
+__device__ __forceinline__ unsigned int smem_addr(const void* ptr) {
+  return static_cast<unsigned int>(__cvta_generic_to_shared(ptr));
+}
 
-template <bool kRegs>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1) pv_fps_kernel(const FpsParams p) {
-  extern __shared__ __align__(16) float4 s_pts[];  // (x, y, z, running minimum; unused in the register variant)
-  __shared__ __align__(16) Best s_warp[kWarps];     // this CTA's warp bests
-  __shared__ __align__(16) Best s_in[2][kCluster];  // every CTA's best, pushed by iteration parity
-  __shared__ int s_bad;
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ unsigned int peer_addr(unsigned int addr, unsigned int rank) {
+  unsigned int r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_init(unsigned int bar, unsigned int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// The local arrival of a phase, announcing the bytes the peers will store.
+__device__ __forceinline__ void mbar_expect(unsigned int bar, unsigned int bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(unsigned int bar, unsigned int parity) {
+  unsigned int ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `parity` to complete, for about a second at most.
+__device__ __forceinline__ bool mbar_wait(unsigned int bar, unsigned int parity) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_test(bar, parity))
+    if (global_ns() - t0 > 1000000000ull) return false;
+  return true;
+}
+
+// Stores into a peer CTA's shared memory that count their bytes on the
+// peer's barrier (`bar` is the peer's barrier address).
+__device__ __forceinline__ void push_key(unsigned int addr, unsigned int d, unsigned int i, unsigned int bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "r"(d), "r"(i), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void push_xyz(unsigned int addr, float x, float y, float z, unsigned int bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "f"(x), "f"(y), "f"(z), "f"(0.0f), "r"(bar)
+               : "memory");
+}
+
+// One cluster of kC CTAs of kT threads per cloud.  kP > 0: each thread holds
+// kP points in registers (point tid + t * kT of the CTA's share in slot t),
+// with a copy of the coordinates in shared memory to look a winner up;
+// kP == 0: the points live in shared memory with their running minima.
+//
+// Per sample, every warp pushes its best (distance bits, index, coordinates)
+// into every CTA of the cluster, into the slot of (CTA, warp) of the buffer
+// of the sample's parity; each CTA's barrier of that parity completes when
+// all kC * kT / 32 entries have landed, and every warp then takes the winner
+// among them from its own shared memory.  A buffer is written again two
+// samples later, only by a warp that has seen the next sample's entries of
+// every warp of the cluster, each pushed after its warp had read this buffer.
+template <int kC, int kT, int kP>
+__global__ void __launch_bounds__(kT, 1) pv_fps_kernel(const FpsParams p) {
+  constexpr int kW = kT / 32;
+  constexpr int kE = kC;  // entries a CTA receives per sample: one from each CTA
+  constexpr unsigned int kTx = kE * (8 + 16);
+  extern __shared__ __align__(16) float4 s_pts[];  // (x, y, z, running minimum; unused with kP > 0)
+  __shared__ __align__(8) uint2 s_wk[kW];          // each warp's best (distance bits, index)
+  __shared__ __align__(16) float4 s_q[2][kE];      // coordinates of each entry
+  __shared__ __align__(8) uint2 s_k[2][kE];        // (distance bits, index) of each entry
+  __shared__ __align__(8) unsigned long long s_bar[2];
+  __shared__ int s_bad, s_late;
 
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned int rank = cluster.block_rank();
   const unsigned int tid = threadIdx.x;
   const unsigned int lane = tid & 31u;
   const unsigned int warp = tid >> 5;
-  const long long cloud = blockIdx.x / kCluster;
+  const long long cloud = blockIdx.x / kC;
   const float4* pts = p.points + cloud * p.n;
-  const long long per = (p.n + kCluster - 1) / kCluster;
+  const long long per = (p.n + kC - 1) / kC;
   const long long lo = static_cast<long long>(rank) * per;
   const long long cnt = lo < p.n ? (p.n - lo < per ? p.n - lo : per) : 0;
   const float inf = __int_as_float(0x7f800000);
 
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
+  if (tid == 0) {
+    s_bad = 0;
+    s_late = 0;
+    mbar_init(smem_addr(&s_bar[0]), 1);
+    mbar_init(smem_addr(&s_bar[1]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   bool bad = false;
-  constexpr int R = kRegs ? kPerThread : 2;
-  unsigned long long px2[R / 2], py2[R / 2], pz2[R / 2];
-  float pd[R];
-  for (long long j = tid; j < cnt; j += kThreads) {
+  constexpr int R = kP > 0 ? kP : 1;
+  float px[R], py[R], pz[R], pd[R];
+  for (long long j = tid; j < cnt; j += kT) {
     float4 v = __ldg(pts + lo + j);
     bad |= !finite3(v);
     v.w = inf;  // above every distance
     s_pts[j] = v;
   }
-  if (kRegs) {
+  if (kP > 0) {
 #pragma unroll
-    for (int t = 0; t < kPerThread; t += 2) {
-      const long long j0 = tid + static_cast<long long>(t) * kThreads, j1 = j0 + kThreads;
-      const float4 a = j0 < cnt ? __ldg(pts + lo + j0) : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 b = j1 < cnt ? __ldg(pts + lo + j1) : make_float4(0.f, 0.f, 0.f, 0.f);
-      px2[t / 2] = f32x2(a.x, b.x);
-      py2[t / 2] = f32x2(a.y, b.y);
-      pz2[t / 2] = f32x2(a.z, b.z);
-      pd[t] = j0 < cnt ? inf : -inf;  // -inf: no point, never the farthest
-      pd[t + 1] = j1 < cnt ? inf : -inf;
+    for (int t = 0; t < kP; ++t) {
+      const long long j = tid + static_cast<long long>(t) * kT;
+      const float4 v = j < cnt ? __ldg(pts + lo + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      px[t] = v.x;
+      py[t] = v.y;
+      pz[t] = v.z;
+      pd[t] = j < cnt ? inf : -inf;  // -inf: no point, never the farthest
     }
   }
-  if (bad) s_bad = 1;
+  // Lane c < kC pushes this warp's entry into CTA c.
+  const unsigned int slot = rank;
+  const unsigned int tgt = lane < static_cast<unsigned int>(kC) ? lane : 0u;
+  const unsigned int rk0 = peer_addr(smem_addr(&s_k[0][slot]), tgt), rk1 = peer_addr(smem_addr(&s_k[1][slot]), tgt);
+  const unsigned int rq0 = peer_addr(smem_addr(&s_q[0][slot]), tgt), rq1 = peer_addr(smem_addr(&s_q[1][slot]), tgt);
+  const unsigned int rb0 = peer_addr(smem_addr(&s_bar[0]), tgt), rb1 = peer_addr(smem_addr(&s_bar[1]), tgt);
+  const unsigned int lb0 = smem_addr(&s_bar[0]), lb1 = smem_addr(&s_bar[1]);
   const float4 q0 = __ldg(pts + p.start);
   float qx = q0.x, qy = q0.y, qz = q0.z;
-  if (rank == 0 && tid == 0) p.out_idx[cloud * p.m] = static_cast<int32_t>(p.start);
-  __syncthreads();
+  // Rank 0's last warp, which does not push, writes the sample indices.
+  const bool writer = rank == 0 && warp == static_cast<unsigned int>(kW - 1);
+  int32_t* const out_idx = p.out_idx + cloud * p.m;
+  if (writer && lane == 0) out_idx[0] = static_cast<int32_t>(p.start);
+  __syncthreads();   // the shared copy of the points is complete
+  cluster.sync();    // every CTA's barriers are initialised before any entry is pushed
+  if (bad) s_bad = 1;
 
   for (long long k = 1; k < p.m; ++k) {
     const int par = static_cast<int>(k & 1);
+    const unsigned int parity = static_cast<unsigned int>((k - 1) >> 1) & 1u;
+    const unsigned int lb = par ? lb1 : lb0;
+    if (tid == 0) mbar_expect(lb, kTx);
     // Update the running minima against the last sample; this thread's farthest point.
     float m = -1.0f;
     long long bj = -1;  // point index inside this CTA
-    if (kRegs) {
-      const unsigned long long qx2 = f32x2(qx, qx), qy2 = f32x2(qy, qy), qz2 = f32x2(qz, qz);
+    if (kP > 0) {
 #pragma unroll
-      for (int t = 0; t < kPerThread; t += 2) {
-        float d0, d1;
-        dist2_x2(px2[t / 2], py2[t / 2], pz2[t / 2], qx2, qy2, qz2, &d0, &d1);
-        pd[t] = fminf(pd[t], d0);
-        pd[t + 1] = fminf(pd[t + 1], d1);
-      }
+      for (int t = 0; t < kP; ++t) pd[t] = fminf(pd[t], dist2(px[t], py[t], pz[t], qx, qy, qz));
 #pragma unroll
-      for (int t = 0; t < kPerThread; ++t) m = fmaxf(m, pd[t]);
+      for (int t = 0; t < kP; ++t) m = fmaxf(m, pd[t]);
+      int bt = 0;
 #pragma unroll
-      for (int t = kPerThread - 1; t >= 0; --t)  // the lowest slot (lowest index) holding the maximum
-        if (pd[t] == m) bj = tid + static_cast<long long>(t) * kThreads;
+      for (int t = kP - 1; t >= 0; --t)  // the lowest slot (lowest index) holding the maximum
+        if (pd[t] == m) bt = t;
+      bj = tid + static_cast<long long>(bt) * kT;
     } else {
-      for (long long j = tid; j < cnt; j += kThreads) {
+      for (long long j = tid; j < cnt; j += kT) {
         float4 v = s_pts[j];
         const float d = dist2(v.x, v.y, v.z, qx, qy, qz);
         if (d < v.w) {
@@ -204,51 +281,102 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1) 
     const unsigned int gidx = has ? static_cast<unsigned int>(lo + bj) : 0xFFFFFFFFu;
     unsigned int wd, wi;
     warp_best(dbits, gidx, &wd, &wi);
-    if (has && dbits == wd && gidx == wi) {  // the warp's winner records itself
-      const float4 v = s_pts[bj];
-      Best b;
-      b.dbits = wd;
-      b.idx = wi;
-      b.x = v.x;
-      b.y = v.y;
-      b.z = v.z;
-      s_warp[warp] = b;
-    } else if (lane == 0 && wi == 0xFFFFFFFFu) {  // a warp without points
-      Best b;
-      b.dbits = 0u;
-      b.idx = 0xFFFFFFFFu;
-      b.x = b.y = b.z = 0.f;
-      s_warp[warp] = b;
-    }
+    if (lane == 0) s_wk[warp] = make_uint2(wd, wi);  // (0, none) from a warp without points
     __syncthreads();
-    if (warp == 0) {  // the CTA's best, pushed into every CTA of the cluster (lane c writes CTA c)
-      const Best mine = s_warp[lane];
+    if (warp == 0) {  // the CTA's best, into every CTA of the cluster (lane c stores into CTA c)
+      const bool in = lane < static_cast<unsigned int>(kW);
+      const uint2 e = in ? s_wk[lane] : make_uint2(0u, 0xFFFFFFFFu);
       unsigned int cd, ci;
-      warp_best(mine.dbits, mine.idx, &cd, &ci);
-      const int c = __ffs(__ballot_sync(0xffffffffu, mine.dbits == cd && mine.idx == ci)) - 1;
-      if (lane < static_cast<unsigned int>(kCluster)) *cluster.map_shared_rank(&s_in[par][rank], lane) = s_warp[c];
+      warp_best(e.x, e.y, &cd, &ci);
+      // The CTA's best is one of its own points: its coordinates from the shared copy.
+      const float4 v = ci != 0xFFFFFFFFu ? s_pts[static_cast<long long>(ci) - lo] : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane < static_cast<unsigned int>(kC)) {
+        const unsigned int rb = par ? rb1 : rb0;
+        push_key(par ? rk1 : rk0, cd, ci, rb);
+        push_xyz(par ? rq1 : rq0, v.x, v.y, v.z, rb);
+      }
     }
-    cluster.sync();  // every CTA's best of iteration k is in every CTA
-    // Every warp picks the winner among the 8 CTA bests, from its own shared memory.
-    const bool in = lane < static_cast<unsigned int>(kCluster);
-    const unsigned int td = in ? s_in[par][lane].dbits : 0u;
-    const unsigned int ti = in ? s_in[par][lane].idx : 0xFFFFFFFFu;
+    if (!__all_sync(0xffffffffu, mbar_wait(lb, parity))) {  // a peer stopped: give up
+      if (lane == 0) s_late = 1;
+      break;
+    }
+    // The winner among the cluster's entries, from this CTA's shared memory.
+    const bool inq = lane < static_cast<unsigned int>(kC);
+    const uint2 bk = inq ? s_k[par][lane] : make_uint2(0u, 0xFFFFFFFFu);
+    const float4 bq = inq ? s_q[par][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
     unsigned int gd, gi;
-    warp_best(td, ti, &gd, &gi);
-    const int src = __ffs(__ballot_sync(0xffffffffu, in && td == gd && ti == gi)) - 1;
-    qx = s_in[par][src].x;
-    qy = s_in[par][src].y;
-    qz = s_in[par][src].z;
-    if (rank == 0 && tid == 0) p.out_idx[cloud * p.m + k] = static_cast<int32_t>(gi);
+    warp_best(bk.x, bk.y, &gd, &gi);
+    const int sl = __ffs(__ballot_sync(0xffffffffu, inq && bk.x == gd && bk.y == gi)) - 1;
+    qx = __shfl_sync(0xffffffffu, bq.x, sl);
+    qy = __shfl_sync(0xffffffffu, bq.y, sl);
+    qz = __shfl_sync(0xffffffffu, bq.z, sl);
+    if (writer && lane == 0) out_idx[k] = static_cast<int32_t>(gi);
   }
-  cluster.sync();  // no CTA leaves while a peer may still write into it
+  cluster.sync();  // no CTA leaves while a peer may still store into it
 
-  if (rank == 0 && p.out_samples) {
-    __syncthreads();  // thread 0's index writes are visible to the block
-    for (long long k = tid; k < p.m; k += kThreads)
-      p.out_samples[cloud * p.m + k] = __ldg(pts + p.out_idx[cloud * p.m + k]);
+  if (rank == 0 && p.out_samples && !s_late) {
+    __syncthreads();  // the index writes are visible to the block
+    for (long long k = tid; k < p.m; k += kT) p.out_samples[cloud * p.m + k] = __ldg(pts + out_idx[k]);
   }
   if (tid == 0 && s_bad) atomicMin(p.status, PV_ERR_INVALID);
+  if (tid == 0 && s_late) atomicMin(p.status, PV_ERR_TIMEOUT);
+}
+
+template <int kC, int kT, int kP>
+cudaError_t launch_fps(const FpsParams& fp, int clouds, size_t smem, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned int>(clouds) * kC, 1, 1);
+  cfg.blockDim = dim3(kT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kC;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pv_fps_kernel<kC, kT, kP>, fp);
+}
+
+// Dynamic shared memory of a register-variant CTA: the coordinates of its
+// points, and at least kSmemFloor so that one CTA takes a whole SM.
+inline size_t regs_smem(long long points) {
+  const size_t b = static_cast<size_t>(points) * 16;
+  return b < static_cast<size_t>(kSmemFloor) ? static_cast<size_t>(kSmemFloor) : b;
+}
+
+// How many clusters of this kernel the GPU runs at once (0 if the query fails).
+template <int kC, int kT, int kP>
+int max_clusters(size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kC, 1, 1);
+  cfg.blockDim = dim3(kT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kC;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, pv_fps_kernel<kC, kT, kP>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int kC, int kT, int kP>
+bool prepare_fps(size_t smem) {
+  if (cudaFuncSetAttribute(pv_fps_kernel<kC, kT, kP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return false;
+  if (kC > 8 && cudaFuncSetAttribute(pv_fps_kernel<kC, kT, kP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                    cudaSuccess)
+    return false;
+  return true;
 }
 
 int device_of(const void* ptr) {
@@ -262,13 +390,16 @@ int device_of(const void* ptr) {
 
 std::mutex g_fps_mu;
 bool g_fps_ready[64];
+int g_wide_clusters[64];  // 16-CTA clusters the GPU holds at once (0: never take them)
 
 }  // namespace
 
 extern "C" int pv_fps(const float* points, int num_clouds, int64_t num_points, int64_t num_samples, int64_t start,
                       int32_t* out_indices, float* out_samples, int32_t* out_status, pv_stream_t stream) {
   if (!points || !out_indices || !out_status) return PV_ERR_INVALID;
-  if (num_clouds < 1 || num_points < 1 || num_samples < 1 || start < 0 || start >= num_points) return PV_ERR_INVALID;
+  if (num_clouds < 1 || num_clouds > (1 << 26) || num_points < 1 || num_samples < 1 || start < 0 ||
+      start >= num_points)
+    return PV_ERR_INVALID;
   if (num_samples >= (int64_t(1) << 31) || static_cast<int64_t>(num_clouds) * num_samples >= (int64_t(1) << 31))
     return PV_ERR_INVALID;
   if (num_points > PV_FPS_MAX_POINTS) return PV_ERR_TOO_LARGE;
@@ -287,13 +418,17 @@ extern "C" int pv_fps(const float* points, int num_clouds, int64_t num_points, i
   {
     std::lock_guard<std::mutex> lk(g_fps_mu);
     if (!g_fps_ready[dev]) {
-      if (cudaFuncSetAttribute(pv_fps_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-              cudaSuccess ||
-          cudaFuncSetAttribute(pv_fps_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kThreads * kPerThread * 16) != cudaSuccess) {
+      if (!prepare_fps<kClusterSmem, kThreadsSmem, 0>(kSmemBytes) ||
+          !prepare_fps<kNarrowCluster, kNarrowThreads, kNarrowPer>(regs_smem(kNarrowThreads * kNarrowPer))) {
         cudaGetLastError();
         st = PV_ERR_CUDA;
       } else {
+        // 16-CTA clusters are optional: without them every cloud takes 8.
+        const size_t wide = regs_smem(kWideThreads * kWidePer);
+        g_wide_clusters[dev] = prepare_fps<kWideCluster, kWideThreads, kWidePer>(wide)
+                                   ? max_clusters<kWideCluster, kWideThreads, kWidePer>(wide)
+                                   : 0;
+        cudaGetLastError();
         g_fps_ready[dev] = true;
       }
     }
@@ -308,16 +443,24 @@ extern "C" int pv_fps(const float* points, int num_clouds, int64_t num_points, i
     fp.out_idx = out_indices;
     fp.out_samples = reinterpret_cast<float4*>(out_samples);
     fp.status = out_status;
-    const long long per = (num_points + kCluster - 1) / kCluster;
     if (cudaMemsetAsync(out_status, 0, sizeof(int32_t), s) != cudaSuccess) {
       st = PV_ERR_CUDA;
     } else {
-      const size_t smem = static_cast<size_t>(per) * 16;
-      if (per <= static_cast<long long>(kThreads) * kPerThread)
-        pv_fps_kernel<true><<<num_clouds * kCluster, kThreads, smem, s>>>(fp);
-      else
-        pv_fps_kernel<false><<<num_clouds * kCluster, kThreads, smem, s>>>(fp);
-      if (cudaGetLastError() != cudaSuccess) st = PV_ERR_CUDA;
+      cudaError_t e;
+      if (num_points <= kRegsPoints && num_clouds <= g_wide_clusters[dev]) {
+        const long long per = (num_points + kWideCluster - 1) / kWideCluster;
+        e = launch_fps<kWideCluster, kWideThreads, kWidePer>(fp, num_clouds, regs_smem(per), s);
+      } else if (num_points <= kRegsPoints) {
+        const long long per = (num_points + kNarrowCluster - 1) / kNarrowCluster;
+        e = launch_fps<kNarrowCluster, kNarrowThreads, kNarrowPer>(fp, num_clouds, regs_smem(per), s);
+      } else {
+        const long long per = (num_points + kClusterSmem - 1) / kClusterSmem;
+        e = launch_fps<kClusterSmem, kThreadsSmem, 0>(fp, num_clouds, static_cast<size_t>(per) * 16, s);
+      }
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        st = PV_ERR_CUDA;
+      }
     }
   }
   if (prev != dev) cudaSetDevice(prev);

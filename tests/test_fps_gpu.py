@@ -2,7 +2,8 @@
 oracle's (the distances are the same float operations in the same order, and
 ties go to the lowest index on both sides).
 
-Covers the page's benchmark size (65,536 points, 4,096 samples), the largest
+Covers the page's benchmark size (65,536 points, 4,096 samples) on uniform
+and on LiDAR-shaped clouds (near-ties that expose any fused arithmetic), the largest
 cloud one launch holds, clouds of a few points (CTAs of the cluster without
 points), exact ties on a lattice, several start points, more samples than
 distinct points, batches of clouds, the sampled-point copies, and
@@ -15,6 +16,7 @@ import numpy as np
 import pytest
 
 import oracle
+from lidar_point_cloud_gb300 import synth
 
 torch = pytest.importorskip("torch")
 pv = pytest.importorskip("lidar_point_cloud_gb300")
@@ -46,6 +48,24 @@ def check(pts, m, start=0):
 
 def test_page_benchmark_size():
     check(cloud(65_536, 1), 4096)
+
+
+@pytest.mark.parametrize("seed", [1, 3])
+def test_lidar_shaped_cloud(seed):
+    # Structured ranges put many points within an ulp of the farthest
+    # distance: a distance rounded once instead of per operation picks a
+    # different sample (seed 1: first at sample 1,408).
+    check(synth.fps_cloud(seed), 4096)
+
+
+@pytest.mark.parametrize("clouds", [2, 19])
+def test_batch_in_16_and_8_cta_clusters(clouds):
+    # Two clouds fit at once in 16-CTA clusters; 19 take 8-CTA clusters.
+    pts = np.stack([synth.fps_cloud(1 + b) for b in range(clouds)])
+    got = pv.fps(torch.from_numpy(pts).to(DEV), 600).cpu().numpy()
+    for b in range(clouds):
+        st, ref = oracle.fps(pts[b], 600, 0)
+        assert st == 0 and np.array_equal(got[b], ref), b
 
 
 def test_largest_cloud():

@@ -5,6 +5,8 @@
   clouds, several sizes, sample counts and start points: identical indices;
 * FPS invariants: the distance of each new sample to the earlier ones never
   grows, and samples are distinct while points remain uncovered;
+* the restatement on the LiDAR-shaped benchmark cloud, whose near-ties
+  expose a distance rounded once instead of per operation;
 * planted mistakes in the oracle are caught.
 """
 
@@ -64,7 +66,23 @@ def pin_restatement(lib, seed=808):
     return fails
 
 
-PINS = (pin_examples, pin_restatement)
+def pin_lidar_cloud(lib, samples=1600):
+    """The restatement on the LiDAR-shaped benchmark cloud: its structured
+    ranges put many points within an ulp of the farthest distance, so a
+    distance rounded once instead of per operation (a fused multiply-add)
+    picks a different sample within the first 1,600 (the first such sample of
+    seed 1 is number 1,408)."""
+    from lidar_point_cloud_gb300 import synth
+
+    pts = synth.fps_cloud(1)
+    st, idx = oracle.fps(pts, samples, 0, lib)
+    ref = oracle.fps_numpy(pts, samples, 0)
+    if st != 0 or not np.array_equal(idx, ref):
+        return [f"lidar cloud: first difference at {int(np.argmax(idx != ref))}"]
+    return []
+
+
+PINS = (pin_examples, pin_restatement, pin_lidar_cloud)
 
 
 def test_examples():
@@ -73,6 +91,10 @@ def test_examples():
 
 def test_restatement():
     assert pin_restatement(oracle.load()) == []
+
+
+def test_lidar_cloud():
+    assert pin_lidar_cloud(oracle.load()) == []
 
 
 def test_invariants():
@@ -102,6 +124,8 @@ MUTANTS = {
     "no_running_minimum": ("if (d < min_dist[i]) min_dist[i] = d;", "min_dist[i] = d;"),
     "start_ignored": ("int64_t sel = start;", "int64_t sel = 0;"),
     "no_z_term": ("const float d = (dx * dx + dy * dy) + dz * dz;", "const float d = dx * dx + dy * dy;"),
+    "fused_distance": ("const float d = (dx * dx + dy * dy) + dz * dz;",
+                       "const float d = std::fma(dx, dx, dy * dy) + dz * dz;"),
 }
 
 
