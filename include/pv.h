@@ -225,10 +225,14 @@ int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cl
 /*
  * pv_voxelize_host - the same operation on HOST buffers, synchronous.
  *
- * Copies points_host to the device, runs pv_voxelize on `stream`, copies all
- * four outputs back (the full padded [max_voxels, ...] buffers) and waits for
- * the stream.  Host buffers may be pageable; pinned buffers copy faster.
- * The device copies live in the library's per-(device, stream) workspace.
+ * Runs pv_voxelize on `stream` for a cloud in host memory, fills all four
+ * host outputs (the full padded [max_voxels, ...] buffers) and waits for the
+ * stream.  Pinned buffers (page-locked and mapped: cudaHostAlloc,
+ * cudaHostRegister) aligned as pv_voxelize requires (16 bytes for points and
+ * voxels, 4 for the rest) are used in place: the kernel reads the points and
+ * writes the outputs across the host link.  Any other host buffer (pageable,
+ * or less aligned) goes through a device copy in the library's per-(device,
+ * stream) workspace, copied in before or out after the kernel.
  * Returns PV_OK, a host-side error, or the negative status the device wrote
  * (then *out_num_voxels_host holds it too).
  */

@@ -232,33 +232,65 @@ def voxelize(points, point_cloud_range, voxel_size, max_points: int = 32, max_vo
         return out[0][:V], out[1][:V], out[2][:V]
 
 
+_vec_cache = {}
+
+
+def _vec(seq, n: int):
+    """ctypes float[n] of a range or voxel size, cached by value (read-only on the C side)."""
+    key = (seq if type(seq) is tuple else tuple(float(x) for x in seq), n)
+    arr = _vec_cache.get(key)
+    if arr is None:
+        arr = _f6(key[0], n)
+        if len(_vec_cache) < 256:
+            _vec_cache[key] = arr
+    return arr
+
+
+def _host_ptr(a) -> int:
+    """Address of a contiguous host array: a NumPy array or a CPU torch tensor."""
+    if hasattr(a, "data_ptr"):
+        if a.is_cuda or not a.is_contiguous():
+            raise ValueError("host buffers must be contiguous CPU tensors or NumPy arrays")
+        return a.data_ptr()
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("output arrays must be C-contiguous")
+    return a.ctypes.data
+
+
 def voxelize_host(points, point_cloud_range, voxel_size, max_points: int = 32, max_voxels: int = 16000,
                   out=None, stream=None):
-    """Voxelize a host (NumPy or CPU torch) cloud through pv_voxelize_host.
+    """Voxelize a host cloud (NumPy or CPU torch, [N, 4] float32) through pv_voxelize_host.
 
-    Copies in, runs on the current CUDA device, copies the padded outputs
-    back into ``out`` (NumPy arrays; allocated if None) and returns
-    (voxels [M,K,4], coords [M,3], counts [M], V).
+    Runs on the current CUDA device and fills ``out`` (NumPy arrays or CPU
+    torch tensors; NumPy arrays are allocated if None) with the padded
+    outputs; returns (voxels [M,K,4], coords [M,3], counts [M], V).  Pinned
+    buffers (for example ``torch.empty(..).pin_memory()``) are read and
+    written in place by the kernel; other host memory is staged on the
+    device.
     """
     import numpy as np
 
-    pts = np.ascontiguousarray(np.asarray(points, dtype=np.float32)).reshape(-1, 4)
+    if hasattr(points, "data_ptr"):
+        if points.dtype.itemsize != 4 or not points.is_floating_point() or points.is_cuda:
+            raise TypeError("points must be a float32 CPU tensor")
+        n = int(points.numel()) // 4
+        pts_ptr = _host_ptr(points) if n else 0
+    else:
+        pts = np.ascontiguousarray(np.asarray(points, dtype=np.float32)).reshape(-1, 4)
+        n = int(pts.shape[0])
+        pts_ptr = pts.ctypes.data if n else 0
     if out is None:
         out = (np.empty((max_voxels, max_points, 4), np.float32), np.empty((max_voxels, 3), np.int32),
                np.empty((max_voxels,), np.int32), np.empty((1,), np.int32))
     vox, coords, counts, num = out
-    for a in out:
-        if not a.flags["C_CONTIGUOUS"]:
-            raise ValueError("output arrays must be C-contiguous")
-    handle = ctypes.c_void_p(0 if stream is None else (stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)))
-    st = load().pv_voxelize_host(
-        ctypes.c_void_p(pts.ctypes.data if pts.shape[0] else 0), int(pts.shape[0]),
-        _f6(point_cloud_range, 6), _f6(voxel_size, 3), int(max_points), int(max_voxels),
-        ctypes.c_void_p(vox.ctypes.data), ctypes.c_void_p(coords.ctypes.data),
-        ctypes.c_void_p(counts.ctypes.data), ctypes.c_void_p(num.ctypes.data), handle)
+    handle = 0 if stream is None else (stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    num_ptr = _host_ptr(num)
+    st = load().pv_voxelize_host(pts_ptr, n, _vec(point_cloud_range, 6), _vec(voxel_size, 3), int(max_points),
+                                 int(max_voxels), _host_ptr(vox), _host_ptr(coords), _host_ptr(counts), num_ptr,
+                                 handle)
     if st != 0:
         raise PVError(st, "pv_voxelize_host")
-    return vox, coords, counts, int(num[0])
+    return vox, coords, counts, ctypes.c_int32.from_address(num_ptr).value
 
 
 def alloc_batch_outputs(num_frames: int, max_points: int, max_voxels: int, device):

@@ -1961,6 +1961,19 @@ int get_workspace(int dev, pv_stream_t stream, Workspace** out) {
 
 size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
 
+// The device address of a pinned host buffer (page-locked and mapped into
+// the device's address space: cudaHostAlloc, cudaHostRegister) when it is
+// aligned to `align` bytes, or null for any other pointer.
+void* mapped_host(const void* ptr, size_t align) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+  return reinterpret_cast<uintptr_t>(a.devicePointer) % align == 0 ? a.devicePointer : nullptr;
+}
+
 // Makes every region big enough for `pl` (caller holds ws->mu).
 int reserve(Workspace* ws, const Plan& pl, int64_t N, pv_stream_t stream) {
   bool synced = false;
@@ -2359,38 +2372,55 @@ int pv_voxelize_host(const float* points_host, int64_t num_points, const float p
   if ((st = get_workspace(dev, stream, &ws)) != PV_OK) return st;
   std::lock_guard<std::mutex> lk(ws->mu);
   if ((st = reserve(ws, pl, num_points, stream)) != PV_OK) return st;
-  // Staging layout: points | voxels | coords | counts | num, each 256-byte aligned.
-  const size_t b_pts = round_up(16 * static_cast<size_t>(num_points), 256);
-  const size_t b_vox = round_up(16 * static_cast<size_t>(max_voxels) * max_points, 256);
-  const size_t b_crd = round_up(12 * static_cast<size_t>(max_voxels), 256);
-  const size_t b_cnt = round_up(4 * static_cast<size_t>(max_voxels), 256);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Pinned buffers (page-locked and mapped) are used in place: the kernel
+  // reads the points and writes the outputs across the host link itself, so
+  // each byte crosses it once, as with copies, without a copy's set-up or
+  // its wait for the kernel.  Other host memory goes through device staging.
+  const float* in_pts = static_cast<const float*>(num_points > 0 ? mapped_host(points_host, 16) : nullptr);
+  float* mv = static_cast<float*>(mapped_host(out_voxels_host, 16));
+  int32_t* mc = static_cast<int32_t*>(mapped_host(out_coords_host, 4));
+  int32_t* mn = static_cast<int32_t*>(mapped_host(out_counts_host, 4));
+  int32_t* mu = static_cast<int32_t*>(mapped_host(out_num_voxels_host, 4));
+  const bool in_place = mv && mc && mn && mu;
+  // Staging layout: points | voxels | coords | counts | num, each 256-byte aligned (only what is needed).
+  const size_t b_pts = in_pts ? 0 : round_up(16 * static_cast<size_t>(num_points), 256);
+  const size_t b_vox = in_place ? 0 : round_up(16 * static_cast<size_t>(max_voxels) * max_points, 256);
+  const size_t b_crd = in_place ? 0 : round_up(12 * static_cast<size_t>(max_voxels), 256);
+  const size_t b_cnt = in_place ? 0 : round_up(4 * static_cast<size_t>(max_voxels), 256);
   const size_t need = b_pts + b_vox + b_crd + b_cnt + 256;
   bool synced = false;
-  if ((st = grow(&ws->staging, &ws->staging_cap, need, 0, stream, &synced)) !=
-      PV_OK)
-    return st;
+  if ((st = grow(&ws->staging, &ws->staging_cap, need, 0, stream, &synced)) != PV_OK) return st;
   unsigned char* base = ws->staging;
-  float* d_pts = reinterpret_cast<float*>(base);
-  float* d_vox = reinterpret_cast<float*>(base + b_pts);
-  int32_t* d_crd = reinterpret_cast<int32_t*>(base + b_pts + b_vox);
-  int32_t* d_cnt = reinterpret_cast<int32_t*>(base + b_pts + b_vox + b_crd);
-  int32_t* d_num = reinterpret_cast<int32_t*>(base + b_pts + b_vox + b_crd + b_cnt);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (num_points > 0 &&
-      cudaMemcpyAsync(d_pts, points_host, 16 * static_cast<size_t>(num_points), cudaMemcpyHostToDevice, s) !=
-          cudaSuccess)
-    return PV_ERR_CUDA;
-  if ((st = launch(ws, pl, d_pts, num_points, point_cloud_range, voxel_size, max_points, max_voxels, d_vox, d_crd,
-                   d_cnt, d_num, stream)) != PV_OK)
-    return st;
-  if (cudaMemcpyAsync(out_voxels_host, d_vox, 16 * static_cast<size_t>(max_voxels) * max_points,
-                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(out_coords_host, d_crd, 12 * static_cast<size_t>(max_voxels), cudaMemcpyDeviceToHost, s) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(out_counts_host, d_cnt, 4 * static_cast<size_t>(max_voxels), cudaMemcpyDeviceToHost, s) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(out_num_voxels_host, d_num, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return PV_ERR_CUDA;
+  if (!in_pts) {
+    float* d_pts = reinterpret_cast<float*>(base);
+    if (num_points > 0 &&
+        cudaMemcpyAsync(d_pts, points_host, 16 * static_cast<size_t>(num_points), cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+      return PV_ERR_CUDA;
+    in_pts = d_pts;
+  }
+  if (in_place) {
+    if ((st = launch(ws, pl, in_pts, num_points, point_cloud_range, voxel_size, max_points, max_voxels, mv, mc, mn,
+                     mu, stream)) != PV_OK)
+      return st;
+  } else {
+    float* d_vox = reinterpret_cast<float*>(base + b_pts);
+    int32_t* d_crd = reinterpret_cast<int32_t*>(base + b_pts + b_vox);
+    int32_t* d_cnt = reinterpret_cast<int32_t*>(base + b_pts + b_vox + b_crd);
+    int32_t* d_num = reinterpret_cast<int32_t*>(base + b_pts + b_vox + b_crd + b_cnt);
+    if ((st = launch(ws, pl, in_pts, num_points, point_cloud_range, voxel_size, max_points, max_voxels, d_vox,
+                     d_crd, d_cnt, d_num, stream)) != PV_OK)
+      return st;
+    if (cudaMemcpyAsync(out_voxels_host, d_vox, 16 * static_cast<size_t>(max_voxels) * max_points,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(out_coords_host, d_crd, 12 * static_cast<size_t>(max_voxels), cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess ||
+        cudaMemcpyAsync(out_counts_host, d_cnt, 4 * static_cast<size_t>(max_voxels), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(out_num_voxels_host, d_num, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return PV_ERR_CUDA;
+  }
   if (cudaStreamSynchronize(s) != cudaSuccess) return PV_ERR_CUDA;
   return *out_num_voxels_host < 0 ? *out_num_voxels_host : PV_OK;
 }

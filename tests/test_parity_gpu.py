@@ -226,6 +226,40 @@ def test_host_entry_point():
     assert V == oV and same_bits(vox, ov) and same_bits(coords, oc) and same_bits(counts, on)
 
 
+@pytest.mark.parametrize("name", ["kitti", "dense"])
+def test_host_entry_point_pinned_buffers_in_place(name):
+    # Pinned input and outputs: the kernel reads and writes them across the
+    # host link; pinned input with pageable outputs, and the reverse, mix
+    # in-place use with staging copies.
+    pts, P = synth.make(name)
+    K, M = P.max_points, P.max_voxels
+    st, ov, oc, on, oV = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, K, M)
+    pin_pts = torch.from_numpy(pts).pin_memory().numpy()
+    shapes = (((M, K, 4), torch.float32), ((M, 3), torch.int32), ((M,), torch.int32), ((1,), torch.int32))
+    pinned = tuple(torch.full(sh, 7, dtype=dt).pin_memory().numpy() for sh, dt in shapes)
+    pageable = tuple(np.full(sh, 7, dtype=np.float32 if dt == torch.float32 else np.int32) for sh, dt in shapes)
+    tensors = tuple(torch.from_numpy(a) for a in pinned)  # CPU tensors (pinned) as the buffers
+    for src, out in ((pin_pts, pinned), (pin_pts, pageable), (pts, pinned), (torch.from_numpy(pin_pts), tensors)):
+        for a in out:
+            a.fill(7) if isinstance(a, np.ndarray) else a.fill_(7)
+        vox, coords, counts, V = pv.voxelize_host(src, P.point_cloud_range, P.voxel_size, K, M, out=out)
+        vox, coords, counts = (np.asarray(a) for a in (vox, coords, counts))
+        assert V == oV and same_bits(vox, ov) and same_bits(coords, oc) and same_bits(counts, on)
+
+
+def test_host_entry_point_misaligned_pinned_input():
+    # A pinned cloud that starts 4 bytes into its allocation cannot be read in
+    # place (16-byte loads): it goes through the staging copy.
+    pts, P = synth.make("tiny")
+    buf = torch.zeros(pts.size + 1, dtype=torch.float32).pin_memory().numpy()
+    view = buf[1:].reshape(-1, 4)
+    view[:] = pts
+    assert view.ctypes.data % 16 != 0
+    vox, coords, counts, V = pv.voxelize_host(view, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    st, ov, oc, on, oV = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    assert V == oV and same_bits(vox, ov) and same_bits(coords, oc) and same_bits(counts, on)
+
+
 def test_sliced_python_entry_point():
     pts, P = synth.make("tiny")
     vox, coords, counts = pv.voxelize(torch.from_numpy(pts).to(DEV), P.point_cloud_range, P.voxel_size)
