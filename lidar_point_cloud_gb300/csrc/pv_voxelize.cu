@@ -1500,8 +1500,42 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel
 // points in index order; counts, barrier, scan.  Phase D3: rank r reads its
 // voxel's accumulator, writes the centroid (double quotient rounded to
 // float), coordinates and count, and empties the accumulator.
-constexpr int kDsHash = 2 * kThreads;  // tile map positions
-constexpr int kDsSmem = kDsHash * (4 + 32 + 4 + 4);
+// (*ah, *al) += (bh, bl) in float-float: the high parts' exact two-sum, the
+// low parts folded into its error, and an exact two-sum to renormalise.  The
+// result is within a few units of 2^-46 of the operands' magnitudes.
+__device__ __forceinline__ void two_sum(float a, float b, float* s, float* e) {
+  *s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(*s, a);
+  *e = __fadd_rn(__fsub_rn(a, __fsub_rn(*s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void ff_add(float* ah, float* al, float bh, float bl) {
+  float s, e;
+  two_sum(*ah, bh, &s, &e);
+  e = __fadd_rn(e, __fadd_rn(*al, bl));
+  two_sum(s, e, ah, al);
+}
+
+// A double sum divided by a count, rounded to float, within one float ulp
+// of float(s / n) and without a double division (slow on GB300): s split
+// into two floats, the quotient of the high part by n from a correctly
+// rounded 1/n, then one correction with the exact remainder and the low
+// part.  Counts from 2^24 (not exact as floats) take the double division.
+__device__ __forceinline__ float mean_of(double s, unsigned int count) {
+  if (count >= (1u << 24)) return static_cast<float>(s / static_cast<double>(count));
+  const float sh = __double2float_rn(s);
+  const float sl = __double2float_rn(s - static_cast<double>(sh));
+  const float nf = static_cast<float>(count);
+  const float rcp = __frcp_rn(nf);
+  const float q = __fmul_rn(sh, rcp);
+  const float rem = __fmaf_rn(-q, nf, sh);  // sh - q * n, rounded once
+  return __fmaf_rn(__fadd_rn(rem, sl), rcp, q);
+}
+
+constexpr int kDsHash = 2 * kThreads;  // count map positions (a tile's warp groups)
+constexpr int kDsHot = 256;            // hot table positions (at most half used)
+constexpr unsigned int kDsHotGroups = 4;  // warp groups of one voxel in the first tile that make it hot
+constexpr int kDsSmem = kDsHash * (4 + 4) + kDsHot * (4 + 16 + 16 + 4 + 4);
 
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kernel(const KParams p) {
   extern __shared__ __align__(16) unsigned char s_dyn[];
@@ -1509,10 +1543,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
   __shared__ unsigned int s_tile[kFlagUnroll][kWarps];
   __shared__ unsigned int s_tmp[kWarps + 1];
   __shared__ int s_flag;
-  double* m_sum = reinterpret_cast<double*>(s_dyn);                        // [4][kDsHash]
-  int* m_key = reinterpret_cast<int*>(s_dyn + 32 * kDsHash);               // [kDsHash], -1 = free
-  unsigned int* m_cnt = reinterpret_cast<unsigned int*>(m_key + kDsHash);  // [kDsHash]
-  unsigned int* m_first = m_cnt + kDsHash;                                 // [kDsHash]
+  __shared__ int s_hot;  // the hot table holds a voxel
 
   const unsigned int P = gridDim.x;
   const unsigned int cta = blockIdx.x;
@@ -1538,14 +1569,42 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
   }
 
   if (alive) {
-    for (int h = static_cast<int>(tid); h < kDsHash; h += kThreads) {
-      m_key[h] = -1;
-      m_cnt[h] = 0u;
-      m_first[h] = 0xFFFFFFFFu;
-      for (int c = 0; c < 4; ++c) m_sum[c * kDsHash + h] = 0.0;
+    // ---- phase D1, every tile: bin and find the slot; each warp sums its
+    // points of one voxel by pointer jumping along the group (at most five
+    // shuffle rounds; none for lone points) in float-float (exact two-sums in
+    // fp32: GB300's fp64 rate is a small fraction of its fp32 rate), and the
+    // group's leader adds the sums' high and low parts to the voxel's double
+    // accumulator with global reductions, with the count and the first index.
+    //
+    // Hot voxels (one voxel in many warps of a tile) would pile those
+    // reductions onto one address.  A block with several tiles learns them
+    // from its first tile (warp groups registered per voxel in a shared
+    // count map) and sums them for the rest of its chunk in a shared table
+    // instead: fp32 atomics whose exact rounding error (a two-sum with the
+    // returned old value) goes into a second fp32 accumulator, flushed once
+    // at the end.
+    int* c_key = reinterpret_cast<int*>(s_dyn);                                 // [kDsHash] count map
+    unsigned int* c_n = reinterpret_cast<unsigned int*>(c_key + kDsHash);       // [kDsHash]
+    int* h_key = reinterpret_cast<int*>(c_n + kDsHash);                         // [kDsHot] hot table
+    float* h_hi = reinterpret_cast<float*>(h_key + kDsHot);                     // [4][kDsHot]
+    float* h_lo = h_hi + 4 * kDsHot;                                            // [4][kDsHot]
+    unsigned int* h_n = reinterpret_cast<unsigned int*>(h_lo + 4 * kDsHot);     // [kDsHot]
+    unsigned int* h_first = h_n + kDsHot;                                       // [kDsHot]
+    const bool learn = end - begin > kThreads;  // several tiles: learn from the first
+    if (learn) {
+      for (int h = static_cast<int>(tid); h < kDsHash; h += kThreads) {
+        c_key[h] = -1;
+        c_n[h] = 0u;
+      }
+      for (int h = static_cast<int>(tid); h < kDsHot; h += kThreads) {
+        h_key[h] = -1;
+        for (int c = 0; c < 4; ++c) h_hi[c * kDsHot + h] = h_lo[c * kDsHot + h] = 0.f;
+        h_n[h] = 0u;
+        h_first[h] = 0xFFFFFFFFu;
+      }
+      if (tid == 0) s_hot = 0;
+      __syncthreads();
     }
-    __syncthreads();
-    // ---- phase D1
     for (long long tb = begin; tb < end; tb += kThreads) {
       const long long i = tb + tid;
       const float4 q = i < end ? __ldg(p.points + i) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1559,57 +1618,100 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
       }
       const unsigned int peers = __match_any_sync(0xffffffffu, slot);
       const int leader = __ffs(peers) - 1;
-      // Suffix sums along the group by pointer jumping: nxt is the next member above this lane.
-      double v0 = q.x, v1 = q.y, v2 = q.z, v3 = q.w;
-      int nxt = __ffs(peers & ~((2u << lane) - 1u)) - 1;  // -1: last member (2 << 31 wraps to 0: no member above)
-      if (lane == 31u) nxt = -1;
+      float hi[4] = {q.x, q.y, q.z, q.w}, lo[4] = {0.f, 0.f, 0.f, 0.f};
+      int nxt = __ffs(peers & ~((2u << lane) - 1u)) - 1;  // the next member above this lane, or -1
+      if (lane == 31u) nxt = -1;                           // (2 << 31 wraps to 0: no member above)
       while (__any_sync(0xffffffffu, nxt >= 0)) {
         const int src = nxt >= 0 ? nxt : static_cast<int>(lane);
-        const double o0 = __shfl_sync(0xffffffffu, v0, src);
-        const double o1 = __shfl_sync(0xffffffffu, v1, src);
-        const double o2 = __shfl_sync(0xffffffffu, v2, src);
-        const double o3 = __shfl_sync(0xffffffffu, v3, src);
+        float oh[4], ol[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          oh[c] = __shfl_sync(0xffffffffu, hi[c], src);
+          ol[c] = __shfl_sync(0xffffffffu, lo[c], src);
+        }
         const int onext = __shfl_sync(0xffffffffu, nxt, src);
         if (nxt >= 0) {
-          v0 += o0;
-          v1 += o1;
-          v2 += o2;
-          v3 += o3;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) ff_add(&hi[c], &lo[c], oh[c], ol[c]);
           nxt = onext;
         }
       }
       const bool lead = slot >= 0 && static_cast<int>(lane) == leader;
       if (i < end) p.slot_of_point[i] = slot < 0 ? -1 : (lead ? (slot | kLeaderBit) : slot);
-      if (lead) {
-        unsigned int h = mix32(static_cast<unsigned int>(slot)) & (kDsHash - 1);
-        for (int probe = 0; probe < kDsHash; ++probe) {  // at most kThreads keys: never full
-          const int cur = atomicCAS(m_key + h, -1, slot);
-          if (cur == -1 || cur == slot) break;
-          h = (h + 1) & (kDsHash - 1);
+      const bool first_tile = tb == begin;
+      int hp = -1;  // hot table position of this group's voxel
+      if (lead && learn && !first_tile && s_hot) {
+        unsigned int h = mix32(static_cast<unsigned int>(slot)) & (kDsHot - 1);
+        for (int probe = 0; probe < kDsHot; ++probe) {  // the table is fixed: read-only probes
+          const int cur = h_key[h];
+          if (cur == slot) {
+            hp = static_cast<int>(h);
+            break;
+          }
+          if (cur == -1) break;
+          h = (h + 1) & (kDsHot - 1);
         }
-        atomicAdd(m_sum + h, v0);
-        atomicAdd(m_sum + kDsHash + h, v1);
-        atomicAdd(m_sum + 2 * kDsHash + h, v2);
-        atomicAdd(m_sum + 3 * kDsHash + h, v3);
-        atomicAdd(m_cnt + h, static_cast<unsigned int>(__popc(peers)));
-        atomicMin(m_first + h, static_cast<unsigned int>(i));
       }
-      __syncthreads();  // the tile's voxels are in the map
-      for (int h = static_cast<int>(tid); h < kDsHash; h += kThreads) {
-        const int key = m_key[h];
-        if (key < 0) continue;
+      if (hp >= 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float old = atomicAdd(h_hi + c * kDsHot + hp, hi[c]);
+          float sum, err;
+          two_sum(old, hi[c], &sum, &err);  // sum is what the atomic stored; err its exact rounding error
+          atomicAdd(h_lo + c * kDsHot + hp, __fadd_rn(err, lo[c]));
+        }
+        atomicAdd(h_n + hp, static_cast<unsigned int>(__popc(peers)));
+        atomicMin(h_first + hp, static_cast<unsigned int>(i));
+      } else if (lead) {
+        VoxAcc* A = p.acc + slot;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          atomicAdd(&A->s[c], static_cast<double>(hi[c]));
+          if (lo[c] != 0.f) atomicAdd(&A->s[c], static_cast<double>(lo[c]));
+        }
+        atomicAdd(&A->count, static_cast<unsigned int>(__popc(peers)));
+        atomicMax(&A->first_c, ~static_cast<unsigned int>(i));  // the leader holds the group's lowest index
+      }
+      if (learn && first_tile) {  // register the tile's warp groups, then keep the voxels with many
+        if (lead) {
+          unsigned int h = mix32(static_cast<unsigned int>(slot)) & (kDsHash - 1);
+          for (int probe = 0; probe < kDsHash; ++probe) {  // at most kThreads keys: never full
+            const int cur = atomicCAS(c_key + h, -1, slot);
+            if (cur == -1 || cur == slot) break;
+            h = (h + 1) & (kDsHash - 1);
+          }
+          atomicAdd(c_n + h, 1u);
+        }
+        __syncthreads();
+        for (int h = static_cast<int>(tid); h < kDsHash; h += kThreads) {
+          if (c_key[h] < 0 || c_n[h] < kDsHotGroups) continue;
+          const int key = c_key[h];
+          unsigned int t = mix32(static_cast<unsigned int>(key)) & (kDsHot - 1);
+          for (int probe = 0; probe < kDsHot / 2; ++probe) {  // at most half full: later ones stay direct
+            const int cur = atomicCAS(h_key + t, -1, key);
+            if (cur == -1) {
+              s_hot = 1;
+              break;
+            }
+            t = (t + 1) & (kDsHot - 1);
+          }
+        }
+        __syncthreads();  // the hot table is fixed from here on
+      }
+    }
+    if (learn) {  // flush the hot table
+      __syncthreads();
+      for (int h = static_cast<int>(tid); h < kDsHot; h += kThreads) {
+        const int key = h_key[h];
+        if (key < 0 || h_n[h] == 0u) continue;
         VoxAcc* A = p.acc + key;
         for (int c = 0; c < 4; ++c) {
-          atomicAdd(&A->s[c], m_sum[c * kDsHash + h]);
-          m_sum[c * kDsHash + h] = 0.0;
+          atomicAdd(&A->s[c], static_cast<double>(h_hi[c * kDsHot + h]));
+          atomicAdd(&A->s[c], static_cast<double>(h_lo[c * kDsHot + h]));
         }
-        atomicAdd(&A->count, m_cnt[h]);
-        atomicMax(&A->first_c, ~m_first[h]);
-        m_key[h] = -1;
-        m_cnt[h] = 0u;
-        m_first[h] = 0xFFFFFFFFu;
+        atomicAdd(&A->count, h_n[h]);
+        atomicMax(&A->first_c, ~h_first[h]);
       }
-      __syncthreads();  // the map is empty again
     }
     alive = grid_sync(p.ctl, bar_target + p.bar_extra, &s_flag);
   }
@@ -1675,10 +1777,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
     if (tid == 0) s_prefix[P] = total;
     __syncthreads();
     V = total < M ? total : M;
-    // ---- phase D3: one voxel per thread, ranks in order across the grid;
-    // voxels past the budget only have their accumulators emptied.
+    // ---- phase D3: one voxel per thread; voxels past the budget only have
+    // their accumulators emptied.  Runs of 32 ranks go to the warps of all
+    // blocks in turn (block-major order would leave the first blocks alone
+    // with every kept voxel's double divisions, which GB300 runs slowly).
     const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-    for (size_t r = gtid; r < total; r += gthreads) {
+    const size_t r0 = (static_cast<size_t>(warp) * P + cta) * 32 + lane;
+    for (size_t r = r0; r < total; r += gthreads) {
       const int slot = slot_of_rank(p, s_prefix, P, static_cast<unsigned int>(r));
       uint4* a4 = reinterpret_cast<uint4*>(p.acc + slot);
       if (r < V) {
@@ -1686,9 +1791,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
         reinterpret_cast<uint4*>(&A)[0] = __ldcg(a4);
         reinterpret_cast<uint4*>(&A)[1] = __ldcg(a4 + 1);
         reinterpret_cast<uint4*>(&A)[2] = __ldcg(a4 + 2);
-        const double n = static_cast<double>(A.count);
-        p.out_voxels[r] = make_float4(static_cast<float>(A.s[0] / n), static_cast<float>(A.s[1] / n),
-                                      static_cast<float>(A.s[2] / n), static_cast<float>(A.s[3] / n));
+        p.out_voxels[r] = make_float4(mean_of(A.s[0], A.count), mean_of(A.s[1], A.count),
+                                      mean_of(A.s[2], A.count), mean_of(A.s[3], A.count));
         const int key = p.hash_mode ? __ldcg(p.keys + slot) : slot;
         const int kxy = key / p.g_x;
         p.out_coords[3 * r] = kxy / p.g_y;
