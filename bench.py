@@ -498,6 +498,12 @@ def run_gb300(args, rank, world, local_rank):
         return
     value = whole_job_rate(n, args.steps, world, region_ms)
     avg_kernel_s = statistics.mean(kernel_ms) * 1e-3
+    # Data-only bytes: the input once and the rows actually filled (V of them),
+    # beside the padded contract's every output byte.
+    if ds:
+        data_bytes = 16 * n + V * 32 + 4
+    else:
+        data_bytes = 16 * n + V * (16 * K + 16) + 4 * Bf
     peak, peak_src = measured_peak()
     achieved = bytes_launch / avg_kernel_s / 1e9
 
@@ -586,6 +592,9 @@ def run_gb300(args, rank, world, local_rank):
             "traffic": profiled_traffic(args.workload + (f"_x{Bf}" if Bf > 1 else ""), kernel),
             "peak_source": f"{peak_src} (hbm_gbs)", "kernel": kernel,
             "bytes_per_launch": bytes_launch, "avg_launch_us": round(avg_kernel_s * 1e6, 3),
+            "median_launch_us": None if use_graph else round(statistics.median(kernel_ms) * 1e3, 3),
+            "data_bytes_per_launch": data_bytes,
+            "frac_data": round(data_bytes / avg_kernel_s / 1e9 / peak, 4),
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
