@@ -382,17 +382,33 @@ __device__ __forceinline__ unsigned int mix32(unsigned int h) {
 
 // Find or claim the hashed slot of `key`.  At most table-size probes; -1 if
 // the table is full.
+#ifdef PV_INSTRUMENT
+__device__ unsigned long long g_probe_hist[34];  // lookups by positions probed: 1 .. 32, more, table full
+#define PV_PROBES(n) atomicAdd(&g_probe_hist[(n) < 33u ? (n) : 33u], 1ull)
+#else
+#define PV_PROBES(n) \
+  do {               \
+  } while (0)
+#endif
+
 __device__ __forceinline__ int claim_slot(int32_t* keys, unsigned int mask, int key) {
   unsigned int h = mix32(static_cast<unsigned int>(key)) & mask;
   for (unsigned int probe = 0; probe <= mask; ++probe) {
     const int cur = __ldcg(keys + h);
-    if (cur == key) return static_cast<int>(h);
+    if (cur == key) {
+      PV_PROBES(probe < 32u ? probe + 1u : 32u);
+      return static_cast<int>(h);
+    }
     if (cur == kNoKey) {
       const int old = atomicCAS(keys + h, kNoKey, key);
-      if (old == kNoKey || old == key) return static_cast<int>(h);
+      if (old == kNoKey || old == key) {
+        PV_PROBES(probe < 32u ? probe + 1u : 32u);
+        return static_cast<int>(h);
+      }
     }
     h = (h + 1) & mask;
   }
+  PV_PROBES(33u);
   return -1;
 }
 
@@ -2633,6 +2649,15 @@ int pv_debug_ins_times(unsigned long long* out, int max_ctas) {
 }
 
 // Instrumented builds only: copies [max_ctas][8] phase stamps (ns) to host.
+// Instrumented builds only: lookups in the hashed table by positions probed
+// (index 0 unused, 1 .. 32, 32 = 32 or more, 33 = table full); reset after the read.
+int pv_debug_probe_hist(unsigned long long* out) {
+  if (cudaMemcpyFromSymbol(out, g_probe_hist, sizeof(g_probe_hist)) != cudaSuccess) return PV_ERR_CUDA;
+  const unsigned long long zero[34] = {};
+  if (cudaMemcpyToSymbol(g_probe_hist, zero, sizeof(zero)) != cudaSuccess) return PV_ERR_CUDA;
+  return PV_OK;
+}
+
 int pv_debug_phase_times(unsigned long long* out, int max_ctas) {
   const int n = max_ctas < kStampCtas ? max_ctas : kStampCtas;
   if (cudaMemcpyFromSymbol(out, g_phase_ns, sizeof(unsigned long long) * kStamps * n) != cudaSuccess)
