@@ -928,11 +928,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         if (tid == 0) *prev.layout = 0;
         tile_clear(prev, tid);
       }
+      // The group's counts before this warp and in all: read by the leader,
+      // shared with the group (one warp) by shuffles.
       unsigned int trank = 0, tot = 0;
-      if (slot >= 0) {
-        tile_counts(tm, h, warp, &trank, &tot);
-        trank += __popc(peers & lanemask_lt());
-      }
+      if (slot >= 0 && static_cast<int>(lane) == leader) tile_counts(tm, h, warp, &trank, &tot);
+      trank = __shfl_sync(0xffffffffu, trank, leader);
+      tot = __shfl_sync(0xffffffffu, tot, leader);
+      if (slot >= 0) trank += __popc(peers & lanemask_lt());
       const bool lead = slot >= 0 && trank == 0;
       const unsigned int cseen = (lead && multi) ? chunk_rank(ckey, ccnt, slot, tot) : 0u;
       const int crank = static_cast<int>(cseen >> 16);
