@@ -58,6 +58,27 @@ def test_downsample_workloads(name):
     assert V > 0 and exact > 0.99
 
 
+@pytest.mark.parametrize("hot", [64, 200])
+def test_downsample_hot_voxels(hot):
+    # Blocks with several tiles (here 14) learn hot voxels, those in 4 or more
+    # warp groups of their first tile, into a shared table of 256 positions:
+    # 64 voxels (16 points each a tile) all qualify; 200 (about 5 each) fill
+    # the table to a high load.  2 M points in random order over `hot`
+    # voxels of a pillar grid.
+    rng = np.random.Generator(np.random.PCG64(1000 + hot))
+    n = 2 * 1024 * 1024
+    r, v = (-20.0, -20.0, -3.0, 20.0, 20.0, 1.0), (0.5, 0.5, 4.0)
+    cells = rng.choice(80 * 80, size=hot, replace=False)
+    c = cells[rng.integers(0, hot, size=n)]
+    pts = np.empty((n, 4), np.float32)
+    pts[:, 0] = (r[0] + ((c % 80) + 0.05 + 0.9 * rng.random(n)) * v[0]).astype(np.float32)
+    pts[:, 1] = (r[1] + ((c // 80) + 0.05 + 0.9 * rng.random(n)) * v[1]).astype(np.float32)
+    pts[:, 2] = (r[2] + 4.0 * rng.random(n)).astype(np.float32)
+    pts[:, 3] = rng.random(n).astype(np.float32)
+    V, exact = check(pts, r, v, 1000)
+    assert V == hot and exact > 0.99
+
+
 @pytest.mark.parametrize("M", [1, 100, 5000])
 def test_downsample_budget(M):
     pts, P = synth.make("kitti3d")
