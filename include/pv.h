@@ -176,10 +176,14 @@ int pv_voxelize_batch(const float* points, const int64_t* frame_offsets, int num
  * binning rule above on all three axes (any grid_z); voxels are in the
  * canonical order (first point), the first max_voxels kept.  Every point of a
  * kept voxel counts (no per-voxel cap).  A centroid is (mean x, mean y,
- * mean z, mean intensity): double-precision sums divided by the count in
- * double, rounded to float.  The sums are accumulated in parallel, so a mean
- * may differ from the sequential index-order sum by one float32 unit in the
- * last place; counts, coordinates, V and the order are exact.
+ * mean z, mean intensity): the defining computation is a double sum in index
+ * order divided by the count in double and rounded to float.  The library
+ * accumulates in parallel with at least that precision (float-float sums of
+ * each warp's points, then double sums) and divides in float-float, so a mean
+ * may differ from the definition by one float32 unit in the last place (for
+ * the points of a voxel of one sign, as LiDAR cells are unless they straddle
+ * a coordinate plane through the origin); counts, coordinates, V and the
+ * order are exact.
  *   out_centroids   device, [max_voxels, 4] float32, 16-byte aligned.
  *   out_coords      device, [max_voxels, 3] int32, (z, y, x).
  *   out_counts      device, [max_voxels] int32, points per voxel.
