@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kT, 1) pv_fps_kernel(const FpsParams p) {
       pd[t] = j < cnt ? inf : -inf;  // -inf: no point, never the farthest
     }
   }
-  // Lane c < kC pushes this warp's entry into CTA c.
+  // Lane c < kC of warp 0 stores this CTA's entry into its slot (rank) in CTA c.
   const unsigned int slot = rank;
   const unsigned int tgt = lane < static_cast<unsigned int>(kC) ? lane : 0u;
   const unsigned int rk0 = peer_addr(smem_addr(&s_k[0][slot]), tgt), rk1 = peer_addr(smem_addr(&s_k[1][slot]), tgt);
