@@ -208,6 +208,9 @@ def run_reference(args, rank, world):
     if args.op == "fps":
         B = max(1, args.batch)
         clouds = [synth.fps_cloud(1 + b) for b in range(B)]
+        for _ in range(args.warmup):  # untimed, as on the GPU arm
+            for c in clouds:
+                oracle.fps(c, synth.FPS_SAMPLES, 0, lib)
         t0 = time.perf_counter()
         for _ in range(args.steps):
             for c in clouds:
@@ -215,7 +218,8 @@ def run_reference(args, rank, world):
         el = time.perf_counter() - t0
         value = synth.FPS_POINTS * B * args.steps / el / 1e6
         line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "Mpoints/s",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": 0, "ms_per_step": round(1e3 * el / args.steps, 4),
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(1e3 * el / args.steps, 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": {"workload": f"lidar65k: {synth.WORKLOADS['lidar65k']}", "op": "fps", "clouds_per_launch": B},
                 "cpu_baseline": {"value": round(value, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
