@@ -214,10 +214,11 @@ int pv_voxel_downsample(const float* points, int64_t num_points, const float poi
  *   out_status    device, one int32: 0, or a negative status found on the device.
  * Returns PV_OK or a negative status found on the host (nothing enqueued).
  * Each cloud runs in one thread-block cluster holding it on chip (16 CTAs
- * while the launch's clouds fit on the GPU at once in such clusters, else 8);
- * clouds run side by side.
+ * while the launch's clouds fit on the GPU at once in such clusters, else 8;
+ * clouds of more than 106,496 points always take 16, and on a device
+ * without 16-CTA clusters return PV_ERR_UNSUPPORTED); clouds run side by side.
  */
-#define PV_FPS_MAX_POINTS 106496
+#define PV_FPS_MAX_POINTS 212992
 int pv_fps(const float* points, int num_clouds, int64_t num_points, int64_t num_samples, int64_t start,
            int32_t* out_indices, float* out_samples, int32_t* out_status, pv_stream_t stream);
 

@@ -35,7 +35,7 @@ EXPORTS = (
     "pv_version",
 )
 
-FPS_MAX_POINTS = 106496  # PV_FPS_MAX_POINTS
+FPS_MAX_POINTS = 212992  # PV_FPS_MAX_POINTS
 
 MAX_FRAMES = 256  # PV_MAX_FRAMES
 

@@ -12,8 +12,8 @@
 // an iteration never touches global memory: 16 CTAs of 256 threads with 16
 // points a thread in registers, or 8 CTAs of 256 threads with 32 points a
 // thread when a launch has more clouds than the GPU holds 16-CTA clusters
-// (clouds up to 65,536 points); 8 CTAs of 1024 threads with the points in
-// shared memory (16 bytes a point, up to 13,312 points a CTA) beyond.
+// (clouds up to 65,536 points); beyond, 16 or 8 CTAs of 1024 threads with the
+// points in shared memory (16 bytes a point, up to 13,312 points a CTA).
 // Iteration k: every thread updates its running minima against the last
 // sample and takes its farthest point (largest distance, then lowest index);
 // each warp reduces (distance bits, index) with two redux instructions, one
@@ -49,10 +49,11 @@ namespace {
 // Clouds up to 65,536 points live in registers: in clusters of 16 CTAs (the
 // non-portable cluster size) while a launch's clouds all fit on the GPU at
 // once in such clusters, else in clusters of 8 CTAs.  Larger clouds (up to
-// PV_FPS_MAX_POINTS) take clusters of 8 CTAs of 1024 threads with the points
-// in shared memory.  Measured on the 65,536-point LiDAR-shaped cloud with
-// 4,096 samples: 16 CTAs x 256 threads 2.51 ms (x 512: 2.77, x 128: 2.52);
-// 8 CTAs x 256 threads 3.9 ms, and 6.5-6.8 ms for 19 clouds at once.
+// PV_FPS_MAX_POINTS) keep their points in shared memory, in clusters of 16
+// CTAs of 1024 threads on the same rule (always past 106,496 points, which 8
+// CTAs cannot hold), else 8.  Measured on the 65,536-point LiDAR-shaped cloud
+// with 4,096 samples: 16 CTAs x 256 threads 2.51 ms (x 512: 2.77, x 128:
+// 2.52); 8 CTAs x 256 threads 3.9 ms, and 3.6 ms for 15 clouds at once.
 constexpr int kRegsPoints = 65536;
 constexpr int kWideCluster = 16;
 constexpr int kWideThreads = 256;
@@ -61,9 +62,11 @@ constexpr int kNarrowCluster = 8;
 constexpr int kNarrowThreads = 256;
 constexpr int kNarrowPer = kRegsPoints / (kNarrowCluster * kNarrowThreads);
 constexpr int kClusterSmem = 8;
+constexpr int kWideSmemCluster = 16;
 constexpr int kThreadsSmem = 1024;
-constexpr int kCapPerCta = PV_FPS_MAX_POINTS / kClusterSmem;  // points held by one CTA
+constexpr int kCapPerCta = 13312;  // points one CTA holds in shared memory
 constexpr int kSmemBytes = kCapPerCta * 16;
+static_assert(kCapPerCta * kWideSmemCluster == PV_FPS_MAX_POINTS, "16 CTAs hold the largest cloud");
 // One CTA a SM: a cluster spread over as many SMs as it has CTAs.
 constexpr int kSmemFloor = 120 * 1024;
 static_assert(kWidePer * kWideCluster * kWideThreads == kRegsPoints && kNarrowPer * kNarrowCluster * kNarrowThreads == kRegsPoints,
@@ -390,7 +393,8 @@ int device_of(const void* ptr) {
 
 std::mutex g_fps_mu;
 bool g_fps_ready[64];
-int g_wide_clusters[64];  // 16-CTA clusters the GPU holds at once (0: never take them)
+int g_wide_clusters[64];       // 16-CTA clusters the GPU holds at once (0: never take them)
+int g_wide_smem_clusters[64];  // the same for the shared-memory variant
 
 }  // namespace
 
@@ -423,11 +427,16 @@ extern "C" int pv_fps(const float* points, int num_clouds, int64_t num_points, i
         cudaGetLastError();
         st = PV_ERR_CUDA;
       } else {
-        // 16-CTA clusters are optional: without them every cloud takes 8.
+        // 16-CTA clusters are optional: without them every cloud takes 8 (and
+        // clouds past 8 CTAs' shared memory are refused).
         const size_t wide = regs_smem(kWideThreads * kWidePer);
         g_wide_clusters[dev] = prepare_fps<kWideCluster, kWideThreads, kWidePer>(wide)
                                    ? max_clusters<kWideCluster, kWideThreads, kWidePer>(wide)
                                    : 0;
+        cudaGetLastError();
+        g_wide_smem_clusters[dev] = prepare_fps<kWideSmemCluster, kThreadsSmem, 0>(kSmemBytes)
+                                        ? max_clusters<kWideSmemCluster, kThreadsSmem, 0>(kSmemBytes)
+                                        : 0;
         cudaGetLastError();
         g_fps_ready[dev] = true;
       }
@@ -454,8 +463,20 @@ extern "C" int pv_fps(const float* points, int num_clouds, int64_t num_points, i
         const long long per = (num_points + kNarrowCluster - 1) / kNarrowCluster;
         e = launch_fps<kNarrowCluster, kNarrowThreads, kNarrowPer>(fp, num_clouds, regs_smem(per), s);
       } else {
-        const long long per = (num_points + kClusterSmem - 1) / kClusterSmem;
-        e = launch_fps<kClusterSmem, kThreadsSmem, 0>(fp, num_clouds, static_cast<size_t>(per) * 16, s);
+        // Points in shared memory: 16-CTA clusters while the clouds fit on the
+        // GPU at once in them (or when 8 CTAs cannot hold a cloud), else 8.
+        const long long per8 = (num_points + kClusterSmem - 1) / kClusterSmem;
+        const long long per16 = (num_points + kWideSmemCluster - 1) / kWideSmemCluster;
+        const bool wide = g_wide_smem_clusters[dev] > 0 &&
+                          (num_clouds <= g_wide_smem_clusters[dev] || per8 > kCapPerCta);
+        if (wide) {
+          e = launch_fps<kWideSmemCluster, kThreadsSmem, 0>(fp, num_clouds, regs_smem(per16), s);
+        } else if (per8 <= kCapPerCta) {
+          e = launch_fps<kClusterSmem, kThreadsSmem, 0>(fp, num_clouds, static_cast<size_t>(per8) * 16, s);
+        } else {
+          st = PV_ERR_UNSUPPORTED;  // no 16-CTA clusters on this device
+          e = cudaSuccess;
+        }
       }
       if (e != cudaSuccess) {
         cudaGetLastError();

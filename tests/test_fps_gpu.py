@@ -69,7 +69,26 @@ def test_batch_in_16_and_8_cta_clusters(clouds):
 
 
 def test_largest_cloud():
+    # 212,992 points: 13,312 a CTA in shared memory, 16-CTA clusters only.
     check(cloud(pv.FPS_MAX_POINTS, 2), 1024, start=777)
+
+
+@pytest.mark.parametrize("n", [65_537, 106_496, 106_497])
+def test_clouds_past_the_register_variant(n):
+    # Past 65,536 points the cloud lives in shared memory; past 106,496 it
+    # needs 16 CTAs.
+    check(cloud(n, 7 + n % 5), 600, start=n // 2)
+
+
+@pytest.mark.parametrize("clouds", [2, 12])
+def test_batch_in_shared_memory(clouds):
+    # 80,000-point clouds: 16-CTA clusters while the batch fits the GPU at
+    # once in them, else 8-CTA clusters.
+    pts = np.stack([cloud(80_000, 40 + b) for b in range(clouds)])
+    got = pv.fps(torch.from_numpy(pts).to(DEV), 300).cpu().numpy()
+    for b in range(clouds):
+        st, ref = oracle.fps(pts[b], 300, 0)
+        assert st == 0 and np.array_equal(got[b], ref), b
 
 
 @pytest.mark.parametrize("n", [1, 2, 7, 8, 9, 100, 8193])
