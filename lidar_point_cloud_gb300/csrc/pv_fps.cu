@@ -48,16 +48,19 @@ namespace {
 
 // Clouds up to 65,536 points live in registers: in clusters of 16 CTAs (the
 // non-portable cluster size) while a launch's clouds all fit on the GPU at
-// once in such clusters, else in clusters of 8 CTAs.  Larger clouds (up to
-// PV_FPS_MAX_POINTS) keep their points in shared memory, in clusters of 16
-// CTAs of 1024 threads on the same rule (always past 106,496 points, which 8
-// CTAs cannot hold), else 8.  Measured on the 65,536-point LiDAR-shaped cloud
-// with 4,096 samples: 16 CTAs x 256 threads 2.51 ms (x 512: 2.77, x 128:
-// 2.52); 8 CTAs x 256 threads 3.9 ms, and 3.6 ms for 15 clouds at once.
+// once in such clusters, else in clusters of 8 CTAs; up to 131,072 points,
+// 16 CTAs with 32 points a thread while the clouds fit at once.  Otherwise
+// (up to PV_FPS_MAX_POINTS) the points live in shared memory, in clusters of
+// 16 CTAs of 1024 threads on the same rule (always past 106,496 points, which
+// 8 CTAs cannot hold), else 8.  Measured on the 65,536-point LiDAR-shaped
+// cloud with 4,096 samples: 16 CTAs x 256 threads 2.51 ms (x 512: 2.77,
+// x 128: 2.52); 8 CTAs x 256 threads 3.9 ms, and 3.6 ms for 15 clouds at once.
 constexpr int kRegsPoints = 65536;
 constexpr int kWideCluster = 16;
 constexpr int kWideThreads = 256;
 constexpr int kWidePer = kRegsPoints / (kWideCluster * kWideThreads);
+constexpr int kBigRegsPoints = 131072;  // 16 CTAs x 256 threads x 32 points
+constexpr int kBigPer = kBigRegsPoints / (kWideCluster * kWideThreads);
 constexpr int kNarrowCluster = 8;
 constexpr int kNarrowThreads = 256;
 constexpr int kNarrowPer = kRegsPoints / (kNarrowCluster * kNarrowThreads);
@@ -395,6 +398,7 @@ std::mutex g_fps_mu;
 bool g_fps_ready[64];
 int g_wide_clusters[64];       // 16-CTA clusters the GPU holds at once (0: never take them)
 int g_wide_smem_clusters[64];  // the same for the shared-memory variant
+int g_big_clusters[64];        // the same for 32 points a thread in registers
 
 }  // namespace
 
@@ -438,6 +442,11 @@ extern "C" int pv_fps(const float* points, int num_clouds, int64_t num_points, i
                                         ? max_clusters<kWideSmemCluster, kThreadsSmem, 0>(kSmemBytes)
                                         : 0;
         cudaGetLastError();
+        const size_t big = regs_smem(kWideThreads * kBigPer);
+        g_big_clusters[dev] = prepare_fps<kWideCluster, kWideThreads, kBigPer>(big)
+                                  ? max_clusters<kWideCluster, kWideThreads, kBigPer>(big)
+                                  : 0;
+        cudaGetLastError();
         g_fps_ready[dev] = true;
       }
     }
@@ -462,6 +471,9 @@ extern "C" int pv_fps(const float* points, int num_clouds, int64_t num_points, i
       } else if (num_points <= kRegsPoints) {
         const long long per = (num_points + kNarrowCluster - 1) / kNarrowCluster;
         e = launch_fps<kNarrowCluster, kNarrowThreads, kNarrowPer>(fp, num_clouds, regs_smem(per), s);
+      } else if (num_points <= kBigRegsPoints && num_clouds <= g_big_clusters[dev]) {
+        const long long per = (num_points + kWideCluster - 1) / kWideCluster;
+        e = launch_fps<kWideCluster, kWideThreads, kBigPer>(fp, num_clouds, regs_smem(per), s);
       } else {
         // Points in shared memory: 16-CTA clusters while the clouds fit on the
         // GPU at once in them (or when 8 CTAs cannot hold a cloud), else 8.

@@ -73,17 +73,19 @@ def test_largest_cloud():
     check(cloud(pv.FPS_MAX_POINTS, 2), 1024, start=777)
 
 
-@pytest.mark.parametrize("n", [65_537, 106_496, 106_497])
-def test_clouds_past_the_register_variant(n):
-    # Past 65,536 points the cloud lives in shared memory; past 106,496 it
-    # needs 16 CTAs.
+@pytest.mark.parametrize("n", [65_537, 106_497, 131_072, 131_073])
+def test_clouds_past_16_points_a_thread(n):
+    # Up to 131,072 points 16 CTAs hold 32 points a thread in registers;
+    # past that the cloud lives in shared memory, in 16 CTAs (8 cannot hold
+    # more than 106,496 points).
     check(cloud(n, 7 + n % 5), 600, start=n // 2)
 
 
 @pytest.mark.parametrize("clouds", [2, 12])
-def test_batch_in_shared_memory(clouds):
-    # 80,000-point clouds: 16-CTA clusters while the batch fits the GPU at
-    # once in them, else 8-CTA clusters.
+def test_batch_of_larger_clouds(clouds):
+    # 80,000-point clouds: 16-CTA clusters with 32 points a thread in
+    # registers while the batch fits the GPU at once in them, else in shared
+    # memory (16 or 8 CTAs by the same rule).
     pts = np.stack([cloud(80_000, 40 + b) for b in range(clouds)])
     got = pv.fps(torch.from_numpy(pts).to(DEV), 300).cpu().numpy()
     for b in range(clouds):
