@@ -1990,11 +1990,19 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   if (pl->cells * frames >= (int64_t(1) << 31)) return PV_ERR_INVALID;  // batched ids stay int32
   const int64_t cells = pl->cells * frames;  // one key space per frame
   const int64_t distinct_bound = std::max<int64_t>(1, std::min(N, cells));
-  const int64_t hashed_T = next_pow2(std::max<int64_t>(2 * distinct_bound, 1024));
+  // Hashed tables at most a quarter full: a warp waits for its longest probe
+  // chain, each probe a dependent L2 round trip.
+  const int64_t hashed_T = next_pow2(std::max<int64_t>(4 * distinct_bound, 1024));
   pl->KT = std::max(0, ((K + 3) & ~3) - kHead);
   const int64_t direct_bytes = cells * (kHead + pl->KT) * 8;
+  // Direct (one slot per cell, no probing) whenever it is not much larger
+  // than the hashed table would be, or costs at most 256 MB whatever the
+  // cloud (a small cloud on the KITTI pillar grid: 55 MB), up to 2 GB.
   int mode = o.table_mode;
-  if (mode == 0) mode = (cells <= 2 * hashed_T && direct_bytes <= (int64_t(1) << 31)) ? 1 : 2;
+  if (mode == 0)
+    mode = ((cells <= 2 * hashed_T || direct_bytes <= (int64_t(256) << 20)) && direct_bytes <= (int64_t(1) << 31))
+               ? 1
+               : 2;
   pl->mode = mode;
   if (mode == 1) {
     pl->T = cells;
@@ -2417,6 +2425,7 @@ int voxelize_static_impl(const float* points, int64_t N, const float range[6], c
   if (st != PV_OK) return st;
   pv_options opt{};
   opt.table_mode = 2;  // hashed: the static table has a fixed number of slots
+  opt.table_log2 = kStaticTableLog2;
   Plan pl;
   if ((st = make_plan(N, range, vsize, K, M, &opt, sd->info, &pl)) != PV_OK) return st;
   if (pl.T > static_cast<int64_t>(kStaticSlots) || pl.list_words > kStaticListWords) return PV_ERR_TOO_LARGE;
