@@ -94,12 +94,19 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+HOST_SIDE_MARKER = b"// ------------------------------------------------------------ host side"
+
+
 def kernel_sha(kernel="pv_voxelize_kernel"):
-    """SHA-256 of the source file that holds the kernel."""
+    """SHA-256 of the device code of the source file that holds the kernel:
+    everything before the file's host-side marker (launch, planning and ABI
+    code after it can change without changing what a profile measured)."""
     name = "pv_fps.cu" if kernel == "pv_fps_kernel" else "pv_voxelize.cu"
     src = os.path.join(ROOT, "lidar_point_cloud_gb300", "csrc", name)
     with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+        text = f.read()
+    cut = text.find(HOST_SIDE_MARKER)
+    return hashlib.sha256(text[:cut] if cut >= 0 else text).hexdigest()
 
 
 def profiled_traffic(workload, kernel="pv_voxelize_kernel"):

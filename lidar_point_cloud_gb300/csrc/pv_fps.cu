@@ -328,6 +328,8 @@ __global__ void __launch_bounds__(kT, 1) pv_fps_kernel(const FpsParams p) {
   if (tid == 0 && s_late) atomicMin(p.status, PV_ERR_TIMEOUT);
 }
 
+// ------------------------------------------------------------ host side
+
 template <int kC, int kT, int kP>
 cudaError_t launch_fps(const FpsParams& fp, int clouds, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
