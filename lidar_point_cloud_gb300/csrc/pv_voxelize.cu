@@ -80,15 +80,16 @@ constexpr int kFlagUnroll = 4;             // block-wide tiles in flight when fl
 // accesses of a launch stay inside a table a fraction of the size.
 constexpr int kHead = PV_HEAD_ENTRIES;
 static_assert(kHead == 4 || kHead == 8, "head rows are 32 or 64 bytes");
-#ifndef PV_EMIT_UNROLL
-#define PV_EMIT_UNROLL 4
+#ifndef PV_EMIT_LANES
+#define PV_EMIT_LANES 8
 #endif
-constexpr int kEmitUnroll = PV_EMIT_UNROLL;  // pillars in flight per warp when emitting
+constexpr int kEmitLanes = PV_EMIT_LANES;    // lanes per pillar when copying short lists
+constexpr int kEmitPer = 32 / kEmitLanes;    // pillars in flight per warp
 #ifndef PV_INSERT_UNROLL
 #define PV_INSERT_UNROLL 1
 #endif
 constexpr int kInsertUnroll = PV_INSERT_UNROLL;  // records in flight per thread when inserting
-static_assert(kEmitUnroll >= 1 && kEmitUnroll <= 16 && 32 % kEmitUnroll == 0, "emit batches tile a warp");
+static_assert(kEmitLanes >= 2 && kEmitLanes <= 32 && 32 % kEmitLanes == 0, "emit batches tile a warp");
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded spins: 1 s
 constexpr int64_t kMaxAxisCells = int64_t(1) << 24;
 
@@ -677,26 +678,33 @@ __device__ __forceinline__ Head read_head(const KParams& p, const unsigned long 
   return h;
 }
 
-// Source row (index into tile_rows) of output position e of the pillar
-// whose head lane u holds, or -1 for a zero row.  Every lane calls it with
-// the same u.
-__device__ __forceinline__ long long head_source(const Head& h, int u, unsigned int e) {
-  const int ng = __shfl_sync(0xffffffffu, h.ng, u);
-  const unsigned int n = __shfl_sync(0xffffffffu, h.n, u);
-  unsigned long long ge = 0;
-  unsigned int start = 0, run = 0;
+// Copy descriptor of a pillar served by its first groups, computed by the
+// lane that read its head: the points taken n, the starts of groups 1..3 in
+// the output row (clamped to n; a missing group starts at n), and per group
+// j its first point's row in tile_rows minus its start, so that position e
+// of group j comes from row o[j] + e.
+struct CopyDesc {
+  unsigned int w0;  // n | s1 << 16
+  unsigned int w1;  // s2 | s3 << 16
+  int o[4];
+};
+
+__device__ __forceinline__ CopyDesc copy_desc(const Head& h) {
+  CopyDesc d;
+  unsigned int st[4];
+  unsigned int run = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const unsigned long long ej = __shfl_sync(0xffffffffu, h.e[j], u);
-    if (j < ng && run <= e) {
-      ge = ej;
-      start = run;
-    }
+    const unsigned long long ej = h.e[j];
+    const long long base = (static_cast<long long>(ej >> 32) & ~static_cast<long long>(kThreads - 1)) +
+                           ((static_cast<unsigned int>(ej) >> 11) & 1023u);
+    d.o[j] = static_cast<int>(base - static_cast<long long>(run));
+    st[j] = j < h.ng ? (run < h.n ? run : h.n) : h.n;
     run += static_cast<unsigned int>(ej) & 2047u;
   }
-  if (e >= n) return -1;
-  return (static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1)) +
-         ((static_cast<unsigned int>(ge) >> 11) & 1023u) + (e - start);
+  d.w0 = h.n | (st[1] << 16);
+  d.w1 = st[2] | (st[3] << 16);
+  return d;
 }
 
 // Writes the output row of a pillar from its whole list: groups in list
@@ -1173,7 +1181,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     // end inside positions 0..3 loses those, any other list every position.
     // Kept: a pillar whose points all come from those groups (its list ends
     // inside them, or they already hold max_points points) is copied by the
-    // warp kEmitUnroll pillars at a time; the others are emitted one by one
+    // warp kEmitPer pillars at a time; the others are emitted one by one
     // from their whole list.
     bool stale = false;
     // (Counts of pillars and warps fit 32 bits: N < 2^29, at most 1024 x 32 warps.)
@@ -1235,31 +1243,37 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       const unsigned int cnt0 = few ? hd.n : 0u;
       unsigned int cnt = cnt0;
       const unsigned int fmask = __ballot_sync(0xffffffffu, few);
-      // Pillars served by their first groups, kEmitUnroll at a time: lane e copies position e.
-      for (int u0 = 0; u0 < 32; u0 += kEmitUnroll) {
-        if (((fmask >> u0) & ((1u << kEmitUnroll) - 1u)) == 0u) continue;
-        float4 v[kEmitUnroll];
+      // Pillars served by their first groups, kEmitPer at a time: kEmitLanes
+      // lanes per pillar, each copying positions sub, sub + kEmitLanes, ...
+      // from the descriptor its pillar's lane computed.
+      {
+        const CopyDesc cd = copy_desc(hd);
+        const unsigned int sub = lane % kEmitLanes;
+        const unsigned int pu = lane / kEmitLanes;
+        for (int u0 = 0; u0 < 32; u0 += kEmitPer) {
+          if (((fmask >> u0) & ((1u << kEmitPer) - 1u)) == 0u) continue;
+          const int u = u0 + static_cast<int>(pu);
+          const unsigned int w0 = __shfl_sync(0xffffffffu, cd.w0, u);
+          const unsigned int w1 = __shfl_sync(0xffffffffu, cd.w1, u);
+          int o[4];
 #pragma unroll
-        for (int j = 0; j < kEmitUnroll; ++j) {
-          const long long src = head_source(hd, u0 + j, lane);
-          v[j] = src >= 0 ? __ldcg(p.tile_rows + src) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+          for (int j = 0; j < 4; ++j) o[j] = __shfl_sync(0xffffffffu, cd.o[j], u);
+          const long long row_u = __shfl_sync(0xffffffffu, row, u);
+          const unsigned int n = w0 & 0xFFFFu, s1 = w0 >> 16, s2 = w1 & 0xFFFFu, s3 = w1 >> 16;
+          float4* orow = p.out_voxels + static_cast<size_t>(row_u) * K;
+          const unsigned int kend = ((fmask >> u) & 1u) ? static_cast<unsigned int>(K) : 0u;  // lanes of a pillar not served here copy nothing
+          for (unsigned int e0 = sub; e0 < kend; e0 += 4 * kEmitLanes) {
+            float4 v[4];
 #pragma unroll
-        for (int j = 0; j < kEmitUnroll; ++j) {
-          const long long row_u = __shfl_sync(0xffffffffu, row, u0 + j);
-          if (((fmask >> (u0 + j)) & 1u) && static_cast<int>(lane) < K)
-            p.out_voxels[static_cast<size_t>(row_u) * K + lane] = v[j];
-        }
-        if (K > 32) {  // positions 32 .. K-1 (every lane runs the same trips: head_source shuffles)
-          const unsigned int k32 = (static_cast<unsigned int>(K) + 31u) & ~31u;
-          for (int j = 0; j < kEmitUnroll; ++j) {
-            if (!((fmask >> (u0 + j)) & 1u)) continue;
-            const long long row_u = __shfl_sync(0xffffffffu, row, u0 + j);
-            for (unsigned int e = lane + 32; e < k32; e += 32) {
-              const long long src = head_source(hd, u0 + j, e);
-              if (e < static_cast<unsigned int>(K))
-                p.out_voxels[static_cast<size_t>(row_u) * K + e] =
-                    src >= 0 ? __ldcg(p.tile_rows + src) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < 4; ++k) {
+              const unsigned int e = e0 + k * kEmitLanes;
+              const int oe = e >= s3 ? o[3] : e >= s2 ? o[2] : e >= s1 ? o[1] : o[0];
+              v[k] = e < n ? __ldcg(p.tile_rows + (static_cast<long long>(oe) + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const unsigned int e = e0 + k * kEmitLanes;
+              if (e < static_cast<unsigned int>(K)) orow[e] = v[k];
             }
           }
         }
