@@ -85,10 +85,6 @@ static_assert(kHead == 4 || kHead == 8, "head rows are 32 or 64 bytes");
 #endif
 constexpr int kEmitLanes = PV_EMIT_LANES;    // lanes per pillar when copying short lists
 constexpr int kEmitPer = 32 / kEmitLanes;    // pillars in flight per warp
-#ifndef PV_INSERT_UNROLL
-#define PV_INSERT_UNROLL 1
-#endif
-constexpr int kInsertUnroll = PV_INSERT_UNROLL;  // records in flight per thread when inserting
 static_assert(kEmitLanes >= 2 && kEmitLanes <= 32 && 32 % kEmitLanes == 0, "emit batches tile a warp");
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded spins: 1 s
 constexpr int64_t kMaxAxisCells = int64_t(1) << 24;
@@ -227,7 +223,6 @@ constexpr int kStamps = 8;
 __device__ unsigned long long g_phase_ns[kStampCtas][kStamps];
 __device__ unsigned long long g_p1_ns[kStampCtas][kStamps];
 __device__ unsigned long long g_insert_stats[4];  // inserts, atomics, rejected up front, max atomics
-__device__ unsigned long long g_ins_ns[kStampCtas][4];  // thread 0's first insert: start, records, heads, done
 __device__ __forceinline__ void pv_wait_reg(unsigned int v) {
   unsigned int d;
   asm volatile("mov.b32 %0, %1;" : "=r"(d) : "r"(v));
@@ -594,9 +589,14 @@ __device__ __forceinline__ unsigned int chunk_rank(int* ckey, unsigned int* ccnt
 }
 
 // Byte counters at map position h: *before = warps 0 .. warp-1, *total = all.
+// Each word holds four warps' counts (at most 32 each), summed with dp4a
+// against ones; the words before this warp's count whole, its own word only
+// in the bytes of lower warps.
 __device__ __forceinline__ void tile_counts(const TileMap& m, int h, unsigned int warp, unsigned int* before,
                                             unsigned int* total) {
   const uint4* row = reinterpret_cast<const uint4*>(m.cnt + static_cast<size_t>(h) * (kWarps / 4));
+  const unsigned int pc = warp >> 2;                       // word holding this warp's byte
+  const unsigned int pm = (1u << (8u * (warp & 3u))) - 1u;  // bytes of lower warps in that word
   unsigned int b = 0, t = 0;
 #pragma unroll
   for (int r = 0; r < kWarps / 16; ++r) {
@@ -604,15 +604,10 @@ __device__ __forceinline__ void tile_counts(const TileMap& m, int h, unsigned in
     const unsigned int w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int lo = 16 * r + 4 * c;  // warp of the word's lowest byte
-      const unsigned int all = (w[c] * 0x01010101u) >> 24;  // byte sum (bytes <= 32)
-      t += all;
-      const int keep = static_cast<int>(warp) - lo;
-      if (keep >= 4) {
-        b += all;
-      } else if (keep > 0) {
-        b += ((w[c] & ((1u << (8 * keep)) - 1u)) * 0x01010101u) >> 24;
-      }
+      const unsigned int idx = static_cast<unsigned int>(4 * r + c);
+      t = __dp4a(w[c], 0x01010101u, t);
+      const unsigned int msk = idx < pc ? 0xFFFFFFFFu : (idx == pc ? pm : 0u);
+      b = __dp4a(w[c] & msk, 0x01010101u, b);
     }
   }
   *before = b;
@@ -952,18 +947,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         // chunk (or max_points groups) can never be kept: not recorded.
         const unsigned int wants =
             (lead && crank < K && (cseen & 0xFFFFu) < static_cast<unsigned int>(K)) ? 1u : 0u;
-        unsigned int incl = need, rincl = wants;
+        // One scan for both: a warp's groups hold at most kThreads points
+        // (low half) and it has at most 32 records (high half).
+        unsigned int pk = need | (wants << 16);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
-          const unsigned int ry = __shfl_up_sync(0xffffffffu, rincl, o);
-          if (lane >= static_cast<unsigned int>(o)) {
-            incl += y;
-            rincl += ry;
-          }
+          const unsigned int y = __shfl_up_sync(0xffffffffu, pk, o);
+          if (lane >= static_cast<unsigned int>(o)) pk += y;
         }
-        const unsigned int wsum = __shfl_sync(0xffffffffu, incl, 31);
-        const unsigned int rsum = __shfl_sync(0xffffffffu, rincl, 31);
+        const unsigned int psum = __shfl_sync(0xffffffffu, pk, 31);
+        const unsigned int incl = pk & 0xFFFFu, rincl = pk >> 16;
+        const unsigned int wsum = psum & 0xFFFFu, rsum = psum >> 16;
         unsigned int base = 0, rbase = 0;
         if (lane == 31) {
           if (wsum) base = atomicAdd(tm.layout, wsum);
@@ -1001,47 +995,25 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     if (tid == 0 && cta < kStampCtas) g_p1_ns[cta][5] = global_timer_ns();
 #endif
     const unsigned int nrec = s_nrec;
-    // kInsertUnroll records per thread at a time: their records, then their
-    // head rows, are read together before the cascades run one by one.
-    for (unsigned int j0 = tid; j0 < nrec; j0 += kInsertUnroll * kThreads) {
-#ifdef PV_INSTRUMENT
-      if (tid == 0 && j0 == 0 && cta < kStampCtas) g_ins_ns[cta][0] = global_timer_ns();
-#endif
-      int rs[kInsertUnroll];
-      unsigned long long entry[kInsertUnroll];
-#pragma unroll
-      for (int u = 0; u < kInsertUnroll; ++u) {
-        const unsigned int j = j0 + u * kThreads;
-        rs[u] = j < nrec ? __ldcg(p.firsts + begin + j) : -1;
-        entry[u] = j < nrec ? __ldcg(p.recs + begin + j) : 0ull;
-      }
-#ifdef PV_INSTRUMENT
-      if (tid == 0 && j0 == 0 && cta < kStampCtas) {
-        pv_wait_reg(static_cast<unsigned int>(rs[0]) ^ static_cast<unsigned int>(entry[0]));
-        g_ins_ns[cta][1] = global_timer_ns();
-      }
-#endif
-      uint4 h[kInsertUnroll][kHead / 2];
-#pragma unroll
-      for (int u = 0; u < kInsertUnroll; ++u)
+    // One record per thread at a time; the thread's next record is read
+    // while the current one's cascade runs.
+    {
+      unsigned int j0 = tid;
+      int rs = j0 < nrec ? __ldcg(p.firsts + begin + j0) : -1;
+      unsigned long long entry = j0 < nrec ? __ldcg(p.recs + begin + j0) : 0ull;
+      for (; j0 < nrec; j0 += kThreads) {
+        const unsigned int j1 = j0 + kThreads;
+        const int rs1 = j1 < nrec ? __ldcg(p.firsts + begin + j1) : -1;
+        const unsigned long long entry1 = j1 < nrec ? __ldcg(p.recs + begin + j1) : 0ull;
+        uint4 h[kHead / 2];
 #pragma unroll
         for (int t = 0; t < kHead / 2; ++t)
-          h[u][t] = rs[u] >= 0 ? __ldcg(reinterpret_cast<const uint4*>(p.lists + static_cast<size_t>(rs[u]) * kHead) + t)
-                               : make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
-#ifdef PV_INSTRUMENT
-      if (tid == 0 && j0 == 0 && cta < kStampCtas) {
-        pv_wait_reg(h[0][0].x ^ h[0][kHead / 2 - 1].w);
-        g_ins_ns[cta][2] = global_timer_ns();
+          h[t] = __ldcg(reinterpret_cast<const uint4*>(p.lists + static_cast<size_t>(rs) * kHead) + t);
+        list_insert(list_of(p, rs), h, K, p.KT, entry, static_cast<int>((entry >> 21) & 2047u),
+                    static_cast<uint32_t>(begin), static_cast<uint32_t>(end - begin));
+        rs = rs1;
+        entry = entry1;
       }
-#endif
-#pragma unroll
-      for (int u = 0; u < kInsertUnroll; ++u)
-        if (rs[u] >= 0)
-          list_insert(list_of(p, rs[u]), h[u], K, p.KT, entry[u], static_cast<int>((entry[u] >> 21) & 2047u),
-                      static_cast<uint32_t>(begin), static_cast<uint32_t>(end - begin));
-#ifdef PV_INSTRUMENT
-      if (tid == 0 && j0 == 0 && cta < kStampCtas) g_ins_ns[cta][3] = global_timer_ns();
-#endif
     }
     PV_STAMP(1);
     alive = grid_sync(p.ctl, bar_target + p.bar_extra, &s_flag);
@@ -2663,13 +2635,6 @@ int pv_debug_p1_times(unsigned long long* out, int max_ctas) {
   const int n = max_ctas < kStampCtas ? max_ctas : kStampCtas;
   if (cudaMemcpyFromSymbol(out, g_p1_ns, sizeof(unsigned long long) * kStamps * n) != cudaSuccess)
     return PV_ERR_CUDA;
-  return PV_OK;
-}
-
-// Instrumented builds only: thread 0's first insert round, [max_ctas][4] stamps (ns).
-int pv_debug_ins_times(unsigned long long* out, int max_ctas) {
-  const int n = max_ctas < kStampCtas ? max_ctas : kStampCtas;
-  if (cudaMemcpyFromSymbol(out, g_ins_ns, sizeof(unsigned long long) * 4 * n) != cudaSuccess) return PV_ERR_CUDA;
   return PV_OK;
 }
 
