@@ -435,6 +435,23 @@ __device__ __forceinline__ unsigned long long ull_of(uint32_t lo, uint32_t hi) {
   return (static_cast<unsigned long long>(hi) << 32) | lo;
 }
 
+// List entry: (leader index << 32) | (chunk rank << 22) | (d << 11) | size,
+// where the group's rows start in tile_rows at leader index + d (d signed,
+// 11 bits: a group lies inside its 1024-point tile) and the chunk rank is
+// below max_points <= 1024.
+__device__ __forceinline__ unsigned long long make_entry(long long leader, unsigned int crank, long long row,
+                                                         unsigned int size) {
+  const unsigned int d = static_cast<unsigned int>(row - leader) & 2047u;
+  return (static_cast<unsigned long long>(leader) << 32) | (crank << 22) | (d << 11) | size;
+}
+__device__ __forceinline__ long long entry_row(unsigned long long ent) {
+  const int d = static_cast<int>(static_cast<unsigned int>(ent) << 10) >> 21;  // bits 11..21, sign-extended
+  return static_cast<long long>(ent >> 32) + d;
+}
+__device__ __forceinline__ int entry_crank(unsigned long long ent) {
+  return static_cast<int>((static_cast<unsigned int>(ent) >> 22) & 1023u);
+}
+
 // A slot's list: positions 0 .. kHead-1 in its head row, the rest in its tail row.
 struct ListRef {
   unsigned long long* head;
@@ -691,9 +708,7 @@ __device__ __forceinline__ CopyDesc copy_desc(const Head& h) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const unsigned long long ej = h.e[j];
-    const long long base = (static_cast<long long>(ej >> 32) & ~static_cast<long long>(kThreads - 1)) +
-                           ((static_cast<unsigned int>(ej) >> 11) & 1023u);
-    d.o[j] = static_cast<int>(base - static_cast<long long>(run));
+    d.o[j] = static_cast<int>(entry_row(ej) - static_cast<long long>(run));
     st[j] = j < h.ng ? (run < h.n ? run : h.n) : h.n;
     run += static_cast<unsigned int>(ej) & 2047u;
   }
@@ -746,8 +761,7 @@ __device__ unsigned int emit_groups(const KParams& p, const ListRef& L, float4* 
     if (e < K) {
       float4 row = z4;
       if (static_cast<unsigned int>(e) < written) {
-        const long long tbase = static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1);
-        row = __ldcg(p.tile_rows + tbase + ((static_cast<unsigned int>(ge) >> 11) & 1023u) + (e - gs));
+        row = __ldcg(p.tile_rows + entry_row(ge) + (e - gs));
       }
       orow[e] = row;
     }
@@ -770,8 +784,7 @@ __device__ unsigned int emit_groups(const KParams& p, const ListRef& L, float4* 
       const unsigned int info = static_cast<unsigned int>(ge);
       const unsigned int room = static_cast<unsigned int>(K) - written;
       const unsigned int n = (info & 2047u) < room ? (info & 2047u) : room;
-      const long long base =
-          (static_cast<long long>(ge >> 32) & ~static_cast<long long>(kThreads - 1)) + ((info >> 11) & 1023u);
+      const long long base = entry_row(ge);
       for (unsigned int j = lane; j < n; j += 32) orow[written + j] = __ldcg(p.tile_rows + base + j);
       written += n;
     }
@@ -856,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   // once (their chunk ranks keep them apart).
   if (alive) {
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    long long tb = begin;  // this block's contiguous, tile-aligned chunk
+    long long tb = begin;  // this block's contiguous chunk, in tiles from its start
     float4 q = (tb + tid < end) ? __ldg(p.points + tb + tid) : z4;
     const bool multi = end - begin > kThreads;  // more than one tile: second map and chunk map in use
     int* ckey = reinterpret_cast<int*>(s_dyn + 2 * kMapBytes);
@@ -975,8 +988,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           if (wants) {
             const long long rj = begin + rbase + rincl - wants;
             p.firsts[rj] = slot;  // the record's slot (firsts is rewritten after the barrier)
-            p.recs[rj] = (static_cast<unsigned long long>(i) << 32) |
-                         (static_cast<unsigned int>(crank) << 21) | (off << 11) | tot;
+            p.recs[rj] = make_entry(i, static_cast<unsigned int>(crank), tb + off, tot);
           }
         }
       }
@@ -1009,7 +1021,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
 #pragma unroll
         for (int t = 0; t < kHead / 2; ++t)
           h[t] = __ldcg(reinterpret_cast<const uint4*>(p.lists + static_cast<size_t>(rs) * kHead) + t);
-        list_insert(list_of(p, rs), h, K, p.KT, entry, static_cast<int>((entry >> 21) & 2047u),
+        list_insert(list_of(p, rs), h, K, p.KT, entry, entry_crank(entry),
                     static_cast<uint32_t>(begin), static_cast<uint32_t>(end - begin));
         rs = rs1;
         entry = entry1;
@@ -2003,9 +2015,10 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
   const int per_sm = o.ctas_per_sm ? std::min(o.ctas_per_sm, dev.blocks_per_sm) : dev.blocks_per_sm;
   // The count scan after the second barrier takes one count per thread.
   pl->ctas = std::min(std::min(kMaxCtas, kThreads), std::max(1, dev.sms * per_sm));
-  // Contiguous, tile-aligned chunks: phase 1 and phase 2 share them.
-  const int64_t tiles = (N + kThreads - 1) / kThreads;
-  pl->chunk = ((tiles + pl->ctas - 1) / pl->ctas) * kThreads;
+  // Contiguous chunks, as even as whole warps allow: phase 1 and phase 2
+  // share them, and a block's tiles start at its chunk's start.
+  const int64_t per = (N + pl->ctas - 1) / pl->ctas;
+  pl->chunk = std::max<int64_t>(32, (per + 31) / 32 * 32);
   pl->row_words = pl->unordered ? static_cast<size_t>(M) : 0;
   pl->bytes = sizeof(Control) + 4 * static_cast<size_t>(kMaxCtas) + 32 * static_cast<size_t>(N) +
               8 * pl->list_words + 4 * pl->key_words + 4 * pl->row_words;
