@@ -70,6 +70,7 @@ constexpr int kWarps = kThreads / 32;
 static_assert(kWarps <= 32 && kWarps % 16 == 0, "warp 0 scans one value per warp; 16-byte counter rows");
 constexpr int kMinBlocksPerSM = 1024 / kThreads;
 constexpr int kMaxCtas = 1024;             // blocks per launch (prefix lives in shared memory)
+static_assert(kMaxCtas < 0x10000, "finished blocks are counted in 16 bits");
 constexpr int kFlagUnroll = 4;             // block-wide tiles in flight when flagging
 #ifndef PV_HEAD_ENTRIES
 #define PV_HEAD_ENTRIES 4
@@ -842,15 +843,45 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   const long long begin = lmin(p.n, static_cast<long long>(cta) * p.chunk);
   const long long end = lmin(p.n, begin + p.chunk);
 
+  // The first tile's points are loaded and the shared maps emptied while the
+  // control block's words are in flight.
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  long long tb = begin;  // this block's contiguous chunk, in tiles from its start
+  float4 q = (tb + tid < end) ? __ldg(p.points + tb + tid) : z4;
   const unsigned int epoch = ld_relaxed(&p.ctl->epoch);
   const unsigned int dirty = ld_relaxed(&p.ctl->dirty);
   unsigned int bar_target = P;
   bool alive = true;
-  (void)epoch;
   const int B = kBatched ? p.frames : 1;
   if (kBatched)
     for (int b = static_cast<int>(tid); b <= B; b += kThreads) s_off[b] = fr.off[b];  // read after a block barrier
   PV_STAMP(0);
+  const bool multi = end - begin > kThreads;  // more than one tile: second map and chunk map in use
+  int* ckey = reinterpret_cast<int*>(s_dyn + 2 * kMapBytes);
+  unsigned int* ccnt = reinterpret_cast<unsigned int*>(ckey + kChunkHash);
+  {  // tile map 0 empty (counters zero, keys -1); map 1 and the chunk map only if used
+    uint4* d4 = reinterpret_cast<uint4*>(s_dyn);
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 m1 = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+    const int maps = multi ? 2 : 1;
+    for (int m = 0; m < maps; ++m) {
+      uint4* base = d4 + m * (kMapBytes / 16);
+      for (int j = static_cast<int>(tid); j < kTileHash * kWarps / 16; j += kThreads) base[j] = z;
+      for (int j = static_cast<int>(tid); j < kTileHash * 4 / 16; j += kThreads)
+        base[kTileHash * kWarps / 16 + j] = m1;
+    }
+    if (multi) {
+      uint4* c4 = reinterpret_cast<uint4*>(ckey);
+      for (int j = static_cast<int>(tid); j < kChunkHash / 4; j += kThreads) {
+        c4[j] = m1;
+        c4[kChunkHash / 4 + j] = z;
+      }
+    }
+  }
+  if (tid == 0) {
+    s_layout[0] = s_layout[1] = 0;
+    s_nrec = 0;
+  }
 
   // Recovery after a failed launch: empty the whole table first.
   if (dirty) {
@@ -868,39 +899,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   // ---- phase 1b: insert the recorded groups into the pillars' lists, all at
   // once (their chunk ranks keep them apart).
   if (alive) {
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    long long tb = begin;  // this block's contiguous chunk, in tiles from its start
-    float4 q = (tb + tid < end) ? __ldg(p.points + tb + tid) : z4;
-    const bool multi = end - begin > kThreads;  // more than one tile: second map and chunk map in use
-    int* ckey = reinterpret_cast<int*>(s_dyn + 2 * kMapBytes);
-    unsigned int* ccnt = reinterpret_cast<unsigned int*>(ckey + kChunkHash);
-    {  // tile map 0 empty (counters zero, keys -1); map 1 and the chunk map only if used
-      uint4* d4 = reinterpret_cast<uint4*>(s_dyn);
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      const uint4 m1 = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
-      const int maps = multi ? 2 : 1;
-      for (int m = 0; m < maps; ++m) {
-        uint4* base = d4 + m * (kMapBytes / 16);
-        for (int j = static_cast<int>(tid); j < kTileHash * kWarps / 16; j += kThreads) base[j] = z;
-        for (int j = static_cast<int>(tid); j < kTileHash * 4 / 16; j += kThreads)
-          base[kTileHash * kWarps / 16 + j] = m1;
-      }
-      if (multi) {
-        uint4* c4 = reinterpret_cast<uint4*>(ckey);
-        for (int j = static_cast<int>(tid); j < kChunkHash / 4; j += kThreads) {
-          c4[j] = m1;
-          c4[kChunkHash / 4 + j] = z;
-        }
-      }
-    }
 #ifdef PV_INSTRUMENT
     __syncthreads();
     if (tid == 0 && cta < kStampCtas) g_p1_ns[cta][6] = global_timer_ns();
 #endif
-    if (tid == 0) {
-      s_layout[0] = s_layout[1] = 0;
-      s_nrec = 0;
-    }
     __syncthreads();
     int buf = 0;
     for (; tb < end; tb += kThreads, buf ^= 1) {
@@ -1103,7 +1105,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   }
 
   unsigned int total = 0;
+  int seen_err = 0;   // thread 0: the error word once the second barrier is passed
+  bool bad = false;   // a ranked pillar without its first group (never in a clean table)
   if (alive) {
+    if (tid == 0) seen_err = static_cast<int>(ld_relaxed(reinterpret_cast<const unsigned int*>(&p.ctl->err)));
     const unsigned int c = tid < P ? __ldcg(p.counts + tid) : 0u;
     const unsigned int excl = block_exclusive_scan(c, s_tmp, &total);
     if (tid < P) s_prefix[tid] = excl;
@@ -1296,19 +1301,25 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       }
     }
     if (stale) atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
+    bad = stale;
     PV_STAMP(6);
 
   }
 
   // ---- the last block to finish publishes the status and rearms the control block.
   PV_STAMP(7);
-  __syncthreads();
+  // A block counts itself finished, in the low half of the word, and, in the
+  // high half, whether it knows of an error: one recorded before the second
+  // barrier (read after it), a failed wait of its own, or one of its
+  // gathers finding a list inconsistent.  Only then does the last block read
+  // the error word; the acquire-release count makes every block's writes
+  // (their errors included) visible to it.
+  const int any_bad = __syncthreads_or(bad || !alive);
   if (tid == 0) {
-    // Acquire-release count of finished blocks: the last one sees every
-    // block's writes (their error words included) before it reads them.
-    const unsigned int prev = atom_add_acq_rel(&p.ctl->done, 1u);
-    if (prev == P - 1) {
-      const int err = *reinterpret_cast<volatile int*>(&p.ctl->err);
+    const unsigned int mine = (any_bad || seen_err != 0) ? 0x10001u : 1u;
+    const unsigned int prev = atom_add_acq_rel(&p.ctl->done, mine);
+    if ((prev & 0xFFFFu) == P - 1) {
+      const int err = ((prev + mine) >> 16) != 0 ? *reinterpret_cast<volatile int*>(&p.ctl->err) : 0;
       if (kBatched) {
         for (int b = 0; b < B; ++b)
           p.out_num[b] = err != 0 ? err : static_cast<int32_t>(s_vcum[b + 1] - s_vcum[b]);
