@@ -827,6 +827,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   __shared__ unsigned int s_tile[kFlagUnroll][kWarps];
   __shared__ unsigned int s_tmp[kWarps + 1];
   __shared__ int s_flag;
+  __shared__ unsigned int s_dirty;
   __shared__ unsigned int s_layout[2];
   __shared__ unsigned int s_nrec;
 
@@ -848,8 +849,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   long long tb = begin;  // this block's contiguous chunk, in tiles from its start
   float4 q = (tb + tid < end) ? __ldg(p.points + tb + tid) : z4;
-  const unsigned int epoch = ld_relaxed(&p.ctl->epoch);
-  const unsigned int dirty = ld_relaxed(&p.ctl->dirty);
+  // Thread 0 alone reads the control block (the same word read by every
+  // thread would queue thousands of requests on one L2 line); the dirty flag
+  // reaches the block through shared memory, the epoch only thread 0 needs.
+  unsigned int epoch = 0, dirty_word = 0;
+  if (tid == 0) {
+    epoch = ld_relaxed(&p.ctl->epoch);
+    dirty_word = ld_relaxed(&p.ctl->dirty);
+  }
   unsigned int bar_target = P;
   bool alive = true;
   const int B = kBatched ? p.frames : 1;
@@ -881,7 +888,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   if (tid == 0) {
     s_layout[0] = s_layout[1] = 0;
     s_nrec = 0;
+    s_dirty = dirty_word;
   }
+  __syncthreads();  // maps empty, dirty flag shared
+  const bool dirty = s_dirty != 0u;
 
   // Recovery after a failed launch: empty the whole table first.
   if (dirty) {
@@ -900,10 +910,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   // once (their chunk ranks keep them apart).
   if (alive) {
 #ifdef PV_INSTRUMENT
-    __syncthreads();
     if (tid == 0 && cta < kStampCtas) g_p1_ns[cta][6] = global_timer_ns();
 #endif
-    __syncthreads();
     int buf = 0;
     for (; tb < end; tb += kThreads, buf ^= 1) {
 #ifdef PV_INSTRUMENT
@@ -1369,6 +1377,8 @@ __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned lon
 
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel(const KParams p) {
   __shared__ int s_flag;
+  __shared__ unsigned int s_dirty;
+  __shared__ unsigned int s_total;
   const unsigned int P = gridDim.x;
   const unsigned int tid = threadIdx.x;
   const unsigned int lane = tid & 31u;
@@ -1378,8 +1388,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel
   const long long nwarps = static_cast<long long>(P) * kWarps;
   const int K = p.K;
   const unsigned int M = static_cast<unsigned int>(p.max_voxels);
-  const unsigned int epoch = ld_relaxed(&p.ctl->epoch);
-  const unsigned int dirty = ld_relaxed(&p.ctl->dirty);
+  unsigned int epoch = 0;  // thread 0 alone reads the control block (one L2 line)
+  if (tid == 0) {
+    epoch = ld_relaxed(&p.ctl->epoch);
+    s_dirty = ld_relaxed(&p.ctl->dirty);
+  }
+  __syncthreads();
+  const bool dirty = s_dirty != 0u;
   unsigned int bar_target = P;
   bool alive = true;
 
@@ -1453,7 +1468,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel
 
   unsigned int V = 0;
   if (alive) {
-    const unsigned int total = ld_relaxed(&p.ctl->created);
+    if (tid == 0) s_total = ld_relaxed(&p.ctl->created);  // thread 0 alone: one L2 line
+    __syncthreads();
+    const unsigned int total = s_total;
     V = total < M ? total : M;
     // ---- phase U2: one warp per row: count, coordinates, zeros past the count.
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1570,6 +1587,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
   __shared__ unsigned int s_tile[kFlagUnroll][kWarps];
   __shared__ unsigned int s_tmp[kWarps + 1];
   __shared__ int s_flag;
+  __shared__ unsigned int s_dirty;
   __shared__ int s_hot;  // the hot table holds a voxel
 
   const unsigned int P = gridDim.x;
@@ -1584,8 +1602,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
   const long long begin = lmin(p.n, static_cast<long long>(cta) * p.chunk);
   const long long end = lmin(p.n, begin + p.chunk);
   const unsigned int M = static_cast<unsigned int>(p.max_voxels);
-  const unsigned int epoch = ld_relaxed(&p.ctl->epoch);
-  const unsigned int dirty = ld_relaxed(&p.ctl->dirty);
+  unsigned int epoch = 0;  // thread 0 alone reads the control block (one L2 line)
+  if (tid == 0) {
+    epoch = ld_relaxed(&p.ctl->epoch);
+    s_dirty = ld_relaxed(&p.ctl->dirty);
+  }
+  __syncthreads();
+  const bool dirty = s_dirty != 0u;
   unsigned int bar_target = P;
   bool alive = true;
 
