@@ -913,6 +913,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     if (tid == 0 && cta < kStampCtas) g_p1_ns[cta][6] = global_timer_ns();
 #endif
     int buf = 0;
+    int own_rs = -1;                  // one-tile chunk: the record this thread leads, if any
+    unsigned long long own_entry = 0;
     for (; tb < end; tb += kThreads, buf ^= 1) {
 #ifdef PV_INSTRUMENT
       const bool first_tile = tb == begin;
@@ -996,9 +998,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           const unsigned int room = cpts < static_cast<unsigned int>(K) ? static_cast<unsigned int>(K) - cpts : 0u;
           tm.off[h] = ((tot < room ? tot : room) << 16) | off;
           if (wants) {
-            const long long rj = begin + rbase + rincl - wants;
-            p.firsts[rj] = slot;  // the record's slot (firsts is rewritten after the barrier)
-            p.recs[rj] = make_entry(i, static_cast<unsigned int>(crank), tb + off, tot);
+            const unsigned long long ent = make_entry(i, static_cast<unsigned int>(crank), tb + off, tot);
+            if (multi) {
+              const long long rj = begin + rbase + rincl - wants;
+              p.firsts[rj] = slot;  // the record's slot (firsts is rewritten after the barrier)
+              p.recs[rj] = ent;
+            } else {  // one tile: the leader inserts its own record
+              own_rs = slot;
+              own_entry = ent;
+            }
           }
         }
       }
@@ -1018,8 +1026,18 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
 #endif
     const unsigned int nrec = s_nrec;
     // One record per thread at a time; the thread's next record is read
-    // while the current one's cascade runs.
-    {
+    // while the current one's cascade runs.  A one-tile chunk's leaders
+    // insert their own records, held in registers.
+    if (!multi) {
+      if (own_rs >= 0) {
+        uint4 h[kHead / 2];
+#pragma unroll
+        for (int t = 0; t < kHead / 2; ++t)
+          h[t] = __ldcg(reinterpret_cast<const uint4*>(p.lists + static_cast<size_t>(own_rs) * kHead) + t);
+        list_insert(list_of(p, own_rs), h, K, p.KT, own_entry, 0, static_cast<uint32_t>(begin),
+                    static_cast<uint32_t>(end - begin));
+      }
+    } else {
       unsigned int j0 = tid;
       int rs = j0 < nrec ? __ldcg(p.firsts + begin + j0) : -1;
       unsigned long long entry = j0 < nrec ? __ldcg(p.recs + begin + j0) : 0ull;
