@@ -87,6 +87,24 @@ def test_random_tiny_clouds():
         assert_parity(pts, r, v, K, M, table_mode=(2 if t % 3 == 0 else 0))
 
 
+def test_chunk_sizes_around_tile_boundaries():
+    # Each block owns ceil(N / blocks) points rounded up to a warp and sweeps
+    # them in 1024-point tiles from its own start, so tiles start anywhere and
+    # a chunk may end with a short tile.  Sizes that make the chunk one warp,
+    # exactly one tile, one tile and a warp, and two tiles and a warp; the
+    # points are KITTI-shaped returns repeated in sensor order, so pillars
+    # span tile and chunk boundaries.
+    P = synth.KITTI_PARAMS
+    base, _ = synth.make("kitti")
+    ctas = pv.query_plan(len(base), P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)["ctas"]
+    for want_chunk, n in [(32, 32 * ctas - 7), (1024, 1024 * ctas - 3), (1056, 1024 * ctas + 1),
+                          (2080, 2048 * ctas + 40)]:
+        plan = pv.query_plan(n, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+        assert plan["points_per_cta"] == want_chunk, (n, plan["points_per_cta"])
+        pts = np.tile(base, (n // len(base) + 1, 1))[:n]
+        assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+
+
 def test_determinism_repeats():
     pts, P = synth.make("kitti")
     ref = gpu_run(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
