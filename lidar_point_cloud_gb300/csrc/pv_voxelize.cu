@@ -101,6 +101,30 @@ struct Control {
   unsigned int pad[2];
 };
 
+// Division of n < 2^31 by a divisor 1 <= d < 2^31 fixed per call, as one
+// 64-bit multiply and a shift: with l = ceil(log2 d), s = 31 + l and
+// m = ceil(2^s / d), the error e = m d - 2^s is below d <= 2^l, so n e < 2^s
+// and floor(n m / 2^s) = floor(n / d); m <= 2^32, so n m fits 64 bits.
+struct FastDiv {
+  unsigned long long m;
+  unsigned int s;
+  unsigned int d;
+};
+
+__host__ __device__ __forceinline__ unsigned int fast_div(unsigned int n, const FastDiv& f) {
+  return static_cast<unsigned int>((static_cast<unsigned long long>(n) * f.m) >> f.s);
+}
+
+inline FastDiv make_fast_div(unsigned int d) {
+  unsigned int l = 0;
+  while ((1ull << l) < d) ++l;
+  FastDiv f;
+  f.s = 31 + l;
+  f.m = ((1ull << f.s) + d - 1) / d;
+  f.d = d;
+  return f;
+}
+
 struct KParams {
   const float4* points;
   long long n;
@@ -111,6 +135,9 @@ struct KParams {
   float g_xf, g_yf, g_zf;
   int g_x;
   int g_y;
+  FastDiv div_x;     // by g_x
+  FastDiv div_y;     // by g_y
+  FastDiv div_cells; // by cells (a batched id's frame)
   int K;             // max_points
   int KT;            // tail entries per slot (max_points rounded up to 4, less kHead; >= 0)
   int max_voxels;
@@ -1314,14 +1341,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           reinterpret_cast<uint4*>(L)[0] = e4;
           reinterpret_cast<uint4*>(L)[1] = e4;
         }
-        const int id = kBatched ? key % p.cells : key;  // the frame is the row's, not the id's
-        const int kxy = id / p.g_x;
+        const unsigned int ukey = static_cast<unsigned int>(key);
+        const int id = kBatched ? static_cast<int>(ukey - fast_div(ukey, p.div_cells) * static_cast<unsigned int>(p.cells))
+                                : key;  // the frame is the row's, not the id's
+        const int kxy = static_cast<int>(fast_div(static_cast<unsigned int>(id), p.div_x));
+        const int kz = static_cast<int>(fast_div(static_cast<unsigned int>(kxy), p.div_y));
         constexpr int cw = kBatched ? 4 : 3;  // (batch,) z, y, x
         int32_t* co = p.out_coords + cw * static_cast<size_t>(row);
         if (kBatched) co[0] = fb;
-        co[cw - 3] = kxy / p.g_y;  // 0 on a pillar grid
-        co[cw - 2] = kxy % p.g_y;
-        co[cw - 1] = id % p.g_x;
+        co[cw - 3] = kz;  // 0 on a pillar grid
+        co[cw - 2] = kxy - kz * p.g_y;
+        co[cw - 1] = id - kxy * p.g_x;
         p.out_counts[static_cast<size_t>(row)] = static_cast<int32_t>(cnt);
         if (p.hash_mode) p.keys[slot] = kNoKey;
       }
@@ -1505,11 +1535,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel
         p.out_voxels[static_cast<size_t>(r) * K + e] = z4;
       if (lane == 0) {
         const bool live = r < static_cast<long long>(V);
-        const int kxy = key / p.g_x;
+        const int kxy = static_cast<int>(fast_div(static_cast<unsigned int>(key), p.div_x));
+        const int kz = static_cast<int>(fast_div(static_cast<unsigned int>(kxy), p.div_y));
         p.out_counts[r] = static_cast<int32_t>(c);
-        p.out_coords[3 * r] = live ? kxy / p.g_y : 0;
-        p.out_coords[3 * r + 1] = live ? kxy % p.g_y : 0;
-        p.out_coords[3 * r + 2] = live ? key % p.g_x : 0;
+        p.out_coords[3 * r] = live ? kz : 0;
+        p.out_coords[3 * r + 1] = live ? kxy - kz * p.g_y : 0;
+        p.out_coords[3 * r + 2] = live ? key - kxy * p.g_x : 0;
         if (live) p.row_cnt[r] = 0u;
       }
     }
@@ -1862,10 +1893,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
         p.out_voxels[r] = make_float4(mean_of(A.s[0], A.count), mean_of(A.s[1], A.count),
                                       mean_of(A.s[2], A.count), mean_of(A.s[3], A.count));
         const int key = p.hash_mode ? __ldcg(p.keys + slot) : slot;
-        const int kxy = key / p.g_x;
-        p.out_coords[3 * r] = kxy / p.g_y;
-        p.out_coords[3 * r + 1] = kxy % p.g_y;
-        p.out_coords[3 * r + 2] = key % p.g_x;
+        const int kxy = static_cast<int>(fast_div(static_cast<unsigned int>(key), p.div_x));
+        const int kz = static_cast<int>(fast_div(static_cast<unsigned int>(kxy), p.div_y));
+        p.out_coords[3 * r] = kz;
+        p.out_coords[3 * r + 1] = kxy - kz * p.g_y;
+        p.out_coords[3 * r + 2] = key - kxy * p.g_x;
         p.out_counts[r] = static_cast<int32_t>(A.count);
       }
       a4[0] = z4;
@@ -2238,6 +2270,8 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.g_zf = static_cast<float>(pl.g[2]);
   kp.g_x = static_cast<int>(pl.g[0]);
   kp.g_y = static_cast<int>(pl.g[1]);
+  kp.div_x = make_fast_div(static_cast<unsigned int>(pl.g[0]));
+  kp.div_y = make_fast_div(static_cast<unsigned int>(pl.g[1]));
   kp.K = K;
   kp.KT = pl.KT;
   kp.max_voxels = M;
@@ -2263,6 +2297,7 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.row_cnt_cap = ws->row_cnt_cap;
   kp.frames = pl.frames;
   kp.cells = static_cast<int>(pl.cells);
+  kp.div_cells = make_fast_div(static_cast<unsigned int>(std::max<int64_t>(1, pl.cells)));
   kp.frame_cnt = ws->counts + kMaxCtas;
   kp.acc = ws->acc;
   kp.acc_cap = ws->acc_cap;
