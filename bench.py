@@ -100,13 +100,20 @@ HOST_SIDE_MARKER = b"// --------------------------------------------------------
 def kernel_sha(kernel="pv_voxelize_kernel"):
     """SHA-256 of the device code of the source file that holds the kernel:
     everything before the file's host-side marker (launch, planning and ABI
-    code after it can change without changing what a profile measured)."""
+    code after it can change without changing what a profile measured), with
+    line comments, trailing blanks and empty lines left out (comment edits
+    do not change the kernel either)."""
     name = "pv_fps.cu" if kernel == "pv_fps_kernel" else "pv_voxelize.cu"
     src = os.path.join(ROOT, "lidar_point_cloud_gb300", "csrc", name)
     with open(src, "rb") as f:
         text = f.read()
     cut = text.find(HOST_SIDE_MARKER)
-    return hashlib.sha256(text[:cut] if cut >= 0 else text).hexdigest()
+    code = []
+    for line in (text[:cut] if cut >= 0 else text).split(b"\n"):
+        line = line.split(b"//", 1)[0].rstrip()
+        if line:
+            code.append(line)
+    return hashlib.sha256(b"\n".join(code)).hexdigest()
 
 
 def profiled_traffic(workload, kernel="pv_voxelize_kernel"):

@@ -16,18 +16,23 @@
 //     pillar (warp match + a small open-addressing map), which gives every
 //     point its rank among the tile's points of its pillar and lays the tile
 //     out group by group in a per-tile buffer.  Only each group's first point
-//     (its leader) touches the pillar's slot in an L2-resident table: the
-//     slot keeps the max_points smallest leader indices with atomicMin (entry
-//     k keeps the minimum of what reaches it and passes the larger value on,
-//     so it ends as the (k+1)-th smallest whatever order the inserts came
-//     in).  Entry 0 is the pillar's first point (the page's atomicCAS claim
-//     plus an atomicMin of the first index), and the pillar's points in index
-//     order are its groups concatenated in entry order.  The table is
+//     (its leader) touches the pillar's slot in an L2-resident table.  For
+//     8..32 points a pillar the slot is an append list: a count taken with
+//     atomicAdd gives the group its position, an atomicMin keeps the lowest
+//     leader (the pillar's first point: the page's atomicCAS claim plus an
+//     atomicMin of the first index), and the gather sorts the entries; a
+//     pillar with more groups than the slot holds spills into an overflow
+//     list of the other kind.  Otherwise the slot keeps the max_points
+//     smallest leader indices sorted with atomicMin (entry k keeps the
+//     minimum of what reaches it and passes the larger value on, so it ends
+//     as the (k+1)-th smallest whatever order the inserts came in), entry 0
+//     being the first point.  The pillar's points in index order are its
+//     groups concatenated in leader order.  The table is
 //     direct-mapped (one slot per grid cell) when the grid is small enough,
 //     else open addressing with linear probing (the page's hash table, "A
 //     hash table instead of a sort"), probes bounded by the table size;
 //   * phase 2: each block owns a contiguous range of point indices.  A point
-//     is the first of its pillar iff its index sits in entry 0 of its slot.
+//     is the first of its pillar iff its index is its slot's lowest leader.
 //     Blocks compact their first points in index order and publish the
 //     count; after the second barrier every block scans all counts into
 //     shared memory, so every pillar's rank (its order of first appearance)
@@ -98,7 +103,8 @@ struct Control {
   unsigned int dirty;   // 1: the table may hold stale entries
   unsigned int epoch;   // launch number
   unsigned int created; // unordered mode: pillars created in the running launch
-  unsigned int pad[2];
+  unsigned int pool;    // append lists: overflow lists handed out in the running launch
+  unsigned int pad;
 };
 
 // Division of n < 2^31 by a divisor 1 <= d < 2^31 fixed per call, as one
@@ -140,6 +146,9 @@ struct KParams {
   FastDiv div_cells; // by cells (a batched id's frame)
   int K;             // max_points
   int KT;            // tail entries per slot (max_points rounded up to 4, less kHead; >= 0)
+  int append;        // 1: append lists (kAppendMinK <= max_points <= 32), 0: sorted lists
+  unsigned long long* pool;  // append lists: overflow lists, kHead + KT words each
+  unsigned int pool_n;       // overflow lists available
   int max_voxels;
   int hash_mode;
   unsigned int bar_extra;  // test hook: extra arrivals the first barrier waits for
@@ -463,6 +472,22 @@ __device__ __forceinline__ unsigned long long ull_of(uint32_t lo, uint32_t hi) {
   return (static_cast<unsigned long long>(hi) << 32) | lo;
 }
 
+// Append lists (8 <= max_points <= 32).  A slot's S = kHead + KT words:
+// word 0 is (lowest leader << 32) | ~count, words 1 .. S-2 hold the first
+// S-2 entries in arrival order, word S-1 the index of the slot's overflow
+// list.  All-ones is the empty slot (count 0, no leader, no overflow list).
+// An insert is one atomicAdd on the count (its arrival index) and one
+// atomicMin on the lowest leader, then a plain store of the entry: no
+// cascade.  Entries past S-2 go, sorted by the cascade of list_insert, into
+// an overflow list taken from a pool by the slot's first overflowing entry;
+// the later ones wait (bounded) for its index.  The gather sorts the stored
+// entries in a warp and merges the overflow list in.
+constexpr int kAppendMinK = 8;
+
+__device__ __forceinline__ unsigned long long* slot_word(unsigned long long* head, unsigned long long* tail, int w) {
+  return w < kHead ? head + w : tail + (w - kHead);
+}
+
 // List entry: (leader index << 32) | (chunk rank << 22) | (d << 11) | size,
 // where the group's rows start in tile_rows at leader index + d (d signed,
 // 11 bits: a group lies inside its 1024-point tile) and the chunk rank is
@@ -549,6 +574,52 @@ __device__ __forceinline__ void list_insert(const ListRef& L, const uint4 (&h)[k
   atomicAdd(&g_insert_stats[1], n_atomics);
   atomicMax(&g_insert_stats[3], n_atomics);
 #endif
+}
+
+// Append-list insert of entry x into slot L (see kAppendMinK).  cbase/cspan:
+// this block's chunk (for the overflow list's cascade).
+__device__ void append_insert(const KParams& p, const ListRef& L, unsigned long long x, uint32_t cbase,
+                              uint32_t cspan) {
+  const int S = kHead + p.KT;
+  unsigned int* w0 = reinterpret_cast<unsigned int*>(L.head);
+  const unsigned int j = ~atomicAdd(w0, 0xFFFFFFFFu);  // the count is kept complemented
+  atomicMin(w0 + 1, static_cast<unsigned int>(x >> 32));
+  if (j < static_cast<unsigned int>(S - 2)) {
+    *slot_word(L.head, L.tail, 1 + static_cast<int>(j)) = x;
+    return;
+  }
+  // Overflow: the first overflowing entry takes a list from the pool and
+  // publishes its index in word S-1; the others wait for it (bounded).
+  unsigned long long* ow = slot_word(L.head, L.tail, S - 1);
+  unsigned long long idx = kEmpty64;
+  if (j == static_cast<unsigned int>(S - 2)) {
+    const unsigned int got = atomicAdd(&p.ctl->pool, 1u);
+    if (got >= p.pool_n) {
+      atomicMin(&p.ctl->err, PV_ERR_CAPACITY);
+      return;
+    }
+    idx = got;
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ow), "l"(idx) : "memory");
+  } else {
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(idx) : "l"(ow) : "memory");
+    if (idx == kEmpty64) {
+      const unsigned long long t0 = global_timer_ns();
+      do {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          atomicMin(&p.ctl->err, PV_ERR_TIMEOUT);
+          return;
+        }
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(idx) : "l"(ow) : "memory");
+      } while (idx == kEmpty64);
+    }
+    if (idx >= p.pool_n) return;  // the taker ran out of pool and recorded it
+  }
+  unsigned long long* base = p.pool + idx * static_cast<unsigned long long>(S);
+  const ListRef O{base, base + kHead};
+  uint4 h[kHead / 2];
+#pragma unroll
+  for (int t = 0; t < kHead / 2; ++t) h[t] = __ldcg(reinterpret_cast<const uint4*>(base) + t);
+  list_insert(O, h, p.K, p.KT, x, 0, cbase, cspan);
 }
 
 // ------------------------------------------------------------ block tiles
@@ -693,6 +764,39 @@ __device__ __forceinline__ Head read_head(const KParams& p, const unsigned long 
     a = __ldcg(reinterpret_cast<const uint4*>(L));
     b = __ldcg(reinterpret_cast<const uint4*>(L) + 1);
   }
+  if (p.append) {
+    // Word 0: the count (complemented); words 1..3: the first three entries
+    // in arrival order, sorted here.  Served from the head only when the
+    // slot holds at most three entries.
+    const unsigned int cnt = ~a.x;
+    unsigned long long e0 = ull_of(a.z, a.w), e1 = ull_of(b.x, b.y), e2 = ull_of(b.z, b.w);
+    if (cnt < 3u) e2 = kEmpty64;
+    if (cnt < 2u) e1 = kEmpty64;
+    if (cnt < 1u) e0 = kEmpty64;
+    const unsigned long long m01 = e0 < e1 ? e0 : e1, x01 = e0 < e1 ? e1 : e0;
+    const unsigned long long m12 = x01 < e2 ? x01 : e2, x12 = x01 < e2 ? e2 : x01;
+    h.e[0] = m01 < m12 ? m01 : m12;
+    h.e[1] = m01 < m12 ? m12 : m01;
+    h.e[2] = x12;
+    h.e[3] = kEmpty64;
+    unsigned int cum = 0;
+    int g = 0;
+    bool filled = false;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const bool good = h.e[j] != kEmpty64 && (h.e[j] >> 32) < static_cast<unsigned long long>(p.n);
+      if (!filled && g == j && good) {
+        cum += static_cast<unsigned int>(h.e[j]) & 2047u;
+        g = j + 1;
+        if (cum >= static_cast<unsigned int>(p.K)) filled = true;
+      }
+    }
+    h.ng = g;
+    h.filled = filled;
+    h.few = g > 0 && cnt <= 3u && (filled || static_cast<unsigned int>(g) == cnt);
+    h.n = filled ? static_cast<unsigned int>(p.K) : cum;
+    return h;
+  }
   h.e[0] = ull_of(a.x, a.y);
   h.e[1] = ull_of(a.z, a.w);
   h.e[2] = ull_of(b.x, b.y);
@@ -819,6 +923,120 @@ __device__ unsigned int emit_groups(const KParams& p, const ListRef& L, float4* 
     if (chunk_raw != kEmpty64) *L.at(g0 + lane) = kEmpty64;
   }
   for (unsigned int e = written + lane; e < static_cast<unsigned int>(K); e += 32) orow[e] = z4;
+  return written;
+}
+
+// Empties an append slot, and its overflow list if it has one.  All 32
+// lanes call it with the same slot.
+__device__ void app_clear(const KParams& p, const ListRef& L, unsigned int lane) {
+  const int S = kHead + p.KT;
+  const unsigned long long ow = __ldcg(slot_word(L.head, L.tail, S - 1));
+  if (ow < p.pool_n) {
+    unsigned long long* base = p.pool + ow * static_cast<unsigned long long>(S);
+    for (int w = static_cast<int>(lane); w < S; w += 32) base[w] = kEmpty64;
+  }
+  __syncwarp();
+  for (int w = static_cast<int>(lane); w < S; w += 32) *slot_word(L.head, L.tail, w) = kEmpty64;
+}
+
+// Writes the output row of an append-list pillar that is not served from
+// its head: lane l reads stored entry l, the warp sorts them by leader
+// (bitonic), merges in the slot's sorted overflow list if it has one (the
+// first 32 of the union, through a per-warp shared buffer), and copies the
+// first max_points points as emit_groups does; empties the slot.  All 32
+// lanes call it with the same arguments (max_points <= 32).
+__device__ unsigned int emit_app(const KParams& p, const ListRef& L, float4* orow, int K, unsigned int lane,
+                                 unsigned long long* wbuf, bool* stale) {
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int S = kHead + p.KT;
+  const unsigned int cnt = ~__ldcg(reinterpret_cast<const unsigned int*>(L.head));
+  const int nent = cnt < static_cast<unsigned int>(S - 2) ? static_cast<int>(cnt) : S - 2;
+  unsigned long long ent = static_cast<int>(lane) < nent ? __ldcg(slot_word(L.head, L.tail, 1 + lane)) : kEmpty64;
+  const unsigned long long ow = cnt > static_cast<unsigned int>(S - 2) ? __ldcg(slot_word(L.head, L.tail, S - 1)) : kEmpty64;
+  if (ent != kEmpty64 && (ent >> 32) >= static_cast<unsigned long long>(p.n)) {
+    ent = kEmpty64;
+    *stale = true;
+  }
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, ent, j);
+      const bool up = (lane & static_cast<unsigned int>(k)) == 0u;
+      const bool lower = (lane & static_cast<unsigned int>(j)) == 0u;
+      const unsigned long long mn = ent < o ? ent : o, mx = ent < o ? o : ent;
+      ent = (lower == up) ? mn : mx;
+    }
+  }
+  if (cnt > static_cast<unsigned int>(S - 2)) {
+    // The overflow list holds the smallest of the entries that did not fit,
+    // ascending in positions 0 .. max_points-1.
+    unsigned long long ov = kEmpty64;
+    if (ow < p.pool_n) {
+      const unsigned long long* base = p.pool + ow * static_cast<unsigned long long>(S);
+      ov = static_cast<int>(lane) < K ? __ldcg(slot_word(const_cast<unsigned long long*>(base),
+                                                         const_cast<unsigned long long*>(base) + kHead, lane))
+                                      : kEmpty64;
+      if (ov != kEmpty64 && (ov >> 32) >= static_cast<unsigned long long>(p.n)) {
+        ov = kEmpty64;
+        *stale = true;
+      }
+    } else {
+      *stale = true;  // a count past the stored entries without an overflow list
+    }
+    // Rank of each element in the union (leaders are distinct): its own
+    // index plus the number of the other list's elements below it.
+    int ra = 0, rb = 0;  // elements of the other list below ent / below ov
+#pragma unroll
+    for (int step = 16; step >= 1; step >>= 1) {
+      const unsigned long long ob = __shfl_sync(0xffffffffu, ov, ra + step - 1);
+      if (ob < ent) ra += step;
+      const unsigned long long oa = __shfl_sync(0xffffffffu, ent, rb + step - 1);
+      if (oa < ov) rb += step;
+    }
+    {
+      const unsigned long long ob = __shfl_sync(0xffffffffu, ov, ra < 32 ? ra : 31);
+      if (ra < 32 && ob < ent) ++ra;
+      const unsigned long long oa = __shfl_sync(0xffffffffu, ent, rb < 32 ? rb : 31);
+      if (rb < 32 && oa < ov) ++rb;
+    }
+    const int pa = static_cast<int>(lane) + ra, pb = static_cast<int>(lane) + rb;
+    if (ent != kEmpty64 && pa < 32) wbuf[pa] = ent;
+    if (ov != kEmpty64 && pb < 32) wbuf[pb] = ov;
+    const unsigned int na = __popc(__ballot_sync(0xffffffffu, ent != kEmpty64));
+    const unsigned int nb = __popc(__ballot_sync(0xffffffffu, ov != kEmpty64));
+    __syncwarp();
+    ent = lane < na + nb ? wbuf[lane] : kEmpty64;
+    __syncwarp();
+  }
+  const unsigned int present = __ballot_sync(0xffffffffu, ent != kEmpty64);
+  const int G = __popc(present);
+  const unsigned int size = ent != kEmpty64 ? (static_cast<unsigned int>(ent) & 2047u) : 0u;
+  unsigned int incl = size;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= static_cast<unsigned int>(o)) incl += y;
+  }
+  const int gstart = static_cast<int>(incl - size);
+  const unsigned int all = __shfl_sync(0xffffffffu, incl, 31);
+  const unsigned int written = all < static_cast<unsigned int>(K) ? all : static_cast<unsigned int>(K);
+  const int e = static_cast<int>(lane);
+  int g = 0;
+#pragma unroll
+  for (int step = 16; step >= 1; step >>= 1) {
+    const int jj = g + step;
+    const int st = __shfl_sync(0xffffffffu, gstart, jj < 32 ? jj : 31);
+    if (jj < G && st <= e) g = jj;
+  }
+  const unsigned long long ge = __shfl_sync(0xffffffffu, ent, g);
+  const int gs = __shfl_sync(0xffffffffu, gstart, g);
+  if (e < K) {
+    float4 row = z4;
+    if (static_cast<unsigned int>(e) < written) row = __ldcg(p.tile_rows + entry_row(ge) + (e - gs));
+    orow[e] = row;
+  }
+  app_clear(p, L, lane);
   return written;
 }
 
@@ -1057,12 +1275,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     // insert their own records, held in registers.
     if (!multi) {
       if (own_rs >= 0) {
-        uint4 h[kHead / 2];
+        if (p.append) {
+          append_insert(p, list_of(p, own_rs), own_entry, static_cast<uint32_t>(begin),
+                        static_cast<uint32_t>(end - begin));
+        } else {
+          uint4 h[kHead / 2];
 #pragma unroll
-        for (int t = 0; t < kHead / 2; ++t)
-          h[t] = __ldcg(reinterpret_cast<const uint4*>(p.lists + static_cast<size_t>(own_rs) * kHead) + t);
-        list_insert(list_of(p, own_rs), h, K, p.KT, own_entry, 0, static_cast<uint32_t>(begin),
-                    static_cast<uint32_t>(end - begin));
+          for (int t = 0; t < kHead / 2; ++t)
+            h[t] = __ldcg(reinterpret_cast<const uint4*>(p.lists + static_cast<size_t>(own_rs) * kHead) + t);
+          list_insert(list_of(p, own_rs), h, K, p.KT, own_entry, 0, static_cast<uint32_t>(begin),
+                      static_cast<uint32_t>(end - begin));
+        }
       }
     } else {
       unsigned int j0 = tid;
@@ -1072,12 +1295,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         const unsigned int j1 = j0 + kThreads;
         const int rs1 = j1 < nrec ? __ldcg(p.firsts + begin + j1) : -1;
         const unsigned long long entry1 = j1 < nrec ? __ldcg(p.recs + begin + j1) : 0ull;
-        uint4 h[kHead / 2];
+        if (p.append) {
+          append_insert(p, list_of(p, rs), entry, static_cast<uint32_t>(begin), static_cast<uint32_t>(end - begin));
+        } else {
+          uint4 h[kHead / 2];
 #pragma unroll
-        for (int t = 0; t < kHead / 2; ++t)
-          h[t] = __ldcg(reinterpret_cast<const uint4*>(p.lists + static_cast<size_t>(rs) * kHead) + t);
-        list_insert(list_of(p, rs), h, K, p.KT, entry, entry_crank(entry),
-                    static_cast<uint32_t>(begin), static_cast<uint32_t>(end - begin));
+          for (int t = 0; t < kHead / 2; ++t)
+            h[t] = __ldcg(reinterpret_cast<const uint4*>(p.lists + static_cast<size_t>(rs) * kHead) + t);
+          list_insert(list_of(p, rs), h, K, p.KT, entry, entry_crank(entry),
+                      static_cast<uint32_t>(begin), static_cast<uint32_t>(end - begin));
+        }
         rs = rs1;
         entry = entry1;
       }
@@ -1226,6 +1453,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     // warp kEmitPer pillars at a time; the others are emitted one by one
     // from their whole list.
     bool stale = false;
+    unsigned long long* wbuf = reinterpret_cast<unsigned long long*>(s_dyn) + warp * 32;  // append lists' merge buffer
     // (Counts of pillars and warps fit 32 bits: N < 2^29, at most 1024 x 32 warps.)
     const unsigned int dropped = kBatched ? s_dcum[B] : total - V;
     const unsigned int nw = static_cast<unsigned int>(nwarps), gw = static_cast<unsigned int>(gwarp);
@@ -1275,7 +1503,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         if (drop && p.hash_mode) p.keys[slot] = kNoKey;
         for (unsigned int m = __ballot_sync(0xffffffffu, drop && !short_drop); m != 0u; m &= m - 1u) {
           const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, __ffs(m) - 1));
-          for (int e = static_cast<int>(lane); e < K; e += 32) *Lu.at(e) = kEmpty64;
+          if (p.append)
+            app_clear(p, Lu, lane);
+          else
+            for (int e = static_cast<int>(lane); e < K; e += 32) *Lu.at(e) = kEmpty64;
         }
       }
 
@@ -1331,7 +1562,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         const int u = __ffs(m) - 1;
         const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, u));
         const long long row_u = __shfl_sync(0xffffffffu, row, u);
-        const unsigned int w = emit_groups(p, Lu, p.out_voxels + static_cast<size_t>(row_u) * K, K, lane, &stale);
+        float4* orow_u = p.out_voxels + static_cast<size_t>(row_u) * K;
+        const unsigned int w = p.append ? emit_app(p, Lu, orow_u, K, lane, wbuf, &stale)
+                                        : emit_groups(p, Lu, orow_u, K, lane, &stale);
         if (static_cast<int>(lane) == u) cnt = w;
       }
       if (valid) {
@@ -1386,6 +1619,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       p.ctl->err = 0;
       p.ctl->bar = 0;
       p.ctl->done = 0;
+      p.ctl->pool = 0;
       const unsigned int next = epoch + 1;
       p.ctl->epoch = next == 0 ? 1u : next;
     }
@@ -1981,6 +2215,8 @@ struct Plan {
   int mode;
   int64_t T;
   int KT;             // tail entries per slot
+  int append = 0;     // append lists (ordered voxelization, kAppendMinK <= max_points <= 32)
+  int64_t pool_n = 0; // append lists: overflow lists in the pool
   int ctas;
   int64_t chunk;
   unsigned int mask;
@@ -2094,7 +2330,13 @@ int make_plan(int64_t N, const float range[6], const float vsize[3], int K, int 
     if (pl->T > (int64_t(1) << 30)) return PV_ERR_INVALID;  // slots stay below the leader bit
     pl->mask = static_cast<unsigned int>(pl->T - 1);
   }
-  pl->list_words = static_cast<size_t>(pl->T) * (kHead + pl->KT);
+  // Append lists need an overflow pool: a slot overflows only with more
+  // than S - 2 entries, each at least one point, so N / (S - 1) + 1 lists
+  // always suffice.
+  const int S = kHead + pl->KT;
+  pl->append = (!pl->unordered && !pl->downsample && K >= kAppendMinK && K <= 32) ? 1 : 0;
+  pl->pool_n = pl->append ? N / (S - 1) + 1 : 0;
+  pl->list_words = static_cast<size_t>(pl->T) * S + static_cast<size_t>(pl->pool_n) * S;
   pl->key_words = mode == 2 ? static_cast<size_t>(pl->T) : 0;
   const int per_sm = o.ctas_per_sm ? std::min(o.ctas_per_sm, dev.blocks_per_sm) : dev.blocks_per_sm;
   // The count scan after the second barrier takes one count per thread.
@@ -2274,6 +2516,9 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.div_y = make_fast_div(static_cast<unsigned int>(pl.g[1]));
   kp.K = K;
   kp.KT = pl.KT;
+  kp.append = pl.append;
+  kp.pool = ws->lists + static_cast<size_t>(pl.T) * (kHead + pl.KT);
+  kp.pool_n = static_cast<unsigned int>(pl.pool_n);
   kp.max_voxels = M;
   kp.hash_mode = pl.mode == 2 ? 1 : 0;
   kp.bar_extra = pl.stall;
@@ -2428,7 +2673,8 @@ constexpr size_t kStaticSlots = size_t(1) << kStaticTableLog2;
 constexpr size_t kStaticOffCounts = 256;
 constexpr size_t kStaticOffKeys = kStaticOffCounts + 4 * kMaxCtas;
 constexpr size_t kStaticOffLists = kStaticOffKeys + 4 * kStaticSlots;
-constexpr size_t kStaticListWords = kStaticSlots * kStaticMaxK;  // 64-bit entries
+constexpr size_t kStaticPoolWords = 40960;  // append lists' overflow pool: (32768 / 7 + 1) x 8 words at most
+constexpr size_t kStaticListWords = kStaticSlots * kStaticMaxK + kStaticPoolWords;  // 64-bit entries
 constexpr size_t kStaticOffRows = kStaticOffLists + 8 * kStaticListWords;
 constexpr size_t kStaticOffRecs = kStaticOffRows + 16 * static_cast<size_t>(kStaticMaxPoints);
 constexpr size_t kStaticOffPoints = kStaticOffRecs + 8 * static_cast<size_t>(kStaticMaxPoints);

@@ -49,7 +49,8 @@ def test_reference_line_has_every_contract_key(op, workload):
 
 def test_profile_lookup_keys_on_device_code(tmp_path, monkeypatch):
     # A committed summary names the SHA-256 of the kernel source up to its
-    # host-side marker: host edits keep the summary, device edits void it.
+    # host-side marker, comments left out: host edits and comment edits keep
+    # the summary, device-code edits void it.
     src_dir = tmp_path / "lidar_point_cloud_gb300" / "csrc"
     src_dir.mkdir(parents=True)
     prof = tmp_path / "profiles"
@@ -64,7 +65,9 @@ def test_profile_lookup_keys_on_device_code(tmp_path, monkeypatch):
         f"# probe\n\n- dram_bytes_per_launch: `1234`\n- kernel_source_sha256: `{sha}`\n")
     assert bench.profiled_traffic("probe") == 1234
     cut = text.index(bench.HOST_SIDE_MARKER)
-    (src_dir / "pv_voxelize.cu").write_bytes(text + b"\n// a host-side edit\n")
+    (src_dir / "pv_voxelize.cu").write_bytes(text + b"\nstatic int host_side_edit = 0;\n")
     assert bench.profiled_traffic("probe") == 1234
-    (src_dir / "pv_voxelize.cu").write_bytes(text[:cut] + b"// a device-side edit\n" + text[cut:])
+    (src_dir / "pv_voxelize.cu").write_bytes(text[:cut] + b"// a comment in the device code\n" + text[cut:])
+    assert bench.profiled_traffic("probe") == 1234
+    (src_dir / "pv_voxelize.cu").write_bytes(text[:cut] + b"static __device__ int device_side_edit;\n" + text[cut:])
     assert bench.profiled_traffic("probe") is None
