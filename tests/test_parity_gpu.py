@@ -160,10 +160,11 @@ def hot_cloud(n, hot_pillars, hot_frac, seed):
     return pts[rng.permutation(n)]
 
 
-@pytest.mark.parametrize("K", [32, 64, 200, 1024])
+@pytest.mark.parametrize("K", [8, 20, 32, 64, 200, 1024])
 def test_hot_pillars_large_caps_twice(K):
     # Most groups of the hot pillars have max_points points before them and are
     # dropped; a second call checks that the first left no list entry behind.
+    # With 8..32 points a pillar the hot pillars overflow their append slots.
     pts = hot_cloud(600_000, 8, 0.6, 31)
     for _ in range(2):
         assert_parity(pts, KR, KV, K, 2000)
@@ -178,7 +179,8 @@ def test_chunk_point_counter_wraps(K):
         assert_parity(pts, KR, KV, K, 500)
 
 
-@pytest.mark.parametrize("K,M", [(1, 1), (1, 16000), (32, 1), (5, 500), (33, 2000), (64, 3000), (100, 700)])
+@pytest.mark.parametrize("K,M", [(1, 1), (1, 16000), (32, 1), (5, 500), (8, 300), (20, 4000), (33, 2000),
+                                 (64, 3000), (100, 700)])
 def test_caps(K, M):
     pts, P = synth.make("kitti")
     assert_parity(pts, P.point_cloud_range, P.voxel_size, K, M)
