@@ -743,11 +743,13 @@ __device__ __forceinline__ int slot_of_rank(const KParams& p, const unsigned int
   return __ldcg(p.firsts + static_cast<long long>(lo) * p.chunk + (r - s_prefix[lo]));
 }
 
-// The first four positions of a pillar's list, as one lane reads them.
+// The head row of a pillar's slot, as one lane reads it: a sorted list's
+// first four entries, or an append list's first three entries sorted here.
 // few: the pillar's points all come from groups among them: either the list
-// ends there (a group is missing after ng present ones and the groups hold
-// fewer than max_points points: a needed group is never missing before
-// another, so nothing follows) or the first ng groups already hold
+// ends there (a sorted list: a group is missing after ng present ones and
+// the groups hold fewer than max_points points, and a needed group is never
+// missing before another, so nothing follows; an append list: it holds at
+// most three entries, all present) or the first ng groups already hold
 // max_points points (filled; unused entries may then follow anywhere).
 struct Head {
   unsigned long long e[4];
