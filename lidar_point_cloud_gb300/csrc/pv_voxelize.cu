@@ -76,7 +76,7 @@ static_assert(kWarps <= 32 && kWarps % 16 == 0, "warp 0 scans one value per warp
 constexpr int kMinBlocksPerSM = 1024 / kThreads;
 constexpr int kMaxCtas = 1024;             // blocks per launch (prefix lives in shared memory)
 static_assert(kMaxCtas < 0x10000, "finished blocks are counted in 16 bits");
-constexpr int kFlagUnroll = 4;             // block-wide tiles in flight when flagging
+constexpr int kFlagUnroll = 8;             // block-wide tiles in flight when flagging
 #ifndef PV_HEAD_ENTRIES
 #define PV_HEAD_ENTRIES 4
 #endif
@@ -594,12 +594,14 @@ __device__ void append_insert(const KParams& p, const ListRef& L, unsigned long 
   unsigned long long idx = kEmpty64;
   if (j == static_cast<unsigned int>(S - 2)) {
     const unsigned int got = atomicAdd(&p.ctl->pool, 1u);
+    idx = got;
+    // Published even when it is out of range (the pool is exhausted), so
+    // that the waiters leave at once through their range check.
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ow), "l"(idx) : "memory");
     if (got >= p.pool_n) {
       atomicMin(&p.ctl->err, PV_ERR_CAPACITY);
       return;
     }
-    idx = got;
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ow), "l"(idx) : "memory");
   } else {
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(idx) : "l"(ow) : "memory");
     if (idx == kEmpty64) {
@@ -643,6 +645,11 @@ constexpr int kChunkProbes = PV_CHUNK_PROBES;  // a full chunk map costs this ma
 constexpr int kMapBytes = kTileHash * kWarps + kTileHash * 4 + kTileHash * 4;
 constexpr int kDynSmem = 2 * kMapBytes + 2 * 4 * kChunkHash;
 static_assert(kMapBytes % 16 == 0, "maps stay 16-byte aligned");
+// After phase 1 the same shared memory holds the gather's per-warp merge
+// buffers (32 entries each) and the block's queue of long lists.
+constexpr unsigned int kQueueCap = kDynSmem / 8 - kWarps * 32;
+constexpr unsigned int kQueueDrop = 0xFFFFFFFFu;  // queue row of a list past the budget (emptied only)
+constexpr int64_t kQueueMinRowsPerWarp = 8;        // rows per warp from which the gather queues long lists
 
 struct TileMap {
   unsigned int* cnt;         // [kTileHash][kWarps / 4] packed byte counters
@@ -930,15 +937,18 @@ __device__ unsigned int emit_groups(const KParams& p, const ListRef& L, float4* 
 
 // Empties an append slot, and its overflow list if it has one.  All 32
 // lanes call it with the same slot.
-__device__ void app_clear(const KParams& p, const ListRef& L, unsigned int lane) {
+__device__ void app_clear_with(const KParams& p, const ListRef& L, unsigned int lane, unsigned long long ow) {
   const int S = kHead + p.KT;
-  const unsigned long long ow = __ldcg(slot_word(L.head, L.tail, S - 1));
   if (ow < p.pool_n) {
     unsigned long long* base = p.pool + ow * static_cast<unsigned long long>(S);
     for (int w = static_cast<int>(lane); w < S; w += 32) base[w] = kEmpty64;
   }
   __syncwarp();
   for (int w = static_cast<int>(lane); w < S; w += 32) *slot_word(L.head, L.tail, w) = kEmpty64;
+}
+
+__device__ void app_clear(const KParams& p, const ListRef& L, unsigned int lane) {
+  app_clear_with(p, L, lane, __ldcg(slot_word(L.head, L.tail, kHead + p.KT - 1)));
 }
 
 // Writes the output row of an append-list pillar that is not served from
@@ -951,10 +961,17 @@ __device__ unsigned int emit_app(const KParams& p, const ListRef& L, float4* oro
                                  unsigned long long* wbuf, bool* stale) {
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   const int S = kHead + p.KT;
-  const unsigned int cnt = ~__ldcg(reinterpret_cast<const unsigned int*>(L.head));
+  // Lane w reads word w of the slot (one round trip for the count, the
+  // stored entries and the overflow index); entry j moves to lane j.
+  const unsigned long long word = static_cast<int>(lane) < S ? __ldcg(slot_word(L.head, L.tail, lane)) : kEmpty64;
+  const unsigned int cnt = ~static_cast<unsigned int>(__shfl_sync(0xffffffffu, static_cast<unsigned int>(word), 0));
   const int nent = cnt < static_cast<unsigned int>(S - 2) ? static_cast<int>(cnt) : S - 2;
-  unsigned long long ent = static_cast<int>(lane) < nent ? __ldcg(slot_word(L.head, L.tail, 1 + lane)) : kEmpty64;
-  const unsigned long long ow = cnt > static_cast<unsigned int>(S - 2) ? __ldcg(slot_word(L.head, L.tail, S - 1)) : kEmpty64;
+  const unsigned long long next = (static_cast<unsigned long long>(__shfl_down_sync(0xffffffffu, static_cast<unsigned int>(word >> 32), 1)) << 32) |
+                                  __shfl_down_sync(0xffffffffu, static_cast<unsigned int>(word), 1);
+  unsigned long long ent = static_cast<int>(lane) < nent ? next : kEmpty64;
+  const unsigned long long owl = (static_cast<unsigned long long>(__shfl_sync(0xffffffffu, static_cast<unsigned int>(word >> 32), S - 1)) << 32) |
+                                 __shfl_sync(0xffffffffu, static_cast<unsigned int>(word), S - 1);
+  const unsigned long long ow = cnt > static_cast<unsigned int>(S - 2) ? owl : kEmpty64;
   if (ent != kEmpty64 && (ent >> 32) >= static_cast<unsigned long long>(p.n)) {
     ent = kEmpty64;
     *stale = true;
@@ -1038,7 +1055,7 @@ __device__ unsigned int emit_app(const KParams& p, const ListRef& L, float4* oro
     if (static_cast<unsigned int>(e) < written) row = __ldcg(p.tile_rows + entry_row(ge) + (e - gs));
     orow[e] = row;
   }
-  app_clear(p, L, lane);
+  app_clear_with(p, L, lane, owl);
   return written;
 }
 
@@ -1062,7 +1079,7 @@ __device__ void reset_tables(const KParams& p, size_t gtid, size_t gthreads) {
 // NF = 1: one cloud (pv_voxelize); NF = kMaxFrames: a batch of up to NF
 // frames (pv_voxelize_batch), where a voxel's id carries its frame, each
 // frame keeps its own first max_voxels voxels and writes its own rows.
-template <int NF>
+template <int NF, bool kQueue>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(const KParams p, const Frames<NF> fr) {
   constexpr bool kBatched = NF > 1;
   extern __shared__ __align__(16) unsigned char s_dyn[];
@@ -1077,6 +1094,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   __shared__ unsigned int s_dirty;
   __shared__ unsigned int s_layout[2];
   __shared__ unsigned int s_nrec;
+  __shared__ unsigned int s_qn, s_qh;  // gather: long lists queued by the block, and taken
 
   const unsigned int P = gridDim.x;
   const unsigned int cta = blockIdx.x;
@@ -1135,6 +1153,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   if (tid == 0) {
     s_layout[0] = s_layout[1] = 0;
     s_nrec = 0;
+    s_qn = s_qh = 0;
     s_dirty = dirty_word;
   }
   __syncthreads();  // maps empty, dirty flag shared
@@ -1456,6 +1475,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     // from their whole list.
     bool stale = false;
     unsigned long long* wbuf = reinterpret_cast<unsigned long long*>(s_dyn) + warp * 32;  // append lists' merge buffer
+    unsigned long long* s_queue = reinterpret_cast<unsigned long long*>(s_dyn) + kWarps * 32;  // (row << 32) | slot
     // (Counts of pillars and warps fit 32 bits: N < 2^29, at most 1024 x 32 warps.)
     const unsigned int dropped = kBatched ? s_dcum[B] : total - V;
     const unsigned int nw = static_cast<unsigned int>(nwarps), gw = static_cast<unsigned int>(gwarp);
@@ -1495,15 +1515,33 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       if (in_range) slot = slot_of_rank(p, s_prefix, P, rank);
       unsigned long long* L = p.lists + static_cast<size_t>(slot) * kHead;  // head row
       Head hd = read_head(p, L, in_range);
+      // Long lists (kept ones not served by their first groups, and those
+      // past the budget that need more than their head emptied) go to the
+      // block's queue and are shared out over its warps after this pass,
+      // since a warp's contiguous share of ranks can hold many of them; a
+      // full queue leaves them to this warp.
+      const bool short_drop = drop && hd.few && !hd.filled;
+      const bool longv = (valid && !hd.few) || (drop && !short_drop);
+      bool inl = longv;  // long, processed here: always without the queue, else when it is full
+      if constexpr (kQueue) {
+        const unsigned int lm = __ballot_sync(0xffffffffu, longv);
+        unsigned int qb = 0;
+        if (lane == 0 && lm) qb = atomicAdd(&s_qn, static_cast<unsigned int>(__popc(lm)));
+        qb = __shfl_sync(0xffffffffu, qb, 0) + __popc(lm & lanemask_lt());
+        if (longv && qb < kQueueCap) {
+          const unsigned int qrow = valid ? static_cast<unsigned int>(row) : kQueueDrop;
+          s_queue[qb] = (static_cast<unsigned long long>(qrow) << 32) | static_cast<unsigned int>(slot);
+          inl = false;
+        }
+      }
       {  // past the budget: empty the list
-        const bool short_drop = drop && hd.few && !hd.filled;
         if (short_drop) {
           const uint4 e4 = make_uint4(kEmpty, kEmpty, kEmpty, kEmpty);
           reinterpret_cast<uint4*>(L)[0] = e4;
           reinterpret_cast<uint4*>(L)[1] = e4;
         }
         if (drop && p.hash_mode) p.keys[slot] = kNoKey;
-        for (unsigned int m = __ballot_sync(0xffffffffu, drop && !short_drop); m != 0u; m &= m - 1u) {
+        for (unsigned int m = __ballot_sync(0xffffffffu, drop && inl); m != 0u; m &= m - 1u) {
           const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, __ffs(m) - 1));
           if (p.append)
             app_clear(p, Lu, lane);
@@ -1559,8 +1597,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, __ffs(m) - 1));
         for (int e = static_cast<int>(lane); e < K; e += 32) *Lu.at(e) = kEmpty64;
       }
-      // Everything else, one pillar at a time from its whole list.
-      for (unsigned int m = __ballot_sync(0xffffffffu, valid && !few); m != 0u; m &= m - 1u) {
+      // Long lists the queue had no room for, one pillar at a time from its whole list.
+      for (unsigned int m = __ballot_sync(0xffffffffu, valid && inl); m != 0u; m &= m - 1u) {
         const int u = __ffs(m) - 1;
         const ListRef Lu = list_of(p, __shfl_sync(0xffffffffu, slot, u));
         const long long row_u = __shfl_sync(0xffffffffu, row, u);
@@ -1587,8 +1625,33 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         co[cw - 3] = kz;  // 0 on a pillar grid
         co[cw - 2] = kxy - kz * p.g_y;
         co[cw - 1] = id - kxy * p.g_x;
-        p.out_counts[static_cast<size_t>(row)] = static_cast<int32_t>(cnt);
+        if (few || inl) p.out_counts[static_cast<size_t>(row)] = static_cast<int32_t>(cnt);
         if (p.hash_mode) p.keys[slot] = kNoKey;
+      }
+    }
+    // The block's queued long lists, taken one at a time by whichever warp is free.
+    if constexpr (kQueue) {
+      __syncthreads();
+      const unsigned int qn = s_qn < kQueueCap ? s_qn : kQueueCap;
+      for (;;) {
+        unsigned int j = 0;
+        if (lane == 0) j = atomicAdd(&s_qh, 1u);
+        j = __shfl_sync(0xffffffffu, j, 0);
+        if (j >= qn) break;
+        const unsigned long long qe = s_queue[j];
+        const ListRef Lq = list_of(p, static_cast<int>(static_cast<unsigned int>(qe)));
+        const unsigned int qrow = static_cast<unsigned int>(qe >> 32);
+        if (qrow == kQueueDrop) {
+          if (p.append)
+            app_clear(p, Lq, lane);
+          else
+            for (int e = static_cast<int>(lane); e < K; e += 32) *Lq.at(e) = kEmpty64;
+        } else {
+          float4* orow_q = p.out_voxels + static_cast<size_t>(qrow) * K;
+          const unsigned int w = p.append ? emit_app(p, Lq, orow_q, K, lane, wbuf, &stale)
+                                          : emit_groups(p, Lq, orow_q, K, lane, &stale);
+          if (lane == 0) p.out_counts[qrow] = static_cast<int32_t>(w);
+        }
       }
     }
     if (stale) atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
@@ -2254,21 +2317,25 @@ int grid_extents(const float r[6], const float v[3], int64_t g[3]) {
 // Dynamic shared memory opt-in for both instantiations of the ordered kernel;
 // returns the resident blocks per SM of the smaller one (0 on failure).
 int prepare_kernels() {
-  int single = 0, batched = 0;
-  if (cudaFuncSetAttribute(pv_voxelize_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
+  int single = 0, queued = 0, batched = 0;
+  if (cudaFuncSetAttribute(pv_voxelize_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
           cudaSuccess ||
-      cudaFuncSetAttribute(pv_voxelize_kernel<kMaxFrames>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
+      cudaFuncSetAttribute(pv_voxelize_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&single, pv_voxelize_kernel<1>, kThreads, kDynSmem) !=
+      cudaFuncSetAttribute(pv_voxelize_kernel<kMaxFrames, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kDynSmem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&single, pv_voxelize_kernel<1, false>, kThreads, kDynSmem) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&batched, pv_voxelize_kernel<kMaxFrames>, kThreads, kDynSmem) !=
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&queued, pv_voxelize_kernel<1, true>, kThreads, kDynSmem) !=
           cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&batched, pv_voxelize_kernel<kMaxFrames, false>, kThreads,
+                                                    kDynSmem) != cudaSuccess ||
       cudaFuncSetAttribute(pv_downsample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDsSmem) !=
           cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  return std::min(single, batched);
+  return std::min(std::min(single, queued), batched);
 }
 
 int device_info(int dev, DeviceInfo* out) {
@@ -2548,6 +2615,11 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.frame_cnt = ws->counts + kMaxCtas;
   kp.acc = ws->acc;
   kp.acc_cap = ws->acc_cap;
+  // The gather's share per warp grows with the rows; long lists bunch up in
+  // some warps' contiguous shares once a share holds more than a few rows,
+  // and queuing them per block is then worth its block barrier (a kernel
+  // of its own: the queue's code alone slows the small frames' gather).
+  const bool queue = static_cast<int64_t>(M) >= kQueueMinRowsPerWarp * pl.ctas * kWarps;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned int>(pl.ctas));
@@ -2569,11 +2641,12 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
     Frames<1> fr;
     fr.off[0] = 0;
     fr.off[1] = N;
-    e = cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1>, kp, fr);
+    e = queue ? cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1, true>, kp, fr)
+              : cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1, false>, kp, fr);
   } else {
     Frames<kMaxFrames> fr;  // copied into the launch: the caller's array may go at once
     for (int b = 0; b <= kMaxFrames; ++b) fr.off[b] = b <= pl.frames ? frame_offsets[b] : N;
-    e = cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<kMaxFrames>, kp, fr);
+    e = cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<kMaxFrames, false>, kp, fr);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
