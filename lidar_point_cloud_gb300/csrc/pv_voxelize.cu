@@ -76,7 +76,9 @@ static_assert(kWarps <= 32 && kWarps % 16 == 0, "warp 0 scans one value per warp
 constexpr int kMinBlocksPerSM = 1024 / kThreads;
 constexpr int kMaxCtas = 1024;             // blocks per launch (prefix lives in shared memory)
 static_assert(kMaxCtas < 0x10000, "finished blocks are counted in 16 bits");
-constexpr int kFlagUnroll = 8;             // block-wide tiles in flight when flagging
+constexpr int kFlagUnroll = 4;             // block-wide tiles in flight when flagging
+constexpr int kFlagUnrollWide = 8;         // the same, in launches whose chunks span up to 8 block tiles
+static_assert(kWarps == 32, "the flag prefix gives each lane U consecutive (tile, warp) counts");
 #ifndef PV_HEAD_ENTRIES
 #define PV_HEAD_ENTRIES 4
 #endif
@@ -352,6 +354,34 @@ __device__ unsigned int block_exclusive_scan(unsigned int x, unsigned int* s_tmp
   *total = s_tmp[kWarps];
   __syncthreads();  // s_tmp may be reused right after
   return before + incl - x;
+}
+
+// Exclusive prefix, in place, of the U x kWarps first-point counts
+// (position u * kWarps + w: block tile u, warp w, in index order), run by
+// warp 0; *total receives the sum.  Lane l sums the U consecutive positions
+// from l * U, one warp scan orders the lanes' sums.
+template <int U>
+__device__ __forceinline__ void flag_prefix(unsigned int* flat, unsigned int* total, unsigned int lane) {
+  unsigned int c[U];
+  unsigned int sum = 0;
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    c[k] = flat[lane * U + k];
+    sum += c[k];
+  }
+  unsigned int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= static_cast<unsigned int>(o)) incl += y;
+  }
+  unsigned int run = incl - sum;
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    flat[lane * U + k] = run;
+    run += c[k];
+  }
+  if (lane == 31) *total = incl;
 }
 
 // ------------------------------------------------------------ binning
@@ -1082,13 +1112,16 @@ __device__ void reset_tables(const KParams& p, size_t gtid, size_t gthreads) {
 template <int NF, bool kQueue>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(const KParams p, const Frames<NF> fr) {
   constexpr bool kBatched = NF > 1;
+  // Block tiles in flight in the first-point pass: 8 where chunks are long
+  // (the launches that queue long lists), else 4 (fewer empty tiles to scan).
+  constexpr int FU = kQueue ? kFlagUnrollWide : kFlagUnroll;
   extern __shared__ __align__(16) unsigned char s_dyn[];
   __shared__ unsigned int s_prefix[kMaxCtas + 1];
   __shared__ long long s_off[NF + 1];
   __shared__ unsigned int s_fpre[NF + 1];  // batched: first points before each frame start (global)
   __shared__ unsigned int s_vcum[NF + 1];  // batched: rows emitted by earlier frames
   __shared__ unsigned int s_dcum[NF + 1];  // batched: voxels past the budget in earlier frames
-  __shared__ unsigned int s_tile[kFlagUnroll][kWarps];
+  __shared__ unsigned int s_tile[FU][kWarps];
   __shared__ unsigned int s_tmp[kWarps + 1];
   __shared__ int s_flag;
   __shared__ unsigned int s_dirty;
@@ -1341,50 +1374,35 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   if (alive) {
     // ---- phase 2a: first points of this block's range, compacted in index order.
     unsigned int local = 0;
-    for (long long base = begin; base < end; base += static_cast<long long>(kFlagUnroll) * kThreads) {
-      int s[kFlagUnroll];
-      uint32_t head[kFlagUnroll];
+    for (long long base = begin; base < end; base += static_cast<long long>(FU) * kThreads) {
+      int s[FU];
+      uint32_t head[FU];
 #pragma unroll
-      for (int u = 0; u < kFlagUnroll; ++u) {
+      for (int u = 0; u < FU; ++u) {
         const long long i = base + u * kThreads + tid;
         s[u] = i < end ? __ldcg(p.slot_of_point + i) : -1;
       }
 #pragma unroll
-      for (int u = 0; u < kFlagUnroll; ++u) {
+      for (int u = 0; u < FU; ++u) {
         // Only a tile-group leader can be its pillar's first point.
         head[u] = (s[u] >= 0 && (s[u] & kLeaderBit))
                       ? static_cast<uint32_t>(__ldcg(p.lists + static_cast<size_t>(s[u] & ~kLeaderBit) * kHead) >> 32)
                       : kEmpty;
         s[u] = s[u] >= 0 ? (s[u] & ~kLeaderBit) : -1;
       }
-      unsigned int ball[kFlagUnroll];
+      unsigned int ball[FU];
 #pragma unroll
-      for (int u = 0; u < kFlagUnroll; ++u) {
+      for (int u = 0; u < FU; ++u) {
         const long long i = base + u * kThreads + tid;
         ball[u] = __ballot_sync(0xffffffffu, s[u] >= 0 && head[u] == static_cast<uint32_t>(i));
         if (lane == 0) s_tile[u][warp] = __popc(ball[u]);
       }
       __syncthreads();
-      if (warp == 0) {  // exclusive prefix over (tile u, warp) in index order
-        unsigned int carry = 0;
-#pragma unroll
-        for (int u = 0; u < kFlagUnroll; ++u) {
-          const unsigned int c = lane < static_cast<unsigned int>(kWarps) ? s_tile[u][lane] : 0u;
-          unsigned int incl = c;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= static_cast<unsigned int>(o)) incl += y;
-          }
-          if (lane < static_cast<unsigned int>(kWarps)) s_tile[u][lane] = carry + incl - c;
-          carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) s_tmp[kWarps] = carry;
-      }
+      if (warp == 0) flag_prefix<FU>(&s_tile[0][0], &s_tmp[kWarps], lane);
       __syncthreads();
       unsigned int run = local;
 #pragma unroll
-      for (int u = 0; u < kFlagUnroll; ++u) {
+      for (int u = 0; u < FU; ++u) {
         const unsigned int before = run + s_tile[u][warp] + __popc(ball[u] & lanemask_lt());
         if ((ball[u] >> lane) & 1u) p.firsts[begin + before] = s[u];
         if (kBatched) {  // a frame start at i records this block's first points before it
@@ -2139,22 +2157,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
         if (lane == 0) s_tile[u][warp] = __popc(ball[u]);
       }
       __syncthreads();
-      if (warp == 0) {
-        unsigned int carry = 0;
-#pragma unroll
-        for (int u = 0; u < kFlagUnroll; ++u) {
-          const unsigned int c = lane < static_cast<unsigned int>(kWarps) ? s_tile[u][lane] : 0u;
-          unsigned int incl = c;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const unsigned int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= static_cast<unsigned int>(o)) incl += y;
-          }
-          if (lane < static_cast<unsigned int>(kWarps)) s_tile[u][lane] = carry + incl - c;
-          carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) s_tmp[kWarps] = carry;
-      }
+      if (warp == 0) flag_prefix<kFlagUnroll>(&s_tile[0][0], &s_tmp[kWarps], lane);
       __syncthreads();
 #pragma unroll
       for (int u = 0; u < kFlagUnroll; ++u)
