@@ -1714,8 +1714,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
 // The page's own contract, without the canonical order ("The hash slot is
 // the output index", "Claiming a pillar and packing points", "Compaction"):
 // a pillar's row is handed out when the pillar is created, its points take
-// positions in arrival order ("atomicAdd returns each thread's write
-// position inside the pillar"), points past max_points are dropped, and
+// positions in the order their counter increments arrive ("Claiming a
+// pillar and packing points"), points past max_points are dropped, and
 // pillars created after max_voxels rows are taken are dropped whole.  Which
 // points and pillars survive a cap, and in what order, varies from run to
 // run, as the page says of its own kernel ("Results"); the pillar set, the
@@ -2753,6 +2753,11 @@ constexpr size_t kStaticOffKeys = kStaticOffCounts + 4 * kMaxCtas;
 constexpr size_t kStaticOffLists = kStaticOffKeys + 4 * kStaticSlots;
 constexpr size_t kStaticPoolWords = 40960;  // append lists' overflow pool: (32768 / 7 + 1) x 8 words at most
 constexpr size_t kStaticListWords = kStaticSlots * kStaticMaxK + kStaticPoolWords;  // 64-bit entries
+// The pool must hold an overflow list for every slot that can overflow: with
+// the shortest append rows (kAppendMinK words) a slot overflows only past
+// kAppendMinK - 2 entries of at least one point each.
+static_assert((kStaticMaxPoints / (kAppendMinK - 1) + 1) * kAppendMinK <= static_cast<int64_t>(kStaticPoolWords),
+              "the static overflow pool holds every list an append plan can take");
 constexpr size_t kStaticOffRows = kStaticOffLists + 8 * kStaticListWords;
 constexpr size_t kStaticOffRecs = kStaticOffRows + 16 * static_cast<size_t>(kStaticMaxPoints);
 constexpr size_t kStaticOffPoints = kStaticOffRecs + 8 * static_cast<size_t>(kStaticMaxPoints);

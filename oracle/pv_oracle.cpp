@@ -33,6 +33,7 @@
 // prints, a hand-derived table of boundary points, a hand-worked example,
 // an O(N^2) brute force, a NumPy stable-sort restatement and invariants.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -328,7 +329,7 @@ int pv_oracle_fps(const float* points, int64_t N, int64_t M, int64_t start,
       const float dy = points[4 * i + 1] - qy;
       const float dz = points[4 * i + 2] - qz;
       const float d = (dx * dx + dy * dy) + dz * dz;
-      if (d < min_dist[i]) min_dist[i] = d;
+      min_dist[i] = std::min(min_dist[i], d);  // each point's distance to its nearest sample so far
       if (min_dist[i] > best_d) {  // strict: the first (lowest-index) maximum stays
         best_d = min_dist[i];
         best = i;

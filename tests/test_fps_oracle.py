@@ -121,7 +121,7 @@ def test_argument_errors():
 
 MUTANTS = {
     "tie_to_last": ("if (min_dist[i] > best_d) {", "if (min_dist[i] >= best_d) {"),
-    "no_running_minimum": ("if (d < min_dist[i]) min_dist[i] = d;", "min_dist[i] = d;"),
+    "no_running_minimum": ("min_dist[i] = std::min(min_dist[i], d);", "min_dist[i] = d;"),
     "start_ignored": ("int64_t sel = start;", "int64_t sel = 0;"),
     "no_z_term": ("const float d = (dx * dx + dy * dy) + dz * dz;", "const float d = dx * dx + dy * dy;"),
     "fused_distance": ("const float d = (dx * dx + dy * dy) + dz * dz;",

@@ -5,9 +5,9 @@ into a CUDA graph under global capture mode, plug-ins whose host owns all
 device memory, real-time loops that forbid allocation after start-up.
 pv_voxelize_static serves them from one fixed scratch array inside the
 library.  These tests call it through the C ABI and compare every output
-byte with the workspace entry point, on calls made back to back, so the
-second call starts from whatever state the first left in the shared array.
-This file is collected last on purpose.
+byte with the workspace entry point and with the CPU oracle, on calls made
+back to back, so the second call starts from whatever state the first left
+in the shared array.  This file is collected last on purpose.
 """
 
 from __future__ import annotations
@@ -16,6 +16,8 @@ import ctypes
 
 import numpy as np
 import pytest
+
+import oracle
 
 torch = pytest.importorskip("torch")
 pv = pytest.importorskip("lidar_point_cloud_gb300")
@@ -64,6 +66,9 @@ def test_static_entry_point_matches_twice_in_a_row():
         assert st == 0
         assert int(got[3][0]) == int(ref[3][0]) > 0
         assert _same(got, ref)
+        ost, ov, oc, on, oV = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+        assert ost == 0 and int(got[3][0]) == oV
+        assert _same(got[:3], [ov, oc, on])
 
 
 def test_static_entry_point_rejects_sizes_beyond_its_limits():
