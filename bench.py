@@ -35,6 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Mpoints/s voxelized per frame; achieved HBM GB/s vs GB300 peak"
+SPIN_CYCLES = 2_000_000  # about 1 ms of GPU spin queued before each timed region
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
@@ -182,36 +183,78 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(busy)}
 
 
-def oracle_frame(pts, P, lib, op="voxelize"):
-    """One frame through the C++ oracle (the 3-D pass when the grid has layers)."""
+def oracle_op(P, op="voxelize"):
+    """The oracle pass a workload takes: the 3-D pass when the grid has layers."""
     import oracle
 
     if op == "downsample":
-        return oracle.downsample(pts, P.point_cloud_range, P.voxel_size, P.max_voxels, lib)
-
-    three_d = oracle.grid3d(P.point_cloud_range, P.voxel_size, lib)[1][2] > 1
-    return oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, lib,
-                           three_d=three_d)
+        return "downsample"
+    return "voxelize3d" if oracle.grid3d(P.point_cloud_range, P.voxel_size)[1][2] > 1 else "voxelize"
 
 
-def cpu_oracle_rate(pts, P, seconds, op="voxelize"):
-    """Single-threaded C++ oracle on the host: (Mpoints/s, frames, seconds)."""
+def host_cpu():
+    """The host's CPU model and logical core count."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return {"model": model or "unknown", "nproc": os.cpu_count()}
+
+
+class OneCore:
+    """Pins the calling process to one core (the last it may run on) and
+    restores its affinity afterwards."""
+
+    def __enter__(self):
+        self.prev = os.sched_getaffinity(0)
+        self.core = max(self.prev)
+        os.sched_setaffinity(0, {self.core})
+        return self
+
+    def __exit__(self, *exc):
+        os.sched_setaffinity(0, self.prev)
+
+
+def oracle_runs(pts, P, op, reps):
+    """Per-run durations (s) of the oracle pass on one frame, measured with
+    steady_clock inside the C++ library (no Python in the timed region)."""
     import oracle
 
-    lib = oracle.load()
+    return oracle.time_passes(oracle_op(P, op), pts, P.point_cloud_range, P.voxel_size, P.max_points,
+                              P.max_voxels, reps) * 1e-9
+
+
+def cpu_baseline(pts, P, seconds, op="voxelize", what="the full frame"):
+    """The single-threaded C++ oracle on one host core: the median of at least
+    five runs (three for frames over a second), about `seconds` of work in all."""
     n = pts.shape[0]
-    oracle_frame(pts, P, lib, op)  # warm
-    frames, t0 = 0, time.perf_counter()
-    while True:
-        oracle_frame(pts, P, lib, op)
-        frames += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or frames >= 100000:
-            break
-    return n * frames / el / 1e6, frames, el
+    with OneCore() as pin:
+        first = float(oracle_runs(pts, P, op, 1)[0])
+        reps = int(max(3 if first > 1.0 else 5, min(1000, seconds / max(first, 1e-6))))
+        runs = oracle_runs(pts, P, op, reps)
+    med = float(statistics.median(runs))
+    return {"value": round(n / med / 1e6, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
+            "median_ms": round(med * 1e3, 3), "runs": int(reps), "pinned_core": pin.core, "host": host_cpu(),
+            "sample": f"{reps} runs on {what} ({sum(runs):.1f} s), median per run on steady_clock inside the "
+                      f"single-threaded C++ oracle ({oracle_op(P, op)}), process pinned to one core"}
 
 
 def run_reference(args, rank, world):
+    import numpy as np
+
     from lidar_point_cloud_gb300 import synth
 
     if rank != 0:
@@ -257,26 +300,19 @@ def run_reference(args, rank, world):
         pts, P = synth.make(args.workload)
         frames = [pts]
 
-    def one_step():
-        for f in frames:
-            oracle_frame(f, P, lib, args.op)
-
-    # A step is a bounded sample: when the whole frames would make the
-    # warm-up and timed steps run past about a minute, each step takes the
-    # first points of each frame instead (the metric counts the points done).
-    t0 = time.perf_counter()
-    one_step()
-    t_full = time.perf_counter() - t0
-    runs = max(1, args.steps + args.warmup)
-    if runs * t_full > 60.0:
-        keep = max(4096 / max(1, max(f.shape[0] for f in frames)), 60.0 / (runs * t_full))
-        frames = [f[:max(1, int(f.shape[0] * keep))] for f in frames]
-    for _ in range(args.warmup):
-        one_step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        one_step()
-    el = time.perf_counter() - t0
+    # A step is one oracle pass per frame, timed on steady_clock inside the
+    # C++ library with the process pinned to one core; a bounded sample: when
+    # whole frames would make the warm-up and timed steps run past about a
+    # minute, each step takes the first points of each frame instead (the
+    # metric counts the points done).
+    with OneCore() as pin:
+        t_full = sum(float(oracle_runs(f, P, args.op, 1)[0]) for f in frames)
+        runs = max(1, args.steps + args.warmup)
+        if runs * t_full > 60.0:
+            keep = max(4096 / max(1, max(f.shape[0] for f in frames)), 60.0 / (runs * t_full))
+            frames = [f[:max(1, int(f.shape[0] * keep))] for f in frames]
+        per_frame = [oracle_runs(f, P, args.op, args.warmup + args.steps)[args.warmup:] for f in frames]
+    el = float(sum(np.sum(t) for t in per_frame))
     n = sum(f.shape[0] for f in frames)
     value = n * args.steps / el / 1e6
     line = {
@@ -288,9 +324,11 @@ def run_reference(args, rank, world):
                                 f"{args.workload}: ") + synth.WORKLOADS[args.workload], "N": n,
                    "max_points": P.max_points, "max_voxels": P.max_voxels, "frames_per_launch": args.batch},
         "cpu_baseline": {"value": round(value, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
+                         "pinned_core": pin.core, "host": host_cpu(),
                          "sample": (f"{args.batch} frame(s) per step, {n:,} of {pts.shape[0]:,} points "
                                     f"({'whole frames' if n == pts.shape[0] else 'the first points of each frame'}), "
-                                    f"{args.steps} steps, single-threaded C++ std::map oracle")},
+                                    f"{args.steps} steps, each pass on steady_clock inside the single-threaded C++ "
+                                    "std::map oracle, process pinned to one core")},
         "e2e": {"value": round(value, 3), "unit": "Mpoints/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -488,30 +526,54 @@ def run_gb300(args, rank, world, local_rank):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    region0 = torch.cuda.Event(enable_timing=True)
-    region1 = torch.cuda.Event(enable_timing=True)
-    region0.record(stream)
-    if use_graph:
-        with torch.cuda.stream(stream):  # replay on the stream the events are recorded on
-            graph.replay()
-    else:
+
+    def stream_launches():
+        """K plain stream launches, an event pair around each."""
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(SPIN_CYCLES)  # the launches queue up behind it
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
         for k in range(args.steps):
             starts[k].record(stream)
             step(args.warmup + k)
             ends[k].record(stream)
-    region1.record(stream)
-    torch.cuda.synchronize(dev)
+        r1.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        return r0.elapsed_time(r1), [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+    # Timed region: the K launches of the graph, replayed once; a spin kernel
+    # queued first keeps the host's graph submission out of the region, so it
+    # holds the K launches back to back whatever K is.
     if dist:
         dist.barrier()
-    region_ms = region0.elapsed_time(region1)
-    # Per-launch duration: event pairs around each launch, or with the graph
-    # (launches back to back, no gaps to hide) the region over K.
-    kernel_ms = ([region_ms / args.steps] if use_graph else [s.elapsed_time(e) for s, e in zip(starts, ends)])
+    torch.cuda.synchronize(dev)
+    if use_graph:
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(SPIN_CYCLES)
+        region0 = torch.cuda.Event(enable_timing=True)
+        region1 = torch.cuda.Event(enable_timing=True)
+        region0.record(stream)
+        with torch.cuda.stream(stream):  # replay on the stream the events are recorded on
+            graph.replay()
+        region1.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        region_ms = region0.elapsed_time(region1)
+        # Launches back to back, no gaps to hide: the region over K.
+        kernel_ms = [region_ms / args.steps]
+        # The same K launches as plain stream launches, reported beside it.
+        stream_region_ms, stream_ms = stream_launches()
+    else:
+        region_ms, kernel_ms = stream_launches()
+        stream_region_ms, stream_ms = region_ms, kernel_ms
     # Keep the GPU busy (untimed) so the clock sampler sees at least ~1.5 s of load.
     t_soak = time.perf_counter()
     k = 0
@@ -593,10 +655,8 @@ def run_gb300(args, rank, world, local_rank):
     cpu = None
     if not args.no_cpu_baseline:
         one = pts[:frame_off[1]] if Bf > 1 else pts
-        rate, frames, el = cpu_oracle_rate(one, P, args.cpu_seconds, args.op)
-        cpu = {"value": round(rate, 3), "unit": "Mpoints/s", "cores": 1, "kind": "oracle",
-               "sample": f"{frames} repetitions of {'the first frame' if Bf > 1 else 'the full frame'} ({el:.1f} s), "
-                         "single-threaded C++ std::map oracle"}
+        cpu = cpu_baseline(one, P, args.cpu_seconds, args.op,
+                           "the first frame" if Bf > 1 else "the full frame")
 
     line = {
         "metric": METRIC,
@@ -632,6 +692,14 @@ def run_gb300(args, rank, world, local_rank):
             "peak_source": f"{peak_src} (hbm_gbs)", "kernel": kernel,
             "bytes_per_launch": bytes_launch, "avg_launch_us": round(avg_kernel_s * 1e6, 3),
             "median_launch_us": None if use_graph else round(statistics.median(kernel_ms) * 1e3, 3),
+            "timing": {
+                "graph_replay_us_per_launch": round(region_ms / args.steps * 1e3, 3) if use_graph else None,
+                "stream_mean_us": round(statistics.mean(stream_ms) * 1e3, 3),
+                "stream_median_us": round(statistics.median(stream_ms) * 1e3, 3),
+                "stream_region_us_per_launch": round(stream_region_ms / args.steps * 1e3, 3),
+                "note": "graph replay = K launches captured once, region over K; stream = the same K launches "
+                        "issued one by one, an event pair around each; both regions start behind a spin kernel",
+            },
             "data_bytes_per_launch": data_bytes,
             "frac_data": round(data_bytes / avg_kernel_s / 1e9 / peak, 4),
         },

@@ -493,6 +493,35 @@ def downsample(points: np.ndarray, pc_range, voxel_size, max_voxels: int, lib=No
     return st, cen, coords, counts, int(num[0])
 
 
+def time_passes(op: str, points: np.ndarray, pc_range, voxel_size, max_points: int, max_voxels: int, reps: int,
+                lib=None) -> np.ndarray:
+    """Durations (ns, steady_clock, measured inside the C++ library) of
+    `reps` runs of one oracle pass on the same cloud: op "voxelize",
+    "voxelize3d" or "downsample".  For the benchmark's CPU baseline only."""
+    lib = lib or load()
+    fn = lib.pv_oracle_time
+    f = ctypes.POINTER(ctypes.c_float)
+    i32 = ctypes.POINTER(ctypes.c_int32)
+    fn.argtypes = [ctypes.c_int, f, ctypes.c_int64, f, f, ctypes.c_int, ctypes.c_int, f, i32, i32, i32, ctypes.c_int,
+                   ctypes.POINTER(ctypes.c_int64)]
+    fn.restype = ctypes.c_int
+    code = {"voxelize": 0, "voxelize3d": 1, "downsample": 2}[op]
+    pts = np.ascontiguousarray(points, dtype=np.float32).reshape(-1, 4)
+    r, v = _f32(pc_range), _f32(voxel_size)
+    width = 1 if code == 2 else max_points
+    rows = np.empty((max_voxels, width, 4), dtype=np.float32)
+    coords = np.empty((max_voxels, 3), dtype=np.int32)
+    counts = np.empty((max_voxels,), dtype=np.int32)
+    num = np.zeros(1, dtype=np.int32)
+    times = np.zeros(reps, dtype=np.int64)
+    st = fn(code, _fptr(pts) if pts.size else None, pts.shape[0], _fptr(r), _fptr(v), int(max_points),
+            int(max_voxels), _fptr(rows), coords.ctypes.data_as(i32), counts.ctypes.data_as(i32),
+            num.ctypes.data_as(i32), int(reps), times.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+    if st != OK:
+        raise RuntimeError(f"oracle status {st}")
+    return times
+
+
 def downsample_exact(points: np.ndarray, pc_range, voxel_size, max_voxels: int):
     """Restatement with exact sums: each voxel's mean is the exact rational sum
     of its points' fields over the count (math.fsum is exact for these sums

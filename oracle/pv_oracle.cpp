@@ -34,6 +34,7 @@
 // an O(N^2) brute force, a NumPy stable-sort restatement and invariants.
 
 #include <algorithm>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -336,6 +337,34 @@ int pv_oracle_fps(const float* points, int64_t N, int64_t M, int64_t start,
       }
     }
     sel = best;
+  }
+  return kOk;
+}
+
+// Benchmark helper, not part of any definition above: runs one of the
+// passes `reps` times on the same cloud and writes each run's duration on
+// std::chrono::steady_clock, in nanoseconds, to times_ns.  op 0 is
+// pv_oracle_voxelize, 1 pv_oracle_voxelize3d, 2 pv_oracle_downsample (which
+// takes no max_points and writes [max_voxels, 4] centroids).  Returns the
+// first non-zero status of a pass, else 0.
+int pv_oracle_time(int op, const float* points, int64_t N, const float range[6], const float voxel_size[3],
+                   int max_points, int max_voxels, float* out_rows, int32_t* out_coords, int32_t* out_counts,
+                   int32_t* out_num, int reps, int64_t* times_ns) {
+  if (reps < 1 || times_ns == nullptr || op < 0 || op > 2) return kErrInvalid;
+  for (int r = 0; r < reps; ++r) {
+    const auto t0 = std::chrono::steady_clock::now();
+    int st;
+    if (op == 0)
+      st = pv_oracle_voxelize(points, N, range, voxel_size, max_points, max_voxels, out_rows, out_coords, out_counts,
+                              out_num);
+    else if (op == 1)
+      st = pv_oracle_voxelize3d(points, N, range, voxel_size, max_points, max_voxels, out_rows, out_coords,
+                                out_counts, out_num);
+    else
+      st = pv_oracle_downsample(points, N, range, voxel_size, max_voxels, out_rows, out_coords, out_counts, out_num);
+    const auto t1 = std::chrono::steady_clock::now();
+    if (st != kOk) return st;
+    times_ns[r] = std::chrono::duration_cast<std::chrono::nanoseconds>(t1 - t0).count();
   }
   return kOk;
 }
