@@ -114,3 +114,52 @@ def test_downsample_python_api():
     cen, coords, counts = pv.downsample(torch.from_numpy(pts).to(DEV), P.point_cloud_range, P.voxel_size)
     ok, *_ = oracle.cells_numpy(pts, P.point_cloud_range, P.voxel_size)
     assert int(counts.sum()) == int(ok.sum()) and cen.shape[0] == coords.shape[0] == counts.shape[0]
+
+
+def test_downsample_voxels_straddling_a_plane():
+    """Voxels that contain the planes x = 0, y = 0 and z = 0, their points
+    in cancelling pairs, so a mean can be far smaller than the values summed.
+
+    The 1-ulp bound of the other tests rests on the values of a voxel sharing
+    one sign: summation errors are relative to the sum of the magnitudes, and
+    for one sign that sum is the sum itself.  Here they are not, so this test
+    takes the bound that holds whatever the signs: the kernel's float-float
+    warp sums and double accumulation err by a few units of 2^-46 of the
+    voxel's mean magnitude sum(|x|) / n, plus the final rounding (half an
+    ulp of the mean).  It checks every centroid against the exact mean within
+    2^-40 sum(|x|) / n plus one ulp, the integers exactly, and the one-ulp
+    bound on the voxels whose values do share a sign (the intensities here).
+    """
+    rng = np.random.Generator(np.random.PCG64(4242))
+    r, v = (-2.5, -2.5, -2.5, 2.5, 2.5, 2.5), (1.0, 1.0, 1.0)  # the middle cell [-0.5, 0.5)^3 holds 0
+    chunks = []
+    for vox in range(27):  # the 3 x 3 x 3 cells around the origin; the centre one straddles all three planes
+        c = np.array([vox % 3, (vox // 3) % 3, vox // 9], np.float64) - 1.0
+        n = 2 * int(rng.integers(4, 400))
+        a = rng.uniform(0.0, 0.49, size=(n // 2, 3))
+        tiny = rng.uniform(-1e-6, 1e-6, size=(n // 2, 3)) * (vox % 2)  # half the voxels exactly symmetric
+        xyz = np.concatenate([c + a, c - a + tiny]).astype(np.float32)
+        w = rng.random(n).astype(np.float32)
+        chunks.append(np.concatenate([xyz, w[:, None]], axis=1))
+    pts = np.concatenate(chunks).astype(np.float32)
+    pts = pts[rng.permutation(pts.shape[0])]
+    M = 64
+    ex_cen, ex_coords, ex_counts, eV = oracle.downsample_exact(pts, r, v, M)
+    t = torch.from_numpy(np.ascontiguousarray(pts)).to(DEV)
+    out = pv.alloc_downsample_outputs(M, DEV)
+    pv.downsample_into(t, r, v, M, out)
+    torch.cuda.synchronize()
+    gc, gco, gn, num = (o.cpu().numpy() for o in out)
+    assert int(num[0]) == eV == 27
+    assert same_bits(gco, ex_coords) and same_bits(gn, ex_counts)
+    ok, cx, cy, cz, g = oracle.cells_numpy(pts, r, v)
+    key = (cz * g[1] + cy) * g[0] + cx
+    for row in range(eV):
+        z, y, x = (int(q) for q in ex_coords[row])
+        sel = ok & (key == (z * g[1] + y) * g[0] + x)
+        mag = np.abs(pts[sel].astype(np.float64)).sum(axis=0) / sel.sum()
+        ulp = np.spacing(np.abs(ex_cen[row]).astype(np.float32)).astype(np.float64)
+        err = np.abs(gc[row].astype(np.float64) - ex_cen[row].astype(np.float64))
+        assert np.all(err <= 2.0 ** -40 * mag + ulp), (row, err, mag, ulp)
+    # The intensities (all of one sign) keep the one-ulp bound.
+    assert oracle.ulp_distance32(gc[:eV, 3], ex_cen[:eV, 3]).max() <= 1
