@@ -256,7 +256,7 @@ int pv_voxelize_host(const float* points_host, int64_t num_points, const float p
  * real-time pipelines that forbid allocation after start-up.  It takes the
  * same arguments and gives the same result as pv_voxelize, but its scratch
  * (table, per-point arrays, control block) lives in one fixed array of
- * 18,092,288 bytes (about 17.3 MiB) of device memory, declared in the library at file scope:
+ * 18,419,968 bytes (about 17.6 MiB) of device memory, declared in the library at file scope:
  * every GPU that loads the library holds it until the process exits.  The
  * caller still owns and passes the input and the outputs.
  *
