@@ -1089,6 +1089,92 @@ __device__ unsigned int emit_app(const KParams& p, const ListRef& L, float4* oro
   return written;
 }
 
+// Up to four queued append-list pillars at once, eight lanes each (group g =
+// lanes 8g .. 8g+7, with the queue entry `qe` valid where `mine`).  A kept
+// pillar whose slot holds at most min(7, S - 2) entries (so no overflow list)
+// is served here: its group reads slot words 0..7 (one request a group), lane
+// s takes entry s (word s + 1), the group sorts its entries by leader (a
+// bitonic network over 8 lanes), sums the group sizes, and copies positions
+// s, s + 8, s + 16, s + 24 of the row, zeros past the points taken, then
+// writes the count and empties the words it read.  Returns true on the lanes
+// of a group whose pillar needs the whole-warp way (more entries, an overflow
+// list, or a list past the budget).  All 32 lanes call it.
+__device__ bool emit_app_quad(const KParams& p, unsigned long long qe, bool mine, unsigned int lane, int K,
+                              bool* stale) {
+  const unsigned int sl = lane & 7u, base = lane & ~7u;
+  const int S = kHead + p.KT;
+  const unsigned int qrow = static_cast<unsigned int>(qe >> 32);
+  const bool kept = mine && qrow != kQueueDrop;
+  const ListRef L = list_of(p, kept ? static_cast<int>(static_cast<unsigned int>(qe)) : 0);
+  const unsigned long long w = kept ? __ldcg(slot_word(L.head, L.tail, static_cast<int>(sl))) : kEmpty64;
+  const unsigned int cnt = ~__shfl_sync(0xffffffffu, static_cast<unsigned int>(w), static_cast<int>(base));
+  const unsigned int cap = S - 2 < 7 ? static_cast<unsigned int>(S - 2) : 7u;
+  const bool fast = kept && cnt >= 1u && cnt <= cap;
+  const int src = lane < 31u ? static_cast<int>(lane) + 1 : 31;  // entry s is word s + 1 (s < cnt <= 7)
+  unsigned long long ent = (static_cast<unsigned long long>(__shfl_sync(0xffffffffu, static_cast<unsigned int>(w >> 32), src)) << 32) |
+                           __shfl_sync(0xffffffffu, static_cast<unsigned int>(w), src);
+  if (!(fast && sl < cnt)) ent = kEmpty64;
+  if (ent != kEmpty64 && (ent >> 32) >= static_cast<unsigned long long>(p.n)) {
+    ent = kEmpty64;
+    *stale = true;
+  }
+#pragma unroll
+  for (int size = 2; size <= 8; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int o_src = static_cast<int>(lane ^ static_cast<unsigned int>(stride));
+      const unsigned long long o = (static_cast<unsigned long long>(__shfl_sync(0xffffffffu, static_cast<unsigned int>(ent >> 32), o_src)) << 32) |
+                                   __shfl_sync(0xffffffffu, static_cast<unsigned int>(ent), o_src);
+      const bool up = (sl & static_cast<unsigned int>(size)) == 0u;
+      const bool lower = (sl & static_cast<unsigned int>(stride)) == 0u;
+      const unsigned long long mn = ent < o ? ent : o, mx = ent < o ? o : ent;
+      ent = (lower == up) ? mn : mx;
+    }
+  }
+  const unsigned int sz = ent != kEmpty64 ? (static_cast<unsigned int>(ent) & 2047u) : 0u;
+  unsigned int incl = sz;
+#pragma unroll
+  for (int d = 1; d < 8; d <<= 1) {
+    const unsigned int y = __shfl_up_sync(0xffffffffu, incl, d, 8);
+    if (sl >= static_cast<unsigned int>(d)) incl += y;
+  }
+  const unsigned int st = incl - sz;  // the group's first position in the row
+  const unsigned int all = __shfl_sync(0xffffffffu, incl, static_cast<int>(base) + 7);
+  const unsigned int tk = all < static_cast<unsigned int>(K) ? all : static_cast<unsigned int>(K);
+  const unsigned int G = (__ballot_sync(0xffffffffu, ent != kEmpty64) >> base) & 0xFFu;
+  const int ng = __popc(G);
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 v[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const unsigned int e = sl + 8u * static_cast<unsigned int>(k);
+    int gi = 0;
+#pragma unroll
+    for (int step = 4; step >= 1; step >>= 1) {
+      const int c = gi + step;
+      const unsigned int sc = __shfl_sync(0xffffffffu, st, static_cast<int>(base) + (c < 8 ? c : 7));
+      if (c < ng && sc <= e) gi = c;
+    }
+    const int gl = static_cast<int>(base) + gi;
+    const unsigned long long ge = (static_cast<unsigned long long>(__shfl_sync(0xffffffffu, static_cast<unsigned int>(ent >> 32), gl)) << 32) |
+                                  __shfl_sync(0xffffffffu, static_cast<unsigned int>(ent), gl);
+    const unsigned int gs = __shfl_sync(0xffffffffu, st, gl);
+    v[k] = (fast && e < tk) ? __ldcg(p.tile_rows + entry_row(ge) + (e - gs)) : z4;
+  }
+  if (fast) {
+    float4* orow = p.out_voxels + static_cast<size_t>(qrow) * K;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const unsigned int e = sl + 8u * static_cast<unsigned int>(k);
+      if (e < static_cast<unsigned int>(K)) orow[e] = v[k];
+    }
+    if (sl == 0u) p.out_counts[qrow] = static_cast<int32_t>(tk);
+  }
+  __syncwarp();
+  if (fast) *slot_word(L.head, L.tail, static_cast<int>(sl)) = kEmpty64;  // words 0..7: the count and every entry
+  return mine && !fast;
+}
+
 // Recovery after a failed launch (the control block's dirty flag): every
 // table a launch of any kind fills is emptied whole, since the next launch
 // may be of another kind: lists, hashed keys, unordered-mode row counters,
@@ -1651,24 +1737,33 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     if constexpr (kQueue) {
       __syncthreads();
       const unsigned int qn = s_qn < kQueueCap ? s_qn : kQueueCap;
+      // Four queued lists at a time: append lists of up to seven entries are
+      // served eight lanes a pillar; the rest one at a time by the whole warp.
       for (;;) {
         unsigned int j = 0;
-        if (lane == 0) j = atomicAdd(&s_qh, 1u);
+        if (lane == 0) j = atomicAdd(&s_qh, 4u);
         j = __shfl_sync(0xffffffffu, j, 0);
         if (j >= qn) break;
-        const unsigned long long qe = s_queue[j];
-        const ListRef Lq = list_of(p, static_cast<int>(static_cast<unsigned int>(qe)));
-        const unsigned int qrow = static_cast<unsigned int>(qe >> 32);
-        if (qrow == kQueueDrop) {
-          if (p.append)
-            app_clear(p, Lq, lane);
-          else
-            for (int e = static_cast<int>(lane); e < K; e += 32) *Lq.at(e) = kEmpty64;
-        } else {
-          float4* orow_q = p.out_voxels + static_cast<size_t>(qrow) * K;
-          const unsigned int w = p.append ? emit_app(p, Lq, orow_q, K, lane, wbuf, &stale)
-                                          : emit_groups(p, Lq, orow_q, K, lane, &stale);
-          if (lane == 0) p.out_counts[qrow] = static_cast<int32_t>(w);
+        const bool mine = j + (lane >> 3) < qn;
+        const unsigned long long qe4 = mine ? s_queue[j + (lane >> 3)] : 0ull;
+        const bool slow = p.append ? emit_app_quad(p, qe4, mine, lane, K, &stale) : mine;
+        for (unsigned int m = __ballot_sync(0xffffffffu, slow && (lane & 7u) == 0u); m != 0u; m &= m - 1u) {
+          const int u = __ffs(m) - 1;
+          const unsigned long long qe = (static_cast<unsigned long long>(__shfl_sync(0xffffffffu, static_cast<unsigned int>(qe4 >> 32), u)) << 32) |
+                                        __shfl_sync(0xffffffffu, static_cast<unsigned int>(qe4), u);
+          const ListRef Lq = list_of(p, static_cast<int>(static_cast<unsigned int>(qe)));
+          const unsigned int qrow = static_cast<unsigned int>(qe >> 32);
+          if (qrow == kQueueDrop) {
+            if (p.append)
+              app_clear(p, Lq, lane);
+            else
+              for (int e = static_cast<int>(lane); e < K; e += 32) *Lq.at(e) = kEmpty64;
+          } else {
+            float4* orow_q = p.out_voxels + static_cast<size_t>(qrow) * K;
+            const unsigned int w = p.append ? emit_app(p, Lq, orow_q, K, lane, wbuf, &stale)
+                                            : emit_groups(p, Lq, orow_q, K, lane, &stale);
+            if (lane == 0) p.out_counts[qrow] = static_cast<int32_t>(w);
+          }
         }
       }
     }
