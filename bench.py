@@ -97,23 +97,32 @@ def measured_peak():
 
 HOST_SIDE_MARKER = b"// ------------------------------------------------------------ host side"
 
+# The source files of each profiled kernel: the shared device header and the
+# kernel's own file (farthest point sampling is one file).
+KERNEL_SOURCES = {
+    "pv_voxelize_kernel": ("pv_device.cuh", "pv_ordered.cu"),
+    "pv_unordered_kernel": ("pv_device.cuh", "pv_unordered.cu"),
+    "pv_downsample_kernel": ("pv_device.cuh", "pv_downsample.cu"),
+    "pv_fps_kernel": ("pv_fps.cu",),
+}
+
 
 def kernel_sha(kernel="pv_voxelize_kernel"):
-    """SHA-256 of the device code of the source file that holds the kernel:
-    everything before the file's host-side marker (launch, planning and ABI
-    code after it can change without changing what a profile measured), with
-    line comments, trailing blanks and empty lines left out (comment edits
-    do not change the kernel either)."""
-    name = "pv_fps.cu" if kernel == "pv_fps_kernel" else "pv_voxelize.cu"
-    src = os.path.join(ROOT, "lidar_point_cloud_gb300", "csrc", name)
-    with open(src, "rb") as f:
-        text = f.read()
-    cut = text.find(HOST_SIDE_MARKER)
+    """SHA-256 of the device code of the files that hold the kernel: each
+    file up to its host-side marker (launch, planning and ABI code after it
+    can change without changing what a profile measured), with line
+    comments, trailing blanks and empty lines left out (comment edits do not
+    change the kernel either)."""
     code = []
-    for line in (text[:cut] if cut >= 0 else text).split(b"\n"):
-        line = line.split(b"//", 1)[0].rstrip()
-        if line:
-            code.append(line)
+    for name in KERNEL_SOURCES[kernel]:
+        src = os.path.join(ROOT, "lidar_point_cloud_gb300", "csrc", name)
+        with open(src, "rb") as f:
+            text = f.read()
+        cut = text.find(HOST_SIDE_MARKER)
+        for line in (text[:cut] if cut >= 0 else text).split(b"\n"):
+            line = line.split(b"//", 1)[0].rstrip()
+            if line:
+                code.append(line)
     return hashlib.sha256(b"\n".join(code)).hexdigest()
 
 

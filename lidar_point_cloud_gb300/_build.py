@@ -8,8 +8,13 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "pv_voxelize.cu")  # voxelizer, downsampling and their C ABI
-SRCS = [SRC, os.path.join(PKG, "csrc", "pv_fps.cu")]  # every translation unit of libpv.so
+CSRC = os.path.join(PKG, "csrc")
+# Every translation unit of libpv.so: the block-tile voxelizer, the unordered
+# voxelizer, centroid downsampling, the host side with the C ABI, and farthest
+# point sampling (kernel and entry); pv_device.cuh is the kernels' shared code.
+SRCS = [os.path.join(CSRC, f) for f in ("pv_ordered.cu", "pv_unordered.cu", "pv_downsample.cu", "pv_host.cu",
+                                         "pv_fps.cu")]
+HEADERS = [os.path.join(CSRC, "pv_device.cuh")]
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libpv.so")
 
@@ -35,7 +40,7 @@ def nvcc_path() -> str:
 
 
 def sources():
-    return [*SRCS, os.path.join(INCLUDE, "pv.h")]
+    return [*SRCS, *HEADERS, os.path.join(INCLUDE, "pv.h")]
 
 
 def is_stale(lib: str = LIB) -> bool:

@@ -48,26 +48,32 @@ def test_reference_line_has_every_contract_key(op, workload):
 
 
 def test_profile_lookup_keys_on_device_code(tmp_path, monkeypatch):
-    # A committed summary names the SHA-256 of the kernel source up to its
-    # host-side marker, comments left out: host edits and comment edits keep
-    # the summary, device-code edits void it.
+    # A committed summary names the SHA-256 of the kernel's sources (the
+    # shared device header and the kernel's file) up to their host-side
+    # markers, comments left out: host edits and comment edits keep the
+    # summary, device-code edits in either file void it.
     src_dir = tmp_path / "lidar_point_cloud_gb300" / "csrc"
     src_dir.mkdir(parents=True)
     prof = tmp_path / "profiles"
     prof.mkdir()
-    src = os.path.join(ROOT, "lidar_point_cloud_gb300", "csrc", "pv_voxelize.cu")
-    text = open(src, "rb").read()
-    assert bench.HOST_SIDE_MARKER in text
-    shutil.copy(src, src_dir / "pv_voxelize.cu")
+    texts = {}
+    for name in bench.KERNEL_SOURCES["pv_voxelize_kernel"]:
+        src = os.path.join(ROOT, "lidar_point_cloud_gb300", "csrc", name)
+        texts[name] = open(src, "rb").read()
+        assert bench.HOST_SIDE_MARKER in texts[name]
+        shutil.copy(src, src_dir / name)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     sha = bench.kernel_sha()
     (prof / "pv_voxelize_kernel_probe.md").write_text(
         f"# probe\n\n- dram_bytes_per_launch: `1234`\n- kernel_source_sha256: `{sha}`\n")
     assert bench.profiled_traffic("probe") == 1234
-    cut = text.index(bench.HOST_SIDE_MARKER)
-    (src_dir / "pv_voxelize.cu").write_bytes(text + b"\nstatic int host_side_edit = 0;\n")
-    assert bench.profiled_traffic("probe") == 1234
-    (src_dir / "pv_voxelize.cu").write_bytes(text[:cut] + b"// a comment in the device code\n" + text[cut:])
-    assert bench.profiled_traffic("probe") == 1234
-    (src_dir / "pv_voxelize.cu").write_bytes(text[:cut] + b"static __device__ int device_side_edit;\n" + text[cut:])
-    assert bench.profiled_traffic("probe") is None
+    for name, text in texts.items():
+        cut = text.index(bench.HOST_SIDE_MARKER)
+        (src_dir / name).write_bytes(text + b"\nstatic int host_side_edit = 0;\n")
+        assert bench.profiled_traffic("probe") == 1234
+        (src_dir / name).write_bytes(text[:cut] + b"// a comment in the device code\n" + text[cut:])
+        assert bench.profiled_traffic("probe") == 1234
+        (src_dir / name).write_bytes(text[:cut] + b"static __device__ int device_side_edit;\n" + text[cut:])
+        assert bench.profiled_traffic("probe") is None
+        (src_dir / name).write_bytes(text)
+        assert bench.profiled_traffic("probe") == 1234
