@@ -468,18 +468,23 @@ __device__ __forceinline__ unsigned long long* slot_word(unsigned long long* hea
   return w < kHead ? head + w : tail + (w - kHead);
 }
 
-// List entry: (leader index << 32) | (chunk rank << 22) | (d << 11) | size,
+// List entry: (leader index << 32) | (chunk rank << 22) | (d << 10) | (size - 1),
 // where the group's rows start in tile_rows at leader index + d (d signed,
-// 11 bits: a group lies inside its 1024-point tile) and the chunk rank is
-// below max_points <= 1024.
+// 12 bits: a group lies inside its block tile of at most 2048 points), the
+// chunk rank is below max_points <= 1024, and size is the group's point
+// count capped at max_points (1 .. 1024): no group contributes more, and a
+// capped size still tells that max_points points lie before later groups.
 __device__ __forceinline__ unsigned long long make_entry(long long leader, unsigned int crank, long long row,
                                                          unsigned int size) {
-  const unsigned int d = static_cast<unsigned int>(row - leader) & 2047u;
-  return (static_cast<unsigned long long>(leader) << 32) | (crank << 22) | (d << 11) | size;
+  const unsigned int d = static_cast<unsigned int>(row - leader) & 4095u;
+  return (static_cast<unsigned long long>(leader) << 32) | (crank << 22) | (d << 10) | (size - 1u);
 }
 __device__ __forceinline__ long long entry_row(unsigned long long ent) {
-  const int d = static_cast<int>(static_cast<unsigned int>(ent) << 10) >> 21;  // bits 11..21, sign-extended
+  const int d = static_cast<int>(static_cast<unsigned int>(ent) << 10) >> 20;  // bits 10..21, sign-extended
   return static_cast<long long>(ent >> 32) + d;
+}
+__device__ __forceinline__ unsigned int entry_size(unsigned long long ent) {
+  return (static_cast<unsigned int>(ent) & 1023u) + 1u;
 }
 __device__ __forceinline__ int entry_crank(unsigned long long ent) {
   return static_cast<int>((static_cast<unsigned int>(ent) >> 22) & 1023u);
@@ -510,7 +515,7 @@ __device__ __forceinline__ void list_insert(const ListRef& L, const uint4 (&h)[k
     if (y < x && (a == 0 || y > prev)) {
       prev = y;
       ++a;
-      before += static_cast<unsigned int>(y) & 2047u;
+      before += entry_size(y);
     } else {
       run = false;
     }
@@ -606,12 +611,13 @@ static __device__ void append_insert(const KParams& p, const ListRef& L, unsigne
 
 // ------------------------------------------------------------ block tiles
 
-// Shared-memory grouping of one block tile (kThreads consecutive points):
-// an open-addressing map slot -> map position, per (position, warp) the
-// number of the warp's points in that slot, and per position the group's
-// offset in the tile's grouped layout.  A point's rank among the tile's
-// points of its pillar is the sum over earlier warps plus its rank in its
-// own warp (lanes hold consecutive indices).
+// Shared-memory grouping of one block tile (kThreads or 2 kThreads
+// consecutive points, each warp holding a run of 32 or 64 of them): an
+// open-addressing map slot -> map position, per (position, warp) the number
+// of the warp's points in that slot, and per position the group's offset in
+// the tile's grouped layout.  A point's rank among the tile's points of its
+// pillar is the sum over earlier warps plus its rank in its own warp's run.
+// The map has a position per point of the largest tile, so it never fills.
 constexpr int kTileHash = 2 * kThreads;
 
 constexpr int kChunkHash = 4096;   // chunk map positions (see chunk_rank)
@@ -692,7 +698,7 @@ __device__ __forceinline__ unsigned int chunk_rank(int* ckey, unsigned int* ccnt
 }
 
 // Byte counters at map position h: *before = warps 0 .. warp-1, *total = all.
-// Each word holds four warps' counts (at most 32 each), summed with dp4a
+// Each word holds four warps' counts (at most 64 each), summed with dp4a
 // against ones; the words before this warp's count whole, its own word only
 // in the bytes of lower warps.
 __device__ __forceinline__ void tile_counts(const TileMap& m, int h, unsigned int warp, unsigned int* before,
@@ -775,7 +781,7 @@ __device__ __forceinline__ Head read_head(const KParams& p, const unsigned long 
     for (int j = 0; j < 3; ++j) {
       const bool good = h.e[j] != kEmpty64 && (h.e[j] >> 32) < static_cast<unsigned long long>(p.n);
       if (!filled && g == j && good) {
-        cum += static_cast<unsigned int>(h.e[j]) & 2047u;
+        cum += entry_size(h.e[j]);
         g = j + 1;
         if (cum >= static_cast<unsigned int>(p.K)) filled = true;
       }
@@ -797,7 +803,7 @@ __device__ __forceinline__ Head read_head(const KParams& p, const unsigned long 
   for (int j = 0; j < 4; ++j) {
     const bool good = h.e[j] != kEmpty64 && (h.e[j] >> 32) < static_cast<unsigned long long>(p.n);
     if (!filled && g == j && good) {
-      cum += static_cast<unsigned int>(h.e[j]) & 2047u;
+      cum += entry_size(h.e[j]);
       g = j + 1;
       if (cum >= static_cast<unsigned int>(p.K)) filled = true;
     } else if (!filled && h.e[j] != kEmpty64) {
@@ -831,7 +837,7 @@ __device__ __forceinline__ CopyDesc copy_desc(const Head& h) {
     const unsigned long long ej = h.e[j];
     d.o[j] = static_cast<int>(entry_row(ej) - static_cast<long long>(run));
     st[j] = j < h.ng ? (run < h.n ? run : h.n) : h.n;
-    run += static_cast<unsigned int>(ej) & 2047u;
+    run += entry_size(ej);  // (unused past the groups present)
   }
   d.w0 = h.n | (st[1] << 16);
   d.w1 = st[2] | (st[3] << 16);
@@ -859,7 +865,7 @@ static __device__ unsigned int emit_groups(const KParams& p, const ListRef& L, f
   unsigned int written = 0;
   if (K <= 32 && (present & (present + 1u)) == 0u) {
     const int G = __popc(present);
-    const unsigned int size = ent != kEmpty64 ? (static_cast<unsigned int>(ent) & 2047u) : 0u;
+    const unsigned int size = ent != kEmpty64 ? entry_size(ent) : 0u;
     unsigned int incl = size;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -902,9 +908,9 @@ static __device__ unsigned int emit_groups(const KParams& p, const ListRef& L, f
     const unsigned int here = __ballot_sync(0xffffffffu, chunk != kEmpty64);
     for (unsigned int m = here; m != 0u && written < static_cast<unsigned int>(K); m &= m - 1u) {
       const unsigned long long ge = __shfl_sync(0xffffffffu, chunk, __ffs(m) - 1);
-      const unsigned int info = static_cast<unsigned int>(ge);
+      const unsigned int gsz = entry_size(ge);
       const unsigned int room = static_cast<unsigned int>(K) - written;
-      const unsigned int n = (info & 2047u) < room ? (info & 2047u) : room;
+      const unsigned int n = gsz < room ? gsz : room;
       const long long base = entry_row(ge);
       for (unsigned int j = lane; j < n; j += 32) orow[written + j] = __ldcg(p.tile_rows + base + j);
       written += n;
@@ -1010,7 +1016,7 @@ static __device__ unsigned int emit_app(const KParams& p, const ListRef& L, floa
   }
   const unsigned int present = __ballot_sync(0xffffffffu, ent != kEmpty64);
   const int G = __popc(present);
-  const unsigned int size = ent != kEmpty64 ? (static_cast<unsigned int>(ent) & 2047u) : 0u;
+  const unsigned int size = ent != kEmpty64 ? entry_size(ent) : 0u;
   unsigned int incl = size;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -1081,7 +1087,7 @@ static __device__ bool emit_app_quad(const KParams& p, unsigned long long qe, bo
       ent = (lower == up) ? mn : mx;
     }
   }
-  const unsigned int sz = ent != kEmpty64 ? (static_cast<unsigned int>(ent) & 2047u) : 0u;
+  const unsigned int sz = ent != kEmpty64 ? entry_size(ent) : 0u;
   unsigned int incl = sz;
 #pragma unroll
   for (int d = 1; d < 8; d <<= 1) {

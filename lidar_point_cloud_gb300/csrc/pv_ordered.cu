@@ -10,7 +10,8 @@
 //   * one cooperative launch, one 1024-thread block per SM, all resident,
 //     and two grid-wide barriers;
 //   * phase 1 (before the first barrier): blocks sweep the cloud in tiles of
-//     1024 consecutive points, in index order across the grid.  Each point is
+//     1024 consecutive points (2048, two a thread, where a block's chunk
+//     spans several tiles), in index order across the grid.  Each point is
 //     read with one 16-byte load and binned with IEEE round-to-nearest
 //     subtract/divide and floorf.  In shared memory the tile is grouped by
 //     pillar (warp match + a small open-addressing map), which gives every
@@ -58,8 +59,20 @@ namespace {
 // NF = 1: one cloud (pv_voxelize); NF = kMaxFrames: a batch of up to NF
 // frames (pv_voxelize_batch), where a voxel's id carries its frame, each
 // frame keeps its own first max_voxels voxels and writes its own rows.
-template <int NF, bool kQueue>
+// U: points per thread in a block tile at most.  A tile of S sub-tiles
+// (S <= U) is S * kThreads consecutive points; warp w holds its points
+// 32S.w .. 32S.w + 32S - 1, sub-tile u the 32 of them from 32S.w + 32u.
+// With U = 2 a block's chunk starts with a one-sub-tile tile, and each next
+// tile takes two sub-tiles while the last one had few tile groups (at most
+// 512 per 1024 points to widen, 1280 per 2048 to stay wide), so the maps
+// stay at most 5/8 full: wide tiles halve the block barriers per point and
+// the tile groups per pillar on clouds whose consecutive points share
+// pillars; sparse clouds keep 1024-point tiles.
+template <int NF, bool kQueue, int U>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(const KParams p, const Frames<NF> fr) {
+  static_assert(U == 1 || U == 2, "one or two points per thread in a tile");
+  static_assert(U * kThreads <= kTileHash, "a tile's keys fit its map");
+  constexpr int kTile = U * kThreads;
   constexpr bool kBatched = NF > 1;
   // Block tiles in flight in the first-point pass: 8 where chunks are long
   // (the launches that queue long lists), else 4 (fewer empty tiles to scan).
@@ -75,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   __shared__ int s_flag;
   __shared__ unsigned int s_dirty;
   __shared__ unsigned int s_layout[2];
+  __shared__ unsigned int s_groups[2];  // tile groups (distinct pillars) of the tile using each map
   __shared__ unsigned int s_nrec;
   __shared__ unsigned int s_qn, s_qh;  // gather: long lists queued by the block, and taken
 
@@ -95,7 +109,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   // control block's words are in flight.
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   long long tb = begin;  // this block's contiguous chunk, in tiles from its start
-  float4 q = (tb + tid < end) ? __ldg(p.points + tb + tid) : z4;
+  int nsub = 1;  // sub-tiles of the current tile (see U)
+  float4 q[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) q[u] = z4;
+  if (tb + 32u * warp + lane < end) q[0] = __ldg(p.points + tb + 32u * warp + lane);
   // Thread 0 alone reads the control block (the same word read by every
   // thread would queue thousands of requests on one L2 line); the dirty flag
   // reaches the block through shared memory, the epoch only thread 0 needs.
@@ -110,7 +128,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   if (kBatched)
     for (int b = static_cast<int>(tid); b <= B; b += kThreads) s_off[b] = fr.off[b];  // read after a block barrier
   PV_STAMP(0);
-  const bool multi = end - begin > kThreads;  // more than one tile: second map and chunk map in use
+  // More than one tile (always so with U = 2): second map, chunk map and records in use.
+  const bool multi = U > 1 || end - begin > kThreads;
   int* ckey = reinterpret_cast<int*>(s_dyn + 2 * kMapBytes);
   unsigned int* ccnt = reinterpret_cast<unsigned int*>(ckey + kChunkHash);
   {  // tile map 0 empty (counters zero, keys -1); map 1 and the chunk map only if used
@@ -134,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   }
   if (tid == 0) {
     s_layout[0] = s_layout[1] = 0;
+    s_groups[0] = s_groups[1] = 0;
     s_nrec = 0;
     s_qn = s_qh = 0;
     s_dirty = dirty_word;
@@ -163,66 +183,120 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     int buf = 0;
     int own_rs = -1;                  // one-tile chunk: the record this thread leads, if any
     unsigned long long own_entry = 0;
-    for (; tb < end; tb += kThreads, buf ^= 1) {
+    for (; tb < end; buf ^= 1) {
 #ifdef PV_INSTRUMENT
       const bool first_tile = tb == begin;
 #endif
       PV_SUB(0);
       const TileMap tm = tile_map(s_dyn + buf * kMapBytes, &s_layout[buf]);
       const TileMap prev = tile_map(s_dyn + (buf ^ 1) * kMapBytes, &s_layout[buf ^ 1]);
-      const long long i = tb + tid;
-      const long long inext = i + kThreads;
-      const float4 qn = inext < end ? __ldg(p.points + inext) : z4;  // next tile, in flight early
-      int slot = -1;
-      if (i < end) {
-        int key;
-        if (bin_point(q, p, &key)) {
-          if (kBatched) key += frame_of(s_off, B, i) * p.cells;
-          slot = p.hash_mode ? claim_slot(p.keys, p.table_mask, key) : key;
-          if (slot < 0) atomicMin(&p.ctl->err, PV_ERR_CAPACITY);
+      const unsigned int wofs = 32u * nsub * warp + lane;  // this thread's first point in the tile
+      const long long tl = static_cast<long long>(nsub) * kThreads;
+      long long i[U];
+      float4 qn[U];
+      int slot[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        i[u] = u < nsub ? tb + wofs + 32 * u : end;
+        const long long inext = i[u] + tl;  // the next tile's point if it has as many sub-tiles
+        qn[u] = (u < nsub && inext < end) ? __ldg(p.points + inext) : z4;  // in flight early
+        slot[u] = -1;
+        if (i[u] < end) {
+          int key;
+          if (bin_point(q[u], p, &key)) {
+            if (kBatched) key += frame_of(s_off, B, i[u]) * p.cells;
+            slot[u] = p.hash_mode ? claim_slot(p.keys, p.table_mask, key) : key;
+            if (slot[u] < 0) atomicMin(&p.ctl->err, PV_ERR_CAPACITY);
+          }
         }
       }
       PV_SUB(1);
-      const unsigned int peers = __match_any_sync(0xffffffffu, slot);
-      const int leader = __ffs(peers) - 1;
-      int h = -1;
-      if (slot >= 0 && static_cast<int>(lane) == leader) {
-        h = tile_claim(tm, slot);
-        if (h >= 0) {
-          reinterpret_cast<unsigned char*>(tm.cnt + h * (kWarps / 4))[warp] =
-              static_cast<unsigned char>(__popc(peers));
-        } else {  // cannot happen: at most kThreads keys in 2 * kThreads positions
-          atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
+      // Warp groups register in the tile map: per (position, warp) a byte
+      // counts the warp's points of the pillar.  With U = 2 the counter is
+      // added to atomically and sub-tile 1 reads how many of the warp's
+      // sub-tile 0 points share its pillar (they come first).
+      unsigned int peers[U], wb[U];
+      int h[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (u >= nsub) {  // (block-uniform)
+          peers[u] = 0u;
+          wb[u] = 0u;
+          h[u] = -1;
+          continue;
         }
+        peers[u] = __match_any_sync(0xffffffffu, slot[u]);
+        const int leader = __ffs(peers[u]) - 1;
+        int hh = -1;
+        unsigned int old = 0;
+        if (slot[u] >= 0 && static_cast<int>(lane) == leader) {
+          hh = tile_claim(tm, slot[u]);
+          if (hh >= 0) {
+            if constexpr (U == 1) {
+              reinterpret_cast<unsigned char*>(tm.cnt + hh * (kWarps / 4))[warp] =
+                  static_cast<unsigned char>(__popc(peers[u]));
+            } else {
+              const unsigned int sh = 8u * (warp & 3u);
+              old = atomicAdd(tm.cnt + hh * (kWarps / 4) + (warp >> 2), static_cast<unsigned int>(__popc(peers[u])) << sh);
+              old = (old >> sh) & 0xFFu;
+            }
+          } else {  // cannot happen: at most kTile keys in kTileHash >= kTile positions
+            atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
+          }
+        }
+        h[u] = __shfl_sync(0xffffffffu, hh, leader);
+        wb[u] = U == 1 ? 0u : __shfl_sync(0xffffffffu, old, leader);
+        if (h[u] < 0) slot[u] = -1;
+        if (U > 1) __syncwarp();  // sub-tile u's counts land before sub-tile u + 1 reads them
       }
-      h = __shfl_sync(0xffffffffu, h, leader);
-      if (h < 0) slot = -1;
       __syncthreads();  // (A) every warp group registered; the previous tile's map is read
       PV_SUB(2);
       // Empty the previous tile's map (used again by the next tile, after barrier B).
       if (multi) {
-        if (tid == 0) *prev.layout = 0;
+        if (tid == 0) {
+          *prev.layout = 0;
+          s_groups[buf ^ 1] = 0;
+        }
         tile_clear(prev, tid);
       }
-      // The group's counts before this warp and in all: read by the leader,
-      // shared with the group (one warp) by shuffles.
-      unsigned int trank = 0, tot = 0;
-      if (slot >= 0 && static_cast<int>(lane) == leader) tile_counts(tm, h, warp, &trank, &tot);
-      trank = __shfl_sync(0xffffffffu, trank, leader);
-      tot = __shfl_sync(0xffffffffu, tot, leader);
-      if (slot >= 0) trank += __popc(peers & lanemask_lt());
-      const bool lead = slot >= 0 && trank == 0;
-      const unsigned int cseen = (lead && multi) ? chunk_rank(ckey, ccnt, slot, tot) : 0u;
-      const int crank = static_cast<int>(cseen >> 16);
+      // Per point: its rank among the tile's points of its pillar; the
+      // group's counts before this warp and in all are read by the leader
+      // and shared by shuffles.  A group's first point (rank 0) leads it.
+      unsigned int trank[U], tot[U], cseen[U];
+      bool lead[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (u >= nsub) {  // (block-uniform)
+          trank[u] = tot[u] = cseen[u] = 0u;
+          lead[u] = false;
+          continue;
+        }
+        const int leader = __ffs(peers[u]) - 1;
+        unsigned int tr = 0, tt = 0;
+        if (slot[u] >= 0 && static_cast<int>(lane) == leader) tile_counts(tm, h[u], warp, &tr, &tt);
+        tr = __shfl_sync(0xffffffffu, tr, leader);
+        tt = __shfl_sync(0xffffffffu, tt, leader);
+        if (slot[u] >= 0) tr += wb[u] + __popc(peers[u] & lanemask_lt());
+        trank[u] = tr;
+        tot[u] = tt;
+        lead[u] = slot[u] >= 0 && tr == 0;
+        cseen[u] = (lead[u] && multi) ? chunk_rank(ckey, ccnt, slot[u], tt) : 0u;
+      }
       {  // group offsets and record slots: one shared-memory atomic per warp each
-        const unsigned int need = lead ? tot : 0u;
         // A group with max_points of its pillar's points before it in this
         // chunk (or max_points groups) can never be kept: not recorded.
-        const unsigned int wants =
-            (lead && crank < K && (cseen & 0xFFFFu) < static_cast<unsigned int>(K)) ? 1u : 0u;
-        // One scan for both: a warp's groups hold at most kThreads points
-        // (low half) and it has at most 32 records (high half).
-        unsigned int pk = need | (wants << 16);
+        unsigned int need = 0, nrec_l = 0;
+        bool wants[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          wants[u] = lead[u] && (cseen[u] >> 16) < static_cast<unsigned int>(K) &&
+                     (cseen[u] & 0xFFFFu) < static_cast<unsigned int>(K);
+          need += lead[u] ? tot[u] : 0u;
+          nrec_l += (multi && wants[u]) ? 1u : 0u;
+        }
+        // One scan for both: a warp's groups hold at most kTile points (low
+        // half) and it has at most 32U records (high half).
+        unsigned int pk = need | (nrec_l << 16);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const unsigned int y = __shfl_up_sync(0xffffffffu, pk, o);
@@ -238,35 +312,66 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         }
         base = __shfl_sync(0xffffffffu, base, 31);
         rbase = __shfl_sync(0xffffffffu, rbase, 31);
-        if (lead) {
-          const unsigned int off = base + incl - need;
-          // Rows of the group that can ever be emitted: those with fewer than
-          // max_points of the pillar's points before them in the chunk.
-          const unsigned int cpts = cseen & 0xFFFFu;
-          const unsigned int room = cpts < static_cast<unsigned int>(K) ? static_cast<unsigned int>(K) - cpts : 0u;
-          tm.off[h] = ((tot < room ? tot : room) << 16) | off;
-          if (wants) {
-            const unsigned long long ent = make_entry(i, static_cast<unsigned int>(crank), tb + off, tot);
-            if (multi) {
-              const long long rj = begin + rbase + rincl - wants;
-              p.firsts[rj] = slot;  // the record's slot (firsts is rewritten after the barrier)
-              p.recs[rj] = ent;
-            } else {  // one tile: the leader inserts its own record
-              own_rs = slot;
-              own_entry = ent;
+        if constexpr (U > 1) {  // the tile's groups, which set the next tile's width
+          unsigned int ng = __popc(__ballot_sync(0xffffffffu, lead[0]));
+          if (nsub > 1) ng += __popc(__ballot_sync(0xffffffffu, lead[1]));
+          if (lane == 0 && ng) atomicAdd(&s_groups[buf], ng);
+        }
+        unsigned int off = base + incl - need;
+        long long rj = begin + rbase + rincl - nrec_l;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (lead[u]) {
+            // Rows of the group that can ever be emitted: those with fewer than
+            // max_points of the pillar's points before them in the chunk.
+            const unsigned int cpts = cseen[u] & 0xFFFFu;
+            const unsigned int room = cpts < static_cast<unsigned int>(K) ? static_cast<unsigned int>(K) - cpts : 0u;
+            tm.off[h[u]] = ((tot[u] < room ? tot[u] : room) << 16) | off;
+            if (wants[u]) {
+              const unsigned int size = tot[u] < static_cast<unsigned int>(K) ? tot[u] : static_cast<unsigned int>(K);
+              const unsigned long long ent = make_entry(i[u], cseen[u] >> 16, tb + off, size);
+              if (multi) {
+                p.firsts[rj] = slot[u];  // the record's slot (firsts is rewritten after the barrier)
+                p.recs[rj] = ent;
+                ++rj;
+              } else {  // one tile (U = 1): the leader inserts its own record
+                own_rs = slot[u];
+                own_entry = ent;
+              }
             }
+            off += tot[u];
           }
         }
       }
-      if (i < end) p.slot_of_point[i] = slot < 0 ? -1 : (lead ? (slot | kLeaderBit) : slot);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (i[u] < end) p.slot_of_point[i[u]] = slot[u] < 0 ? -1 : (lead[u] ? (slot[u] | kLeaderBit) : slot[u]);
       __syncthreads();  // (B) group offsets handed out; the previous map is empty
       PV_SUB(3);
-      if (slot >= 0) {
-        const unsigned int ow = tm.off[h];
-        if (trank < (ow >> 16)) p.tile_rows[tb + (ow & 0xFFFFu) + trank] = q;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (slot[u] >= 0) {
+          const unsigned int ow = tm.off[h[u]];
+          if (trank[u] < (ow >> 16)) p.tile_rows[tb + (ow & 0xFFFFu) + trank[u]] = q[u];
+        }
       }
       PV_SUB(4);
-      q = qn;
+      tb += tl;
+      int next = 1;
+      if constexpr (U > 1) {  // this tile's groups are all counted (barrier B)
+        const unsigned int g = s_groups[buf];
+        next = (nsub == 1 ? g <= 512u : g <= 1280u) ? 2 : 1;
+      }
+      if (next == nsub) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) q[u] = qn[u];
+      } else {  // another width: the prefetched points are not the next tile's
+        nsub = next;
+        const unsigned int w2 = 32u * nsub * warp + lane;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          q[u] = (u < nsub && tb + w2 + 32 * u < end) ? __ldg(p.points + tb + w2 + 32 * u) : z4;
+      }
     }
     __syncthreads();  // every record written
 #ifdef PV_INSTRUMENT
@@ -671,39 +776,45 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
 
 // ------------------------------------------------------------ host side
 
-int prepare_ordered() {
-  int single = 0, queued = 0, batched = 0;
-  if (cudaFuncSetAttribute(pv_voxelize_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(pv_voxelize_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(pv_voxelize_kernel<kMaxFrames, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kDynSmem) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&single, pv_voxelize_kernel<1, false>, kThreads, kDynSmem) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&queued, pv_voxelize_kernel<1, true>, kThreads, kDynSmem) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&batched, pv_voxelize_kernel<kMaxFrames, false>, kThreads,
-                                                    kDynSmem) != cudaSuccess) {
+template <typename F>
+static int prepare_one(F kern) {
+  int blocks = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, kThreads, kDynSmem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  const int m = single < queued ? single : queued;
-  return m < batched ? m : batched;
+  return blocks;
 }
 
+int prepare_ordered() {
+  const int b[6] = {prepare_one(pv_voxelize_kernel<1, false, 1>), prepare_one(pv_voxelize_kernel<1, true, 1>),
+                    prepare_one(pv_voxelize_kernel<1, false, 2>), prepare_one(pv_voxelize_kernel<1, true, 2>),
+                    prepare_one(pv_voxelize_kernel<kMaxFrames, false, 1>),
+                    prepare_one(pv_voxelize_kernel<kMaxFrames, false, 2>)};
+  int m = b[0];
+  for (int k = 1; k < 6; ++k) m = b[k] < m ? b[k] : m;
+  return m;
+}
+
+// Launches whose block chunks span more than one 1024-point tile group
+// them in tiles of 1024 or 2048 points (U = 2), chosen tile by tile.
 cudaError_t launch_ordered(const cudaLaunchConfig_t& cfg, const KParams& kp, bool queue,
                            const int64_t* frame_offsets, int frames, long long n) {
   if (!frame_offsets) {
     Frames<1> fr;
     fr.off[0] = 0;
     fr.off[1] = n;
-    return queue ? cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1, true>, kp, fr)
-                 : cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1, false>, kp, fr);
+    if (kp.chunk > kThreads)
+      return queue ? cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1, true, 2>, kp, fr)
+                   : cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1, false, 2>, kp, fr);
+    return queue ? cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1, true, 1>, kp, fr)
+                 : cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<1, false, 1>, kp, fr);
   }
   Frames<kMaxFrames> fr;  // copied into the launch: the caller's array may go at once
   for (int b = 0; b <= kMaxFrames; ++b) fr.off[b] = b <= frames ? frame_offsets[b] : n;
-  return cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<kMaxFrames, false>, kp, fr);
+  if (kp.chunk > kThreads) return cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<kMaxFrames, false, 2>, kp, fr);
+  return cudaLaunchKernelEx(&cfg, pv_voxelize_kernel<kMaxFrames, false, 1>, kp, fr);
 }
 
 }  // namespace pvk

@@ -89,20 +89,50 @@ def test_random_tiny_clouds():
 
 def test_chunk_sizes_around_tile_boundaries():
     # Each block owns ceil(N / blocks) points rounded up to a warp and sweeps
-    # them in 1024-point tiles from its own start, so tiles start anywhere and
-    # a chunk may end with a short tile.  Sizes that make the chunk one warp,
-    # exactly one tile, one tile and a warp, and two tiles and a warp; the
-    # points are KITTI-shaped returns repeated in sensor order, so pillars
-    # span tile and chunk boundaries.
+    # them in tiles from its own start: 1024-point tiles while the chunk is
+    # one tile, else 2048-point tiles (two points a thread), so tiles start
+    # anywhere and a chunk may end with a short tile, or one whose second
+    # half is empty.  Sizes that make the chunk one warp, exactly one small
+    # tile, one small tile and a warp (one wide tile, half empty), one wide
+    # tile, one wide tile and a warp, two wide tiles and a warp; the points
+    # are KITTI-shaped returns repeated in sensor order, so pillars span
+    # tile and chunk boundaries.
     P = synth.KITTI_PARAMS
     base, _ = synth.make("kitti")
     ctas = pv.query_plan(len(base), P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)["ctas"]
     for want_chunk, n in [(32, 32 * ctas - 7), (1024, 1024 * ctas - 3), (1056, 1024 * ctas + 1),
-                          (2080, 2048 * ctas + 40)]:
+                          (2048, 2048 * ctas - 5), (2080, 2048 * ctas + 40), (4128, 4096 * ctas + 40)]:
         plan = pv.query_plan(n, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
         assert plan["points_per_cta"] == want_chunk, (n, plan["points_per_cta"])
         pts = np.tile(base, (n // len(base) + 1, 1))[:n]
         assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+
+
+def test_sparse_chunks_of_several_tiles():
+    # About six 1024-point tiles a chunk, uniform over a 2048 x 2048 grid of
+    # 0.05 m pillars: nearly every point of a tile has its own pillar, so
+    # the chunks keep 1024-point tiles (their maps half full), and the
+    # pillar budget binds.  Direct and hashed tables.
+    r, v = synth.DENSE_RANGE, synth.ADV_VOXEL
+    ctas = pv.query_plan(1 << 20, r, v, 32, 200_000)["ctas"]
+    n = 3 * 2048 * ctas + 77
+    pts = synth.uniform(n, 41, pc_range=r)
+    for mode in (0, 2):
+        assert_parity(pts, r, v, 32, 200_000, table_mode=mode)
+
+
+@pytest.mark.parametrize("run", [700, 3000])
+def test_tile_width_switches(run):
+    # Runs of `run` sensor-ordered returns of the dense frame (few pillars a
+    # tile: tiles widen to 2048 points) alternating with runs of uniform
+    # points over the same grid (a pillar a point: tiles narrow to 1024), so
+    # chunks change tile width both ways, with tiles straddling the runs.
+    P = synth.DENSE_PARAMS
+    dense, _ = synth.make("dense")
+    uni = synth.uniform(dense.shape[0], 43, pc_range=P.point_cloud_range)
+    k = np.arange(dense.shape[0]) // run
+    pts = np.where((k % 2 == 0)[:, None], dense, uni).astype(np.float32)
+    assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
 
 
 def test_determinism_repeats():
