@@ -568,7 +568,10 @@ static __device__ void append_insert(const KParams& p, const ListRef& L, unsigne
   const int S = kHead + p.KT;
   unsigned int* w0 = reinterpret_cast<unsigned int*>(L.head);
   const unsigned int j = ~atomicAdd(w0, 0xFFFFFFFFu);  // the count is kept complemented
-  atomicMin(w0 + 1, static_cast<unsigned int>(x >> 32));
+  // Only a chunk's first group of the pillar (chunk rank 0, also what a
+  // full chunk map reports) can hold the lowest leader: the chunk's other
+  // groups come after it.
+  if (entry_crank(x) == 0) atomicMin(w0 + 1, static_cast<unsigned int>(x >> 32));
   if (j < static_cast<unsigned int>(S - 2)) {
     *slot_word(L.head, L.tail, 1 + static_cast<int>(j)) = x;
     return;

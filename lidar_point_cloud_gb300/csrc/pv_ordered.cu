@@ -72,7 +72,6 @@ template <int NF, bool kQueue, int U>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(const KParams p, const Frames<NF> fr) {
   static_assert(U == 1 || U == 2, "one or two points per thread in a tile");
   static_assert(U * kThreads <= kTileHash, "a tile's keys fit its map");
-  constexpr int kTile = U * kThreads;
   constexpr bool kBatched = NF > 1;
   // Block tiles in flight in the first-point pass: 8 where chunks are long
   // (the launches that queue long lists), else 4 (fewer empty tiles to scan).
@@ -240,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
               old = atomicAdd(tm.cnt + hh * (kWarps / 4) + (warp >> 2), static_cast<unsigned int>(__popc(peers[u])) << sh);
               old = (old >> sh) & 0xFFu;
             }
-          } else {  // cannot happen: at most kTile keys in kTileHash >= kTile positions
+          } else {  // cannot happen: at most U * kThreads keys in kTileHash >= U * kThreads positions
             atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
           }
         }
@@ -294,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           need += lead[u] ? tot[u] : 0u;
           nrec_l += (multi && wants[u]) ? 1u : 0u;
         }
-        // One scan for both: a warp's groups hold at most kTile points (low
+        // One scan for both: a warp's groups hold at most U * kThreads points (low
         // half) and it has at most 32U records (high half).
         unsigned int pk = need | (nrec_l << 16);
 #pragma unroll
