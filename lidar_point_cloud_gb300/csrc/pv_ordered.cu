@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   __shared__ unsigned int s_groups[2];  // tile groups (distinct pillars) of the tile using each map
   __shared__ unsigned int s_nrec;
   __shared__ unsigned int s_qn, s_qh;  // gather: long lists queued by the block, and taken
+  __shared__ unsigned int s_wrec[kWarps];  // single frame: records of each warp in the current tile
 
   const unsigned int P = gridDim.x;
   const unsigned int cta = blockIdx.x;
@@ -167,6 +168,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     bar_target += P;
   }
 
+  // A single frame's chunk of several tiles lays its records out in index
+  // order (tile by tile; in a tile by warp, sub-tile, lane), with their slots
+  // in slot_of_point: the first-point pass then walks the records instead of
+  // the points.  A batch records in arrival order, with the slots in firsts,
+  // and tags every point in slot_of_point, as does a chunk of one tile.
+  int32_t* const rec_slot = kBatched ? p.firsts : p.slot_of_point;
+
   // ---- phase 1a: bin every point; lay each block tile out grouped by pillar
   // (groups in any order inside the tile, points of a group in index order)
   // and record one entry per (pillar, tile) group, with the group's rank among
@@ -182,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     int buf = 0;
     int own_rs = -1;                  // one-tile chunk: the record this thread leads, if any
     unsigned long long own_entry = 0;
+    unsigned int rec_run = 0;  // single frame: records of the chunk's earlier tiles
     for (; tb < end; buf ^= 1) {
 #ifdef PV_INSTRUMENT
       const bool first_tile = tb == begin;
@@ -281,6 +290,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         lead[u] = slot[u] >= 0 && tr == 0;
         cseen[u] = (lead[u] && multi) ? chunk_rank(ckey, ccnt, slot[u], tt) : 0u;
       }
+      unsigned int rpos[U];         // single frame: each record's place among its warp's records
+      unsigned long long rent[U];  // single frame: the records, written after barrier B
       {  // group offsets and record slots: one shared-memory atomic per warp each
         // A group with max_points of its pillar's points before it in this
         // chunk (or max_points groups) can never be kept: not recorded.
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           wants[u] = lead[u] && (cseen[u] >> 16) < static_cast<unsigned int>(K) &&
                      (cseen[u] & 0xFFFFu) < static_cast<unsigned int>(K);
           need += lead[u] ? tot[u] : 0u;
-          nrec_l += (multi && wants[u]) ? 1u : 0u;
+          nrec_l += (kBatched && multi && wants[u]) ? 1u : 0u;
         }
         // One scan for both: a warp's groups hold at most U * kThreads points (low
         // half) and it has at most 32U records (high half).
@@ -318,8 +329,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         }
         unsigned int off = base + incl - need;
         long long rj = begin + rbase + rincl - nrec_l;
+        if (!kBatched && multi) {  // this warp's records: their places in it, its count to the block
+          unsigned int wr = 0;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const unsigned int bw = u < nsub ? __ballot_sync(0xffffffffu, wants[u]) : 0u;
+            rpos[u] = wr + __popc(bw & lanemask_lt());
+            wr += __popc(bw);
+          }
+          if (lane == 0) s_wrec[warp] = wr;
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+          rent[u] = kEmpty64;
           if (lead[u]) {
             // Rows of the group that can ever be emitted: those with fewer than
             // max_points of the pillar's points before them in the chunk.
@@ -329,24 +351,42 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
             if (wants[u]) {
               const unsigned int size = tot[u] < static_cast<unsigned int>(K) ? tot[u] : static_cast<unsigned int>(K);
               const unsigned long long ent = make_entry(i[u], cseen[u] >> 16, tb + off, size);
-              if (multi) {
+              if (!multi) {  // one tile (U = 1): the leader inserts its own record
+                own_rs = slot[u];
+                own_entry = ent;
+              } else if (!kBatched) {
+                rent[u] = ent;  // written once the block's warp counts are known (barrier B)
+              } else {
                 p.firsts[rj] = slot[u];  // the record's slot (firsts is rewritten after the barrier)
                 p.recs[rj] = ent;
                 ++rj;
-              } else {  // one tile (U = 1): the leader inserts its own record
-                own_rs = slot[u];
-                own_entry = ent;
               }
             }
             off += tot[u];
           }
         }
       }
+      if (kBatched || !multi) {  // slot tags for the first-point pass over points
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (i[u] < end) p.slot_of_point[i[u]] = slot[u] < 0 ? -1 : (lead[u] ? (slot[u] | kLeaderBit) : slot[u]);
+        for (int u = 0; u < U; ++u)
+          if (i[u] < end) p.slot_of_point[i[u]] = slot[u] < 0 ? -1 : (lead[u] ? (slot[u] | kLeaderBit) : slot[u]);
+      }
       __syncthreads();  // (B) group offsets handed out; the previous map is empty
       PV_SUB(3);
+      if (!kBatched && multi) {  // this tile's records, after the chunk's earlier ones, in index order
+        const unsigned int cw = s_wrec[lane];
+        const unsigned int wbase = __reduce_add_sync(0xffffffffu, lane < warp ? cw : 0u);
+        const unsigned int ttot = __reduce_add_sync(0xffffffffu, cw);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (rent[u] != kEmpty64) {
+            const long long r = begin + rec_run + wbase + rpos[u];
+            rec_slot[r] = slot[u];
+            p.recs[r] = rent[u];
+          }
+        }
+        rec_run += ttot;
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (slot[u] >= 0) {
@@ -372,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           q[u] = (u < nsub && tb + w2 + 32 * u < end) ? __ldg(p.points + tb + w2 + 32 * u) : z4;
       }
     }
+    if (!kBatched && multi && tid == 0) s_nrec = rec_run;
     __syncthreads();  // every record written
 #ifdef PV_INSTRUMENT
     if (tid == 0 && cta < kStampCtas) g_p1_ns[cta][5] = global_timer_ns();
@@ -396,11 +437,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       }
     } else {
       unsigned int j0 = tid;
-      int rs = j0 < nrec ? __ldcg(p.firsts + begin + j0) : -1;
+      int rs = j0 < nrec ? __ldcg(rec_slot + begin + j0) : -1;
       unsigned long long entry = j0 < nrec ? __ldcg(p.recs + begin + j0) : 0ull;
       for (; j0 < nrec; j0 += kThreads) {
         const unsigned int j1 = j0 + kThreads;
-        const int rs1 = j1 < nrec ? __ldcg(p.firsts + begin + j1) : -1;
+        const int rs1 = j1 < nrec ? __ldcg(rec_slot + begin + j1) : -1;
         const unsigned long long entry1 = j1 < nrec ? __ldcg(p.recs + begin + j1) : 0ull;
         if (p.append) {
           append_insert(p, list_of(p, rs), entry, static_cast<uint32_t>(begin), static_cast<uint32_t>(end - begin));
@@ -427,46 +468,88 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   if (alive) {
     // ---- phase 2a: first points of this block's range, compacted in index order.
     unsigned int local = 0;
-    for (long long base = begin; base < end; base += static_cast<long long>(FU) * kThreads) {
-      int s[FU];
-      uint32_t head[FU];
+    if (!kBatched && multi) {
+      // Over the chunk's records, in index order: a pillar's first point
+      // leads the first group of the pillar in its chunk (chunk rank 0), so
+      // only those records are tested against the slot's lowest leader.
+      constexpr int FR = FU;
+      const unsigned int nrec = s_nrec;
+      for (unsigned int r0 = 0; r0 < nrec; r0 += FR * kThreads) {
+        int s[FR];
+        unsigned long long e[FR];
 #pragma unroll
-      for (int u = 0; u < FU; ++u) {
-        const long long i = base + u * kThreads + tid;
-        s[u] = i < end ? __ldcg(p.slot_of_point + i) : -1;
-      }
-#pragma unroll
-      for (int u = 0; u < FU; ++u) {
-        // Only a tile-group leader can be its pillar's first point.
-        head[u] = (s[u] >= 0 && (s[u] & kLeaderBit))
-                      ? static_cast<uint32_t>(__ldcg(p.lists + static_cast<size_t>(s[u] & ~kLeaderBit) * kHead) >> 32)
-                      : kEmpty;
-        s[u] = s[u] >= 0 ? (s[u] & ~kLeaderBit) : -1;
-      }
-      unsigned int ball[FU];
-#pragma unroll
-      for (int u = 0; u < FU; ++u) {
-        const long long i = base + u * kThreads + tid;
-        ball[u] = __ballot_sync(0xffffffffu, s[u] >= 0 && head[u] == static_cast<uint32_t>(i));
-        if (lane == 0) s_tile[u][warp] = __popc(ball[u]);
-      }
-      __syncthreads();
-      if (warp == 0) flag_prefix<FU>(&s_tile[0][0], &s_tmp[kWarps], lane);
-      __syncthreads();
-      unsigned int run = local;
-#pragma unroll
-      for (int u = 0; u < FU; ++u) {
-        const unsigned int before = run + s_tile[u][warp] + __popc(ball[u] & lanemask_lt());
-        if ((ball[u] >> lane) & 1u) p.firsts[begin + before] = s[u];
-        if (kBatched) {  // a frame start at i records this block's first points before it
-          const long long i = base + u * kThreads + tid;
-          if (i < end)
-            for (int b = frame_of(s_off, B, i); b >= 1 && s_off[b] == i; --b) p.frame_cnt[b] = before;
+        for (int u = 0; u < FR; ++u) {
+          const unsigned int r = r0 + u * kThreads + tid;
+          s[u] = r < nrec ? __ldcg(rec_slot + begin + r) : -1;
+          e[u] = r < nrec ? __ldcg(p.recs + begin + r) : kEmpty64;
         }
+        uint32_t head[FR];
+#pragma unroll
+        for (int u = 0; u < FR; ++u)
+          head[u] = (s[u] >= 0 && entry_crank(e[u]) == 0)
+                        ? static_cast<uint32_t>(__ldcg(p.lists + static_cast<size_t>(s[u]) * kHead) >> 32)
+                        : kEmpty;
+        unsigned int ball[FR];
+#pragma unroll
+        for (int u = 0; u < FR; ++u) {
+          ball[u] = __ballot_sync(0xffffffffu, s[u] >= 0 && head[u] == static_cast<uint32_t>(e[u] >> 32));
+          if (lane == 0) s_tile[u][warp] = __popc(ball[u]);
+        }
+        __syncthreads();
+        if (warp == 0) flag_prefix<FR>(&s_tile[0][0], &s_tmp[kWarps], lane);
+        __syncthreads();
+        unsigned int run = local;
+#pragma unroll
+        for (int u = 0; u < FR; ++u) {
+          const unsigned int before = run + s_tile[u][warp] + __popc(ball[u] & lanemask_lt());
+          if ((ball[u] >> lane) & 1u) p.firsts[begin + before] = s[u];
+        }
+        run += s_tmp[kWarps];
+        local = run;
+        __syncthreads();
       }
-      run += s_tmp[kWarps];
-      local = run;
-      __syncthreads();
+    } else {
+      for (long long base = begin; base < end; base += static_cast<long long>(FU) * kThreads) {
+        int s[FU];
+        uint32_t head[FU];
+#pragma unroll
+        for (int u = 0; u < FU; ++u) {
+          const long long i = base + u * kThreads + tid;
+          s[u] = i < end ? __ldcg(p.slot_of_point + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < FU; ++u) {
+          // Only a tile-group leader can be its pillar's first point.
+          head[u] = (s[u] >= 0 && (s[u] & kLeaderBit))
+                        ? static_cast<uint32_t>(__ldcg(p.lists + static_cast<size_t>(s[u] & ~kLeaderBit) * kHead) >> 32)
+                        : kEmpty;
+          s[u] = s[u] >= 0 ? (s[u] & ~kLeaderBit) : -1;
+        }
+        unsigned int ball[FU];
+#pragma unroll
+        for (int u = 0; u < FU; ++u) {
+          const long long i = base + u * kThreads + tid;
+          ball[u] = __ballot_sync(0xffffffffu, s[u] >= 0 && head[u] == static_cast<uint32_t>(i));
+          if (lane == 0) s_tile[u][warp] = __popc(ball[u]);
+        }
+        __syncthreads();
+        if (warp == 0) flag_prefix<FU>(&s_tile[0][0], &s_tmp[kWarps], lane);
+        __syncthreads();
+        unsigned int run = local;
+#pragma unroll
+        for (int u = 0; u < FU; ++u) {
+          const unsigned int before = run + s_tile[u][warp] + __popc(ball[u] & lanemask_lt());
+          if ((ball[u] >> lane) & 1u) p.firsts[begin + before] = s[u];
+          if (kBatched) {  // a frame start at i records this block's first points before it
+            const long long i = base + u * kThreads + tid;
+            if (i < end)
+              for (int b = frame_of(s_off, B, i); b >= 1 && s_off[b] == i; --b) p.frame_cnt[b] = before;
+          }
+        }
+        run += s_tmp[kWarps];
+        local = run;
+        __syncthreads();
+      }
     }
     PV_STAMP(3);
 
