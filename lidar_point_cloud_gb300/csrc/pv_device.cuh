@@ -25,6 +25,10 @@ constexpr int32_t kNoKey = -1;             // empty hashed slot
 #define PV_BLOCK_THREADS 1024
 #endif
 constexpr int kThreads = PV_BLOCK_THREADS;  // also the tile: points grouped together in shared memory
+#define PV_CAT_(a, b) a##b
+#define PV_CAT(a, b) PV_CAT_(a, b)
+// A build's own name for an entry point: name##<block threads>.
+#define PV_BLOCK_NAME(name) PV_CAT(name, PV_BLOCK_THREADS)
 constexpr int kWarps = kThreads / 32;
 static_assert(kWarps <= 32 && kWarps % 16 == 0, "warp 0 scans one value per warp; 16-byte counter rows");
 constexpr int kMinBlocksPerSM = 1024 / kThreads;
@@ -32,7 +36,7 @@ constexpr int kMaxCtas = 1024;             // blocks per launch (prefix lives in
 static_assert(kMaxCtas < 0x10000, "finished blocks are counted in 16 bits");
 constexpr int kFlagUnroll = 4;             // block-wide tiles in flight when flagging
 constexpr int kFlagUnrollWide = 8;         // the same, in launches whose chunks span up to 8 block tiles
-static_assert(kWarps == 32, "the flag prefix gives each lane U consecutive (tile, warp) counts");
+static_assert(kWarps == 32 || kWarps == 16, "the flag prefix gives each lane consecutive (tile, warp) counts");
 #ifndef PV_HEAD_ENTRIES
 #define PV_HEAD_ENTRIES 4
 #endif
@@ -311,12 +315,14 @@ static __device__ unsigned int block_exclusive_scan(unsigned int x, unsigned int
 // warp 0; *total receives the sum.  Lane l sums the U consecutive positions
 // from l * U, one warp scan orders the lanes' sums.
 template <int U>
-__device__ __forceinline__ void flag_prefix(unsigned int* flat, unsigned int* total, unsigned int lane) {
-  unsigned int c[U];
+static __device__ __forceinline__ void flag_prefix(unsigned int* flat, unsigned int* total, unsigned int lane) {
+  constexpr int E = U * kWarps / 32;  // consecutive (tile, warp) counts per lane
+  static_assert(E >= 1 && U * kWarps % 32 == 0, "whole counts per lane");
+  unsigned int c[E];
   unsigned int sum = 0;
 #pragma unroll
-  for (int k = 0; k < U; ++k) {
-    c[k] = flat[lane * U + k];
+  for (int k = 0; k < E; ++k) {
+    c[k] = flat[lane * E + k];
     sum += c[k];
   }
   unsigned int incl = sum;
@@ -327,8 +333,8 @@ __device__ __forceinline__ void flag_prefix(unsigned int* flat, unsigned int* to
   }
   unsigned int run = incl - sum;
 #pragma unroll
-  for (int k = 0; k < U; ++k) {
-    flat[lane * U + k] = run;
+  for (int k = 0; k < E; ++k) {
+    flat[lane * E + k] = run;
     run += c[k];
   }
   if (lane == 31) *total = incl;
@@ -647,7 +653,7 @@ struct TileMap {
   unsigned int* layout;      // rows handed out in the tile layout
 };
 
-__device__ __forceinline__ TileMap tile_map(unsigned char* base, unsigned int* layout) {
+static __device__ __forceinline__ TileMap tile_map(unsigned char* base, unsigned int* layout) {
   TileMap m;
   m.cnt = reinterpret_cast<unsigned int*>(base);
   m.key = reinterpret_cast<int*>(base + kTileHash * kWarps);
@@ -657,7 +663,7 @@ __device__ __forceinline__ TileMap tile_map(unsigned char* base, unsigned int* l
 }
 
 // Empty the map positions h = tid, tid + kThreads, ... (keys and counters).
-__device__ __forceinline__ void tile_clear(const TileMap& m, unsigned int tid) {
+static __device__ __forceinline__ void tile_clear(const TileMap& m, unsigned int tid) {
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   for (int h = static_cast<int>(tid); h < kTileHash; h += kThreads) {
     if (m.key[h] != -1) {
@@ -670,7 +676,7 @@ __device__ __forceinline__ void tile_clear(const TileMap& m, unsigned int tid) {
 }
 
 // The warp-group leader claims (or finds) the map position of `slot`.
-__device__ __forceinline__ int tile_claim(const TileMap& m, int slot) {
+static __device__ __forceinline__ int tile_claim(const TileMap& m, int slot) {
   unsigned int h = mix32(static_cast<unsigned int>(slot)) & (kTileHash - 1);
   for (int probe = 0; probe < kTileHash; ++probe) {  // at most kThreads keys: never full
     const int cur = atomicCAS(m.key + h, -1, slot);
@@ -689,7 +695,7 @@ __device__ __forceinline__ int tile_claim(const TileMap& m, int slot) {
 // that the values only decide to drop the group.  When the map is full both
 // fall back to 0, which is still a valid lower bound.
 
-__device__ __forceinline__ unsigned int chunk_rank(int* ckey, unsigned int* ccnt, int slot, unsigned int size) {
+static __device__ __forceinline__ unsigned int chunk_rank(int* ckey, unsigned int* ccnt, int slot, unsigned int size) {
   unsigned int h = mix32(static_cast<unsigned int>(slot) ^ 0x9e3779b9u) & (kChunkHash - 1);
   for (int probe = 0; probe < kChunkProbes; ++probe) {
     int cur = *reinterpret_cast<volatile int*>(ckey + h);  // a plain read first: most probes find a key
@@ -704,7 +710,7 @@ __device__ __forceinline__ unsigned int chunk_rank(int* ckey, unsigned int* ccnt
 // Each word holds four warps' counts (at most 64 each), summed with dp4a
 // against ones; the words before this warp's count whole, its own word only
 // in the bytes of lower warps.
-__device__ __forceinline__ void tile_counts(const TileMap& m, int h, unsigned int warp, unsigned int* before,
+static __device__ __forceinline__ void tile_counts(const TileMap& m, int h, unsigned int warp, unsigned int* before,
                                             unsigned int* total) {
   const uint4* row = reinterpret_cast<const uint4*>(m.cnt + static_cast<size_t>(h) * (kWarps / 4));
   const unsigned int pc = warp >> 2;                       // word holding this warp's byte
@@ -1157,16 +1163,28 @@ constexpr int kDsSmem = kDsHash * (4 + 4) + kDsHot * (4 + 16 + 16 + 4 + 4);
 
 // ------------------------------------------------------------ host side: launch entry points of the kernel files
 
+// The block-tile kernel is built twice: with 1024-thread blocks, one an SM
+// (pv_ordered.cu), and with 512-thread blocks, two an SM (pv_ordered_half.cu,
+// the same source), the second for clouds whose 1024-thread chunks would
+// span several tiles.  Each build names its entry points after its block
+// size.
+//
 // Shared-memory opt-in of the block-tile kernel's instantiations; the
 // resident blocks per SM of the one that fits fewest (0 on failure).
-int prepare_ordered();
+int prepare_ordered_1024();
+int prepare_ordered_512();
+// Dynamic shared memory of a launch of the block-tile kernel.
+int ordered_smem_1024();
+int ordered_smem_512();
 // Shared-memory opt-in of the downsampling kernel; its resident blocks per SM.
 int prepare_downsample();
 // One cooperative launch of the block-tile kernel: one frame (frame_offsets
 // null; queue picks the instantiation that shares long lists out per
 // block) or a batch of `frames` frames (host offsets, frames + 1 of them).
-cudaError_t launch_ordered(const cudaLaunchConfig_t& cfg, const KParams& kp, bool queue,
-                           const int64_t* frame_offsets, int frames, long long n);
+cudaError_t launch_ordered_1024(const cudaLaunchConfig_t& cfg, const KParams& kp, bool queue,
+                                const int64_t* frame_offsets, int frames, long long n);
+cudaError_t launch_ordered_512(const cudaLaunchConfig_t& cfg, const KParams& kp, bool queue,
+                               const int64_t* frame_offsets, int frames, long long n);
 cudaError_t launch_unordered(const cudaLaunchConfig_t& cfg, const KParams& kp);
 cudaError_t launch_downsample(const cudaLaunchConfig_t& cfg, const KParams& kp);
 

@@ -7,8 +7,10 @@
 // canonical order stated in pv.h.  How it is computed differs from the
 // page's one-thread-per-point kernel + Thrust copy_if + gather:
 //
-//   * one cooperative launch, one 1024-thread block per SM, all resident,
-//     and two grid-wide barriers;
+//   * one cooperative launch, one 1024-thread block per SM (two 512-thread
+//     blocks per SM, this file built again by pv_ordered_half.cu, for clouds
+//     whose 1024-thread chunks would span several tiles), all resident, and
+//     two grid-wide barriers;
 //   * phase 1 (before the first barrier): blocks sweep the cloud in tiles of
 //     1024 consecutive points (2048, two a thread, where a block's chunk
 //     spans several tiles), in index order across the grid.  Each point is
@@ -64,7 +66,7 @@ namespace {
 // 32S.w .. 32S.w + 32S - 1, sub-tile u the 32 of them from 32S.w + 32u.
 // With U = 2 a block's chunk starts with a one-sub-tile tile, and each next
 // tile takes two sub-tiles while the last one had few tile groups (at most
-// 512 per 1024 points to widen, 1280 per 2048 to stay wide), so the maps
+// kThreads / 2 to widen, 5/8 of 2 kThreads to stay wide), so the maps
 // stay at most 5/8 full: wide tiles halve the block barriers per point and
 // the tile groups per pillar on clouds whose consecutive points share
 // pillars; sparse clouds keep 1024-point tiles.
@@ -374,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       __syncthreads();  // (B) group offsets handed out; the previous map is empty
       PV_SUB(3);
       if (!kBatched && multi) {  // this tile's records, after the chunk's earlier ones, in index order
-        const unsigned int cw = s_wrec[lane];
+        const unsigned int cw = lane < static_cast<unsigned int>(kWarps) ? s_wrec[lane] : 0u;
         const unsigned int wbase = __reduce_add_sync(0xffffffffu, lane < warp ? cw : 0u);
         const unsigned int ttot = __reduce_add_sync(0xffffffffu, cw);
 #pragma unroll
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       int next = 1;
       if constexpr (U > 1) {  // this tile's groups are all counted (barrier B)
         const unsigned int g = s_groups[buf];
-        next = (nsub == 1 ? g <= 512u : g <= 1280u) ? 2 : 1;
+        next = (nsub == 1 ? g <= kThreads / 2u : g <= kThreads * 5u / 4u) ? 2 : 1;
       }
       if (next == nsub) {
 #pragma unroll
@@ -858,6 +860,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
 
 // ------------------------------------------------------------ host side
 
+// (static: the 512-thread build of this file has its own, with its own
+// shared-memory size)
 template <typename F>
 static int prepare_one(F kern) {
   int blocks = 0;
@@ -869,7 +873,7 @@ static int prepare_one(F kern) {
   return blocks;
 }
 
-int prepare_ordered() {
+int PV_BLOCK_NAME(prepare_ordered_)() {
   const int b[6] = {prepare_one(pv_voxelize_kernel<1, false, 1>), prepare_one(pv_voxelize_kernel<1, true, 1>),
                     prepare_one(pv_voxelize_kernel<1, false, 2>), prepare_one(pv_voxelize_kernel<1, true, 2>),
                     prepare_one(pv_voxelize_kernel<kMaxFrames, false, 1>),
@@ -881,8 +885,10 @@ int prepare_ordered() {
 
 // Launches whose block chunks span more than one 1024-point tile group
 // them in tiles of 1024 or 2048 points (U = 2), chosen tile by tile.
-cudaError_t launch_ordered(const cudaLaunchConfig_t& cfg, const KParams& kp, bool queue,
-                           const int64_t* frame_offsets, int frames, long long n) {
+int PV_BLOCK_NAME(ordered_smem_)() { return kDynSmem; }
+
+cudaError_t PV_BLOCK_NAME(launch_ordered_)(const cudaLaunchConfig_t& cfg, const KParams& kp, bool queue,
+                                           const int64_t* frame_offsets, int frames, long long n) {
   if (!frame_offsets) {
     Frames<1> fr;
     fr.off[0] = 0;
@@ -901,8 +907,9 @@ cudaError_t launch_ordered(const cudaLaunchConfig_t& cfg, const KParams& kp, boo
 
 }  // namespace pvk
 
-#ifdef PV_INSTRUMENT
-// Instrumented builds only: the stamps and counters of this file's kernels.
+#if defined(PV_INSTRUMENT) && PV_BLOCK_THREADS == 1024
+// Instrumented builds only: the stamps and counters of this file's kernels
+// (the 1024-thread build's).
 extern "C" {
 
 using namespace pvk;

@@ -89,23 +89,30 @@ def test_random_tiny_clouds():
 
 def test_chunk_sizes_around_tile_boundaries():
     # Each block owns ceil(N / blocks) points rounded up to a warp and sweeps
-    # them in tiles from its own start: 1024-point tiles while the chunk is
-    # one tile, else 2048-point tiles (two points a thread), so tiles start
-    # anywhere and a chunk may end with a short tile, or one whose second
-    # half is empty.  Sizes that make the chunk one warp, exactly one small
-    # tile, one small tile and a warp (one wide tile, half empty), one wide
-    # tile, one wide tile and a warp, two wide tiles and a warp; the points
-    # are KITTI-shaped returns repeated in sensor order, so pillars span
-    # tile and chunk boundaries.
+    # them in tiles from its own start: while a chunk fits one tile of as
+    # many points as the block has threads, one such tile; past that (on
+    # 512-thread blocks, two an SM, where the planner has that build) a
+    # first tile of one point a thread and then tiles of up to two.  So
+    # tiles start anywhere and a chunk may end with a short tile, or one
+    # whose second half is empty.  For each launch shape, chunks of one warp
+    # or exactly one tile, and around the first narrow and the wide tiles;
+    # the points are KITTI-shaped returns repeated in sensor order, so
+    # pillars span tile and chunk boundaries.
     P = synth.KITTI_PARAMS
     base, _ = synth.make("kitti")
-    ctas = pv.query_plan(len(base), P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)["ctas"]
-    for want_chunk, n in [(32, 32 * ctas - 7), (1024, 1024 * ctas - 3), (1056, 1024 * ctas + 1),
-                          (2048, 2048 * ctas - 5), (2080, 2048 * ctas + 40), (4128, 4096 * ctas + 40)]:
-        plan = pv.query_plan(n, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    args = (P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    small = pv.query_plan(len(base), *args)
+    c1, t1 = small["ctas"], small["threads"]
+    big = pv.query_plan(t1 * c1 + 1, *args)
+    c2, t2 = big["ctas"], big["threads"]
+    cases = [(32, 32 * c1 - 7), (t1, t1 * c1 - 3)]
+    cases += [(t2 + 32, t2 * c2 + 1), (2 * t2, 2 * t2 * c2 - 5), (2 * t2 + 32, 2 * t2 * c2 + 40),
+              (3 * t2, 3 * t2 * c2 - 3), (5 * t2 + 32, 5 * t2 * c2 + 40)]
+    for want_chunk, n in cases:
+        plan = pv.query_plan(n, *args)
         assert plan["points_per_cta"] == want_chunk, (n, plan["points_per_cta"])
         pts = np.tile(base, (n // len(base) + 1, 1))[:n]
-        assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+        assert_parity(pts, *args)
 
 
 def test_sparse_chunks_of_several_tiles():
