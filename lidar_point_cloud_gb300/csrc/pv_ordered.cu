@@ -618,10 +618,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     PV_STAMP(5);
 
     // ---- phase 2c+2d: every ranked pillar, kept or past the budget.  Every
-    // warp of the grid takes an equal contiguous share of the kept rows (so
-    // its output rows are contiguous) and an equal contiguous share of the
-    // pillars past the budget (which only have their lists emptied), and
-    // works through both together, 32 at a time.  Lane l finds the slot of
+    // warp of the grid takes an equal share of the kept rows and an equal
+    // share of the pillars past the budget (which only have their lists
+    // emptied), and works through both together, 32 at a time.  Lane l finds the slot of
     // its pillar and reads list positions 0..3 (one round trip each for 32
     // pillars).  Past the budget (its frame's, in a batch): a list known to
     // end inside positions 0..3 loses those, any other list every position.
@@ -635,12 +634,25 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     // (Counts of pillars and warps fit 32 bits: N < 2^29, at most 1024 x 32 warps.)
     const unsigned int dropped = kBatched ? s_dcum[B] : total - V;
     const unsigned int nw = static_cast<unsigned int>(nwarps), gw = static_cast<unsigned int>(gwarp);
-    const unsigned int pk = (V + nw - 1) / nw;
-    const unsigned int kw0 = gw * pk < V ? gw * pk : V;
-    const unsigned int nk = (kw0 + pk < V ? kw0 + pk : V) - kw0;
-    const unsigned int pd = (dropped + nw - 1) / nw;
-    const unsigned int dw0 = gw * pd < dropped ? gw * pd : dropped;
-    const unsigned int nd = (dw0 + pd < dropped ? dw0 + pd : dropped) - dw0;
+    // A contiguous share of ranks per warp, or, where warps have many rows
+    // (p.interleave), ranks gw, gw + nw, ...: pillars ranked near one another
+    // lie near one another, and their long lists would bunch up in a few
+    // blocks' shares.
+    unsigned int kw0, nk, dw0, nd, stride;
+    if (p.interleave) {
+      kw0 = dw0 = gw;
+      stride = nw;
+      nk = V > gw ? (V - gw - 1) / nw + 1 : 0u;
+      nd = dropped > gw ? (dropped - gw - 1) / nw + 1 : 0u;
+    } else {
+      const unsigned int pk = (V + nw - 1) / nw;
+      kw0 = gw * pk < V ? gw * pk : V;
+      nk = (kw0 + pk < V ? kw0 + pk : V) - kw0;
+      const unsigned int pd = (dropped + nw - 1) / nw;
+      dw0 = gw * pd < dropped ? gw * pd : dropped;
+      nd = (dw0 + pd < dropped ? dw0 + pd : dropped) - dw0;
+      stride = 1;
+    }
     for (unsigned int t0 = 0; t0 < nk + nd; t0 += 32) {
       const unsigned int t = t0 + lane;
       const bool valid = t < nk;                  // kept: an output row
@@ -650,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       unsigned int rank = 0;
       int fb = 0;
       if (valid) {
-        const unsigned int k = kw0 + t;  // the k-th row written (frames one after the other)
+        const unsigned int k = kw0 + t * stride;  // the k-th row written (frames one after the other)
         rank = k;
         row = k;
         if (kBatched) {
@@ -660,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
           row = static_cast<long long>(fb) * M + loc;
         }
       } else if (drop) {
-        const unsigned int j = dw0 + (t - nk);  // the j-th pillar past a budget
+        const unsigned int j = dw0 + (t - nk) * stride;  // the j-th pillar past a budget
         rank = M + j;
         if (kBatched) {
           const int b = slot_in_cum(s_dcum, B, j);
