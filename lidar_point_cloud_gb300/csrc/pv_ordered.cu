@@ -645,11 +645,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
       nk = V > gw ? (V - gw - 1) / nw + 1 : 0u;
       nd = dropped > gw ? (dropped - gw - 1) / nw + 1 : 0u;
     } else {
+      // Share s = warp * blocks + block: a block's shares lie spread over the
+      // rank range, so its queue meets its fair part of the long lists, and
+      // with fewer shares than warps every block keeps warps busy.
+      const unsigned int gs = warp * P + cta;
       const unsigned int pk = (V + nw - 1) / nw;
-      kw0 = gw * pk < V ? gw * pk : V;
+      kw0 = gs * pk < V ? gs * pk : V;
       nk = (kw0 + pk < V ? kw0 + pk : V) - kw0;
       const unsigned int pd = (dropped + nw - 1) / nw;
-      dw0 = gw * pd < dropped ? gw * pd : dropped;
+      dw0 = gs * pd < dropped ? gs * pd : dropped;
       nd = (dw0 + pd < dropped ? dw0 + pd : dropped) - dw0;
       stride = 1;
     }
