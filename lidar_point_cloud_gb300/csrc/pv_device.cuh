@@ -641,6 +641,7 @@ constexpr int kChunkProbes = PV_CHUNK_PROBES;  // a full chunk map costs this ma
 constexpr int kMapBytes = kTileHash * kWarps + kTileHash * 4 + kTileHash * 4;
 constexpr int kDynSmem = 2 * kMapBytes + 2 * 4 * kChunkHash;
 static_assert(kMapBytes % 16 == 0, "maps stay 16-byte aligned");
+static_assert(kWarps * 32 * 8 <= kMapBytes, "the gather's merge buffers fit one tile map");
 // After phase 1 the same shared memory holds the gather's per-warp merge
 // buffers (32 entries each) and the block's queue of long lists.
 constexpr unsigned int kQueueCap = kDynSmem / 8 - kWarps * 32;

@@ -125,7 +125,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     dirty_word = ld_relaxed(&p.ctl->dirty);
   }
   unsigned int bar_target = P;
-  bool alive = true;
+  // The dynamic shared memory this launch has: a launch of one-tile chunks
+  // without the long-list queue uses the first tile map alone (and the
+  // gather's merge buffers inside it), and the host gives it kMapBytes;
+  // every other launch needs kDynSmem.  Too little: an error, no work (the
+  // same in every block, so no barrier waits for a missing block).
+  unsigned int dyn_bytes;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+  const bool smem_short =
+      dyn_bytes < static_cast<unsigned int>(kDynSmem) && (U > 1 || kQueue || p.chunk > kThreads);
+  bool alive = !smem_short;
+  if (smem_short && cta == 0 && tid == 0) atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
   const int B = kBatched ? p.frames : 1;
   if (kBatched)
     for (int b = static_cast<int>(tid); b <= B; b += kThreads) s_off[b] = fr.off[b];  // read after a block barrier
@@ -138,14 +148,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     uint4* d4 = reinterpret_cast<uint4*>(s_dyn);
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     const uint4 m1 = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
-    const int maps = multi ? 2 : 1;
+    const int maps = smem_short ? 0 : (multi ? 2 : 1);
     for (int m = 0; m < maps; ++m) {
       uint4* base = d4 + m * (kMapBytes / 16);
       for (int j = static_cast<int>(tid); j < kTileHash * kWarps / 16; j += kThreads) base[j] = z;
       for (int j = static_cast<int>(tid); j < kTileHash * 4 / 16; j += kThreads)
         base[kTileHash * kWarps / 16 + j] = m1;
     }
-    if (multi) {
+    if (multi && !smem_short) {
       uint4* c4 = reinterpret_cast<uint4*>(ckey);
       for (int j = static_cast<int>(tid); j < kChunkHash / 4; j += kThreads) {
         c4[j] = m1;
@@ -164,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   const bool dirty = s_dirty != 0u;
 
   // Recovery after a failed launch: empty the whole table first.
-  if (dirty) {
+  if (dirty && alive) {
     reset_tables(p, gtid, gthreads);
     alive = grid_sync(p.ctl, bar_target, &s_flag);
     bar_target += P;
