@@ -643,7 +643,8 @@ constexpr int kDynSmem = 2 * kMapBytes + 2 * 4 * kChunkHash;
 static_assert(kMapBytes % 16 == 0, "maps stay 16-byte aligned");
 static_assert(kWarps * 32 * 8 <= kMapBytes, "the gather's merge buffers fit one tile map");
 // After phase 1 the same shared memory holds the gather's per-warp merge
-// buffers (32 entries each) and the block's queue of long lists.
+// buffers (32 entries each) and the block's queue of long lists (at most
+// kQueueCap entries; fewer when the launch has less dynamic shared memory).
 constexpr unsigned int kQueueCap = kDynSmem / 8 - kWarps * 32;
 constexpr unsigned int kQueueDrop = 0xFFFFFFFFu;  // queue row of a list past the budget (emptied only)
 constexpr int64_t kQueueMinRowsPerWarp = 8;        // rows per warp from which the gather queues long lists

@@ -126,14 +126,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   }
   unsigned int bar_target = P;
   // The dynamic shared memory this launch has: a launch of one-tile chunks
-  // without the long-list queue uses the first tile map alone (and the
-  // gather's merge buffers inside it), and the host gives it kMapBytes;
-  // every other launch needs kDynSmem.  Too little: an error, no work (the
-  // same in every block, so no barrier waits for a missing block).
+  // uses the first tile map alone (and, after phase 1, the gather's merge
+  // buffers and the long-list queue in the same space, the queue as long as
+  // it fits), and the host gives it kMapBytes; a launch of longer chunks
+  // needs kDynSmem.  Too little: an error, no work (the same in every
+  // block, so no barrier waits for a missing block).
   unsigned int dyn_bytes;
   asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
-  const bool smem_short =
-      dyn_bytes < static_cast<unsigned int>(kDynSmem) && (U > 1 || kQueue || p.chunk > kThreads);
+  const bool smem_short = dyn_bytes < static_cast<unsigned int>(kDynSmem) && (U > 1 || p.chunk > kThreads);
   bool alive = !smem_short;
   if (smem_short && cta == 0 && tid == 0) atomicMin(&p.ctl->err, PV_ERR_INTERNAL);
   const int B = kBatched ? p.frames : 1;
@@ -641,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     bool stale = false;
     unsigned long long* wbuf = reinterpret_cast<unsigned long long*>(s_dyn) + warp * 32;  // append lists' merge buffer
     unsigned long long* s_queue = reinterpret_cast<unsigned long long*>(s_dyn) + kWarps * 32;  // (row << 32) | slot
+    const unsigned int qcap = dyn_bytes / 8u - static_cast<unsigned int>(kWarps) * 32u;  // queue entries that fit
     // (Counts of pillars and warps fit 32 bits: N < 2^29, at most 1024 x 32 warps.)
     const unsigned int dropped = kBatched ? s_dcum[B] : total - V;
     const unsigned int nw = static_cast<unsigned int>(nwarps), gw = static_cast<unsigned int>(gwarp);
@@ -710,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
         unsigned int qb = 0;
         if (lane == 0 && lm) qb = atomicAdd(&s_qn, static_cast<unsigned int>(__popc(lm)));
         qb = __shfl_sync(0xffffffffu, qb, 0) + __popc(lm & lanemask_lt());
-        if (longv && qb < kQueueCap) {
+        if (longv && qb < qcap) {
           const unsigned int qrow = valid ? static_cast<unsigned int>(row) : kQueueDrop;
           s_queue[qb] = (static_cast<unsigned long long>(qrow) << 32) | static_cast<unsigned int>(slot);
           inl = false;
@@ -814,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     // The block's queued long lists, taken one at a time by whichever warp is free.
     if constexpr (kQueue) {
       __syncthreads();
-      const unsigned int qn = s_qn < kQueueCap ? s_qn : kQueueCap;
+      const unsigned int qn = s_qn < qcap ? s_qn : qcap;
       // Four queued lists at a time: append lists of up to seven entries are
       // served eight lanes a pillar; the rest one at a time by the whole warp.
       for (;;) {
