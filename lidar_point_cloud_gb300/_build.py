@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 # voxelizer, centroid downsampling, the host side with the C ABI, and farthest
 # point sampling (kernel and entry); pv_device.cuh is the kernels' shared code.
 SRCS = [os.path.join(CSRC, f) for f in ("pv_ordered.cu", "pv_ordered_half.cu", "pv_unordered.cu", "pv_downsample.cu",
-                                         "pv_host.cu", "pv_fps.cu")]
+                                         "pv_downsample_half.cu", "pv_host.cu", "pv_fps.cu")]
 HEADERS = [os.path.join(CSRC, "pv_device.cuh")]
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libpv.so")

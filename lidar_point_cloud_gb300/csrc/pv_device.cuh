@@ -1179,8 +1179,13 @@ int prepare_ordered_512();
 // Dynamic shared memory of a launch of the block-tile kernel.
 int ordered_smem_1024();
 int ordered_smem_512();
-// Shared-memory opt-in of the downsampling kernel; its resident blocks per SM.
-int prepare_downsample();
+// Shared-memory opt-in of the downsampling kernel (built with 1024- and with
+// 512-thread blocks, like the block-tile kernel); its resident blocks per SM.
+int prepare_downsample_1024();
+int prepare_downsample_512();
+// Dynamic shared memory of a launch of the downsampling kernel.
+int downsample_smem_1024();
+int downsample_smem_512();
 // One cooperative launch of the block-tile kernel: one frame (frame_offsets
 // null; queue picks the instantiation that shares long lists out per
 // block) or a batch of `frames` frames (host offsets, frames + 1 of them).
@@ -1189,6 +1194,7 @@ cudaError_t launch_ordered_1024(const cudaLaunchConfig_t& cfg, const KParams& kp
 cudaError_t launch_ordered_512(const cudaLaunchConfig_t& cfg, const KParams& kp, bool queue,
                                const int64_t* frame_offsets, int frames, long long n);
 cudaError_t launch_unordered(const cudaLaunchConfig_t& cfg, const KParams& kp);
-cudaError_t launch_downsample(const cudaLaunchConfig_t& cfg, const KParams& kp);
+cudaError_t launch_downsample_1024(const cudaLaunchConfig_t& cfg, const KParams& kp);
+cudaError_t launch_downsample_512(const cudaLaunchConfig_t& cfg, const KParams& kp);
 
 }  // namespace pvk

@@ -1,6 +1,8 @@
 // Voxel-grid centroid downsampling (pv_voxel_downsample): one cooperative
 // launch, two grid barriers; the reading and the design are in the comment
-// before the kernel.
+// before the kernel.  Built with 1024-thread blocks here and with 512-thread
+// blocks, two an SM, by pv_downsample_half.cu (entry points named after the
+// block size).
 
 #include "pv_device.cuh"
 
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
 
 // ------------------------------------------------------------ host side
 
-int prepare_downsample() {
+int PV_BLOCK_NAME(prepare_downsample_)() {
   int blocks = 0;
   if (cudaFuncSetAttribute(pv_downsample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDsSmem) !=
           cudaSuccess ||
@@ -367,7 +369,9 @@ int prepare_downsample() {
   return blocks;
 }
 
-cudaError_t launch_downsample(const cudaLaunchConfig_t& cfg, const KParams& kp) {
+int PV_BLOCK_NAME(downsample_smem_)() { return kDsSmem; }
+
+cudaError_t PV_BLOCK_NAME(launch_downsample_)(const cudaLaunchConfig_t& cfg, const KParams& kp) {
   return cudaLaunchKernelEx(&cfg, pv_downsample_kernel, kp);
 }
 
