@@ -80,6 +80,18 @@ def test_launch_shape_does_not_change_result(ctas_per_sm):
     assert_parity(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels, ctas_per_sm=ctas_per_sm)
 
 
+@pytest.mark.parametrize("ctas_per_sm", [1, 2])
+def test_launch_shape_512_thread_build(ctas_per_sm):
+    # The dense frame on the 512-thread build at one block an SM (6,912-point
+    # chunks; 25 kept rows a warp, so interleaved gather shares) and at two
+    # (3,456-point chunks; block-first contiguous shares).
+    pts, P = synth.make("dense")
+    args = (P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    plan = pv.query_plan(len(pts), *args, ctas_per_sm=ctas_per_sm)
+    assert plan["threads"] == 512 and plan["ctas"] % ctas_per_sm == 0, plan
+    assert_parity(pts, *args, ctas_per_sm=ctas_per_sm)
+
+
 def test_random_tiny_clouds():
     rng = np.random.Generator(np.random.PCG64(4242))
     for t in range(150):
