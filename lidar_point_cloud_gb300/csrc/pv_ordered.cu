@@ -12,10 +12,10 @@
 //     whose 1024-thread chunks would span several tiles), all resident, and
 //     two grid-wide barriers;
 //   * phase 1 (before the first barrier): blocks sweep the cloud in tiles of
-//     1024 consecutive points (2048, two a thread, where a block's chunk
-//     spans several tiles), in index order across the grid.  Each point is
-//     read with one 16-byte load and binned with IEEE round-to-nearest
-//     subtract/divide and floorf.  In shared memory the tile is grouped by
+//     consecutive points, one a thread (two a thread, tile by tile, where a
+//     block's chunk spans several tiles), in index order across the grid.
+//     Each point is read with one 16-byte load and binned with IEEE
+//     round-to-nearest subtract/divide and floorf.  In shared memory the tile is grouped by
 //     pillar (warp match + a small open-addressing map), which gives every
 //     point its rank among the tile's points of its pillar and lays the tile
 //     out group by group in a per-tile buffer.  Only each group's first point
@@ -69,7 +69,7 @@ namespace {
 // kThreads / 2 to widen, 5/8 of 2 kThreads to stay wide), so the maps
 // stay at most 5/8 full: wide tiles halve the block barriers per point and
 // the tile groups per pillar on clouds whose consecutive points share
-// pillars; sparse clouds keep 1024-point tiles.
+// pillars; sparse clouds keep tiles of one point a thread.
 template <int NF, bool kQueue, int U>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(const KParams p, const Frames<NF> fr) {
   static_assert(U == 1 || U == 2, "one or two points per thread in a tile");
