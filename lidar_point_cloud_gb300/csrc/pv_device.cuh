@@ -205,6 +205,14 @@ __device__ __forceinline__ unsigned int atom_add_acq_rel(unsigned int* p, unsign
   return old;
 }
 
+// Programmatic dependent launch: every launch of these kernels carries the
+// programmatic stream serialization attribute, so the next launch's set-up
+// may overlap this grid's end.  A kernel waits for the stream's previous
+// grid to complete, its memory operations visible, before it touches
+// memory, and lets the next grid launch once its own work is done.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned int lanemask_lt() {
   unsigned int m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));

@@ -65,6 +65,7 @@ __device__ __forceinline__ float mean_of(double s, unsigned int count) {
 
 
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kernel(const KParams p) {
+  wait_prior_grid();
   extern __shared__ __align__(16) unsigned char s_dyn[];
   __shared__ unsigned int s_prefix[kMaxCtas + 1];
   __shared__ unsigned int s_tile[kFlagUnroll][kWarps];
@@ -334,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
     }
   }
 
+  allow_next_grid();
   __syncthreads();
   if (tid == 0) {
     // Acquire-release count of finished blocks: the last one sees every

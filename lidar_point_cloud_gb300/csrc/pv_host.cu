@@ -434,11 +434,18 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   if (!pl.unordered && !pl.downsample && !pl.half && pl.chunk <= kThreads)
     cfg.dynamicSmemBytes = kMapBytes;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  // Cooperative (every block resident: the grid barriers) and programmatic
+  // stream serialization (the kernels wait for the previous grid first, so
+  // the launch's set-up may overlap that grid's end; measured: KITTI-shaped
+  // 15.65 -> 15.44 us, tiny 14.41 -> 13.76 us, dense 46.61 -> 45.78 us a launch
+  // back to back).
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e;
   if (pl.downsample) {
     cfg.dynamicSmemBytes = pl.half ? downsample_smem_512() : downsample_smem_1024();

@@ -74,6 +74,7 @@ template <int NF, bool kQueue, int U>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(const KParams p, const Frames<NF> fr) {
   static_assert(U == 1 || U == 2, "one or two points per thread in a tile");
   static_assert(U * kThreads <= kTileHash, "a tile's keys fit its map");
+  wait_prior_grid();
   constexpr bool kBatched = NF > 1;
   // Block tiles in flight in the first-point pass: 8 where chunks are long
   // (the launches that queue long lists), else 4 (fewer empty tiles to scan).
@@ -854,6 +855,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
 
   // ---- the last block to finish publishes the status and rearms the control block.
   PV_STAMP(7);
+  allow_next_grid();
   // A block counts itself finished, in the low half of the word, and, in the
   // high half, whether it knows of an error: one recorded before the second
   // barrier (read after it), a failed wait of its own, or one of its

@@ -39,6 +39,7 @@ __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned lon
 }
 
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel(const KParams p) {
+  wait_prior_grid();
   __shared__ int s_flag;
   __shared__ unsigned int s_dirty;
   __shared__ unsigned int s_total;
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_unordered_kernel
     }
   }
 
+  allow_next_grid();
   __syncthreads();
   if (tid == 0) {
     // Acquire-release count of finished blocks: the last one sees every
