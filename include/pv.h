@@ -230,9 +230,13 @@ int pv_voxelize_ex(const float* points, int64_t num_points, const float point_cl
 /*
  * pv_voxelize_host - the same operation on HOST buffers, synchronous.
  *
- * Runs pv_voxelize on `stream` for a cloud in host memory, fills all four
- * host outputs (the full padded [max_voxels, ...] buffers) and waits for the
- * stream.  Pinned buffers (page-locked and mapped: cudaHostAlloc,
+ * Runs pv_voxelize on `stream` for a cloud in host memory, writes the first
+ * V rows of the three row outputs (each voxel row zero-padded past its
+ * count, as pv_voxelize writes it) and V itself, and waits for the stream.
+ * Rows V .. max_voxels-1 of the host buffers are left as they were: the
+ * result is the outputs sliced to the pillar count, as the page's Python
+ * entry point returns them ("Voxelize" > "The PyTorch side"), and no zero row
+ * crosses the host link.  Pinned buffers (page-locked and mapped: cudaHostAlloc,
  * cudaHostRegister) aligned as pv_voxelize requires (16 bytes for points and
  * voxels, 4 for the rest) are used in place: the kernel reads the points and
  * writes the outputs across the host link.  Any other host buffer (pageable,

@@ -261,11 +261,12 @@ def voxelize_host(points, point_cloud_range, voxel_size, max_points: int = 32, m
                   out=None, stream=None):
     """Voxelize a host cloud (NumPy or CPU torch, [N, 4] float32) through pv_voxelize_host.
 
-    Runs on the current CUDA device and fills ``out`` (NumPy arrays or CPU
-    torch tensors; NumPy arrays are allocated if None) with the padded
-    outputs; returns (voxels [M,K,4], coords [M,3], counts [M], V).  Pinned
-    buffers (for example ``torch.empty(..).pin_memory()``) are read and
-    written in place by the kernel; other host memory is staged on the
+    Runs on the current CUDA device and writes the first V rows of ``out``
+    (NumPy arrays or CPU torch tensors of max_voxels rows; NumPy arrays are
+    allocated if None); rows past V are left as they were.  Returns
+    (voxels [V,K,4], coords [V,3], counts [V], V): views of those rows.
+    Pinned buffers (for example ``torch.empty(..).pin_memory()``) are read
+    and written in place by the kernel; other host memory is staged on the
     device.
     """
     import numpy as np
@@ -290,7 +291,8 @@ def voxelize_host(points, point_cloud_range, voxel_size, max_points: int = 32, m
                                  handle)
     if st != 0:
         raise PVError(st, "pv_voxelize_host")
-    return vox, coords, counts, ctypes.c_int32.from_address(num_ptr).value
+    V = ctypes.c_int32.from_address(num_ptr).value
+    return vox[:V], coords[:V], counts[:V], V
 
 
 def alloc_batch_outputs(num_frames: int, max_points: int, max_voxels: int, device):

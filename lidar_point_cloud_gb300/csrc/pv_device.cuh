@@ -108,6 +108,7 @@ struct KParams {
   int KT;            // tail entries per slot (max_points rounded up to 4, less kHead; >= 0)
   int append;        // 1: append lists (kAppendMinK <= max_points <= 32), 0: sorted lists
   int interleave;    // gather: 1: warp w takes ranks w, w + warps, ...; 0: a contiguous share
+  int zero_tail;     // 1: rows V .. max_voxels-1 are zero-filled; 0: left as they were
   unsigned long long* pool;  // append lists: overflow lists, kHead + KT words each
   unsigned int pool_n;       // overflow lists available
   int max_voxels;

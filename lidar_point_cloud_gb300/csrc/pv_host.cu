@@ -64,6 +64,7 @@ std::map<std::pair<int, pv_stream_t>, Workspace*> g_ws;
 
 struct Plan {
   unsigned int stall = 0;  // test hook (pv_options.test_stall_barrier)
+  bool keep_tail = false;  // rows past V left unwritten (pv_voxelize_host)
   int frames = 1;
   bool batched = false;    // pv_voxelize_batch (any frame count): batched layout of the outputs
   bool downsample = false; // pv_voxel_downsample: per-voxel accumulators instead of lists
@@ -387,6 +388,7 @@ int launch(Workspace* ws, const Plan& pl, const float* points, int64_t N, const 
   kp.max_voxels = M;
   kp.hash_mode = pl.mode == 2 ? 1 : 0;
   kp.bar_extra = pl.stall;
+  kp.zero_tail = pl.keep_tail ? 0 : 1;
   kp.table_mask = pl.mask;
   kp.lists = ws->lists;
   kp.tails = ws->lists + static_cast<size_t>(pl.T) * kHead;
@@ -724,6 +726,10 @@ int pv_voxelize_host(const float* points_host, int64_t num_points, const float p
   std::lock_guard<std::mutex> lk(ws->mu);
   if ((st = reserve(ws, pl, num_points, stream)) != PV_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The result is the first V rows (the page's Python entry point slices
+  // its padded outputs to the pillar count): rows past V are not written,
+  // so no zero row crosses the host link.
+  pl.keep_tail = true;
   // Pinned buffers (page-locked and mapped) are used in place: the kernel
   // reads the points and writes the outputs across the host link itself, so
   // each byte crosses it once, as with copies, without a copy's set-up or
@@ -763,13 +769,17 @@ int pv_voxelize_host(const float* points_host, int64_t num_points, const float p
     if ((st = launch(ws, pl, in_pts, num_points, point_cloud_range, voxel_size, max_points, max_voxels, d_vox,
                      d_crd, d_cnt, d_num, stream)) != PV_OK)
       return st;
-    if (cudaMemcpyAsync(out_voxels_host, d_vox, 16 * static_cast<size_t>(max_voxels) * max_points,
-                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyAsync(out_coords_host, d_crd, 12 * static_cast<size_t>(max_voxels), cudaMemcpyDeviceToHost,
-                        s) != cudaSuccess ||
-        cudaMemcpyAsync(out_counts_host, d_cnt, 4 * static_cast<size_t>(max_voxels), cudaMemcpyDeviceToHost, s) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(out_num_voxels_host, d_num, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    // V first, then its rows only.
+    if (cudaMemcpyAsync(out_num_voxels_host, d_num, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return PV_ERR_CUDA;
+    const int32_t V = *out_num_voxels_host;
+    if (V < 0) return V;
+    const size_t rows = static_cast<size_t>(std::min(V, max_voxels));
+    if (rows > 0 &&
+        (cudaMemcpyAsync(out_voxels_host, d_vox, 16 * rows * max_points, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+         cudaMemcpyAsync(out_coords_host, d_crd, 12 * rows, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+         cudaMemcpyAsync(out_counts_host, d_cnt, 4 * rows, cudaMemcpyDeviceToHost, s) != cudaSuccess))
       return PV_ERR_CUDA;
   }
   if (cudaStreamSynchronize(s) != cudaSuccess) return PV_ERR_CUDA;

@@ -615,10 +615,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
     // ---- phase 2e, issued first: zero rows V .. max_voxels-1 (of every
     // frame; all blocks share it).  These stores depend on nothing else, so
     // they overlap the gather's load latencies instead of trailing it.
+    // Skipped where the caller takes only the first V rows (outputs in host
+    // memory, where every byte crosses the host link).
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     const size_t Kz = static_cast<size_t>(K);
     constexpr size_t cw = kBatched ? 4 : 3;
-    for (int b = 0; b < B; ++b) {
+    for (int b = 0; b < (p.zero_tail ? B : 0); ++b) {
       const unsigned int Vb = kBatched ? s_vcum[b + 1] - s_vcum[b] : V;
       const size_t lo = static_cast<size_t>(b) * M + Vb, hi = static_cast<size_t>(b + 1) * M;
       for (size_t q = lo * Kz + gtid; q < hi * Kz; q += gthreads) p.out_voxels[q] = z4;

@@ -288,21 +288,34 @@ def test_two_streams():
         assert same_bits(out[0].cpu().numpy(), ov)
 
 
+def check_host_result(res, out, oracle_out, fill):
+    # The host entry point's result is the first V rows; rows past V keep
+    # what the caller had in them.
+    vox, coords, counts, V = res
+    st, ov, oc, on, oV = oracle_out
+    assert V == oV and vox.shape[0] == coords.shape[0] == counts.shape[0] == oV
+    vox, coords, counts = (np.asarray(a) for a in (vox, coords, counts))
+    assert same_bits(vox, ov[:oV]) and same_bits(coords, oc[:oV]) and same_bits(counts, on[:oV])
+    if out is not None:
+        for a in out[:3]:
+            tail = np.asarray(a)[oV:]
+            assert (tail == fill).all()
+
+
 def test_host_entry_point():
     pts, P = synth.make("kitti")
-    vox, coords, counts, V = pv.voxelize_host(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
-    st, ov, oc, on, oV = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
-    assert V == oV and same_bits(vox, ov) and same_bits(coords, oc) and same_bits(counts, on)
+    res = pv.voxelize_host(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    check_host_result(res, None, oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels), 0)
 
 
-@pytest.mark.parametrize("name", ["kitti", "dense"])
+@pytest.mark.parametrize("name", ["kitti", "dense", "tiny"])
 def test_host_entry_point_pinned_buffers_in_place(name):
     # Pinned input and outputs: the kernel reads and writes them across the
     # host link; pinned input with pageable outputs, and the reverse, mix
     # in-place use with staging copies.
     pts, P = synth.make(name)
     K, M = P.max_points, P.max_voxels
-    st, ov, oc, on, oV = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, K, M)
+    ref = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, K, M)
     pin_pts = torch.from_numpy(pts).pin_memory().numpy()
     shapes = (((M, K, 4), torch.float32), ((M, 3), torch.int32), ((M,), torch.int32), ((1,), torch.int32))
     pinned = tuple(torch.full(sh, 7, dtype=dt).pin_memory().numpy() for sh, dt in shapes)
@@ -311,9 +324,8 @@ def test_host_entry_point_pinned_buffers_in_place(name):
     for src, out in ((pin_pts, pinned), (pin_pts, pageable), (pts, pinned), (torch.from_numpy(pin_pts), tensors)):
         for a in out:
             a.fill(7) if isinstance(a, np.ndarray) else a.fill_(7)
-        vox, coords, counts, V = pv.voxelize_host(src, P.point_cloud_range, P.voxel_size, K, M, out=out)
-        vox, coords, counts = (np.asarray(a) for a in (vox, coords, counts))
-        assert V == oV and same_bits(vox, ov) and same_bits(coords, oc) and same_bits(counts, on)
+        res = pv.voxelize_host(src, P.point_cloud_range, P.voxel_size, K, M, out=out)
+        check_host_result(res, out, ref, 7)
 
 
 def test_host_entry_point_misaligned_pinned_input():
@@ -324,9 +336,8 @@ def test_host_entry_point_misaligned_pinned_input():
     view = buf[1:].reshape(-1, 4)
     view[:] = pts
     assert view.ctypes.data % 16 != 0
-    vox, coords, counts, V = pv.voxelize_host(view, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
-    st, ov, oc, on, oV = oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
-    assert V == oV and same_bits(vox, ov) and same_bits(coords, oc) and same_bits(counts, on)
+    res = pv.voxelize_host(view, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels)
+    check_host_result(res, None, oracle.voxelize(pts, P.point_cloud_range, P.voxel_size, P.max_points, P.max_voxels), 0)
 
 
 def test_sliced_python_entry_point():
