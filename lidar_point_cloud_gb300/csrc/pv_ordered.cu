@@ -43,7 +43,8 @@
 //     its owner block by binary search in the prefix, reads its groups,
 //     gathers the first max_points points (16-byte rows) and writes the row
 //     stack, coordinates and count; the slots of pillars past the budget are
-//     emptied; rows past V are zero-filled.
+//     emptied; rows past V are zero-filled (left as they were for a
+//     caller that takes only the first V rows: the host-buffer entry point).
 //
 // The table cleans itself: every slot a call fills is emptied by the same
 // call, so no memset runs per call.  A launch that fails on the device marks
