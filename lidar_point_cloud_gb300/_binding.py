@@ -262,10 +262,12 @@ def voxelize_host(points, point_cloud_range, voxel_size, max_points: int = 32, m
     """Voxelize a host cloud (NumPy or CPU torch, [N, 4] float32) through pv_voxelize_host.
 
     Runs on the current CUDA device and writes the first V rows of ``out``
-    (NumPy arrays or CPU torch tensors of max_voxels rows; NumPy arrays are
-    allocated if None); rows past V are left as they were.  Returns
-    (voxels [V,K,4], coords [V,3], counts [V], V): views of those rows.
-    Pinned buffers (for example ``torch.empty(..).pin_memory()``) are read
+    (NumPy arrays or CPU torch tensors of max_voxels rows); rows past V are
+    left as they were.  Returns (voxels, coords, counts, V): with ``out``
+    given, its buffers themselves (the result is their first V rows: no
+    slicing here, which would cost a few microseconds a call on torch
+    tensors); with ``out`` None, NumPy arrays allocated here, sliced to
+    [V,K,4], [V,3] and [V].  Pinned buffers (for example ``torch.empty(..).pin_memory()``) are read
     and written in place by the kernel; other host memory is staged on the
     device.
     """
@@ -280,7 +282,8 @@ def voxelize_host(points, point_cloud_range, voxel_size, max_points: int = 32, m
         pts = np.ascontiguousarray(np.asarray(points, dtype=np.float32)).reshape(-1, 4)
         n = int(pts.shape[0])
         pts_ptr = pts.ctypes.data if n else 0
-    if out is None:
+    own = out is None
+    if own:
         out = (np.empty((max_voxels, max_points, 4), np.float32), np.empty((max_voxels, 3), np.int32),
                np.empty((max_voxels,), np.int32), np.empty((1,), np.int32))
     vox, coords, counts, num = out
@@ -292,7 +295,9 @@ def voxelize_host(points, point_cloud_range, voxel_size, max_points: int = 32, m
     if st != 0:
         raise PVError(st, "pv_voxelize_host")
     V = ctypes.c_int32.from_address(num_ptr).value
-    return vox[:V], coords[:V], counts[:V], V
+    if own:
+        return vox[:V], coords[:V], counts[:V], V
+    return vox, coords, counts, V
 
 
 def alloc_batch_outputs(num_frames: int, max_points: int, max_voxels: int, device):

@@ -293,8 +293,12 @@ def check_host_result(res, out, oracle_out, fill):
     # what the caller had in them.
     vox, coords, counts, V = res
     st, ov, oc, on, oV = oracle_out
-    assert V == oV and vox.shape[0] == coords.shape[0] == counts.shape[0] == oV
-    vox, coords, counts = (np.asarray(a) for a in (vox, coords, counts))
+    assert V == oV
+    if out is None:  # arrays of the wrapper's own, sliced to V
+        assert vox.shape[0] == coords.shape[0] == counts.shape[0] == oV
+    else:  # the caller's buffers themselves
+        assert all(r is o for r, o in zip(res[:3], out[:3]))
+    vox, coords, counts = (np.asarray(a)[:oV] for a in (vox, coords, counts))
     assert same_bits(vox, ov[:oV]) and same_bits(coords, oc[:oV]) and same_bits(counts, on[:oV])
     if out is not None:
         for a in out[:3]:
