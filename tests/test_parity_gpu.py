@@ -7,8 +7,9 @@ equality.  Covers the five workloads at full size, random tiny clouds where
 both caps bind, edge cases (empty, one point, all invalid, one pillar with
 many points, caps of 1, caps not a multiple of 4 or 32), both table modes,
 several launch shapes, repeated runs (determinism), two streams at once,
-the host-buffer entry point and the device error paths (undersized table,
-recovery afterwards).
+the host-buffer entry point (whose result is the first V rows: those are
+compared, and the rows past V must still hold what the caller put there)
+and the device error paths (undersized table, recovery afterwards).
 """
 
 from __future__ import annotations
