@@ -79,7 +79,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_voxelize_kernel(
   constexpr bool kBatched = NF > 1;
   // Block tiles in flight in the first-point pass: 8 where chunks are long
   // (the launches that queue long lists), else 4 (fewer empty tiles to scan).
-  constexpr int FU = kQueue ? kFlagUnrollWide : kFlagUnroll;
+  // With one point a thread a chunk is one tile (at most kThreads points):
+  // its pass over points is one block tile (two on 512-thread blocks, so
+  // that the counts fill whole lanes).
+  constexpr int FU = U == 1 ? (kWarps >= 32 ? 1 : 32 / kWarps) : (kQueue ? kFlagUnrollWide : kFlagUnroll);
   extern __shared__ __align__(16) unsigned char s_dyn[];
   __shared__ unsigned int s_prefix[kMaxCtas + 1];
   __shared__ long long s_off[NF + 1];
