@@ -64,6 +64,47 @@ __device__ __forceinline__ float mean_of(double s, unsigned int count) {
 }
 
 
+// First points of [begin, end) (a point whose index is its voxel's first),
+// compacted in index order into firsts[begin ...]; FU block tiles a step.
+// s_tile holds FU x kWarps counts, s_tmp kWarps + 1.  Returns the count.
+template <int FU>
+static __device__ unsigned int flag_firsts(const KParams& p, long long begin, long long end, unsigned int* s_tile,
+                                           unsigned int* s_tmp) {
+  const unsigned int tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+  unsigned int local = 0;
+  for (long long base = begin; base < end; base += static_cast<long long>(FU) * kThreads) {
+    int s[FU];
+    unsigned int fc[FU];
+#pragma unroll
+    for (int u = 0; u < FU; ++u) {
+      const long long i = base + u * kThreads + tid;
+      s[u] = i < end ? __ldcg(p.slot_of_point + i) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < FU; ++u) {
+      fc[u] = (s[u] >= 0 && (s[u] & kLeaderBit)) ? __ldcg(&p.acc[s[u] & ~kLeaderBit].first_c) : 0u;
+      s[u] = s[u] >= 0 ? (s[u] & ~kLeaderBit) : -1;
+    }
+    unsigned int ball[FU];
+#pragma unroll
+    for (int u = 0; u < FU; ++u) {
+      const long long i = base + u * kThreads + tid;
+      ball[u] = __ballot_sync(0xffffffffu, s[u] >= 0 && fc[u] == ~static_cast<unsigned int>(i));
+      if (lane == 0) s_tile[u * kWarps + warp] = __popc(ball[u]);
+    }
+    __syncthreads();
+    if (warp == 0) flag_prefix<FU>(s_tile, &s_tmp[kWarps], lane);
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < FU; ++u)
+      if ((ball[u] >> lane) & 1u)
+        p.firsts[begin + local + s_tile[u * kWarps + warp] + __popc(ball[u] & lanemask_lt())] = s[u];
+    local += s_tmp[kWarps];
+    __syncthreads();
+  }
+  return local;
+}
+
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kernel(const KParams p) {
   wait_prior_grid();
   extern __shared__ __align__(16) unsigned char s_dyn[];
@@ -253,37 +294,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSM) pv_downsample_kerne
   unsigned int V = 0;
   if (alive) {
     // ---- phase D2: first points of this block's range, compacted in index order.
-    unsigned int local = 0;
-    for (long long base = begin; base < end; base += static_cast<long long>(kFlagUnroll) * kThreads) {
-      int s[kFlagUnroll];
-      unsigned int fc[kFlagUnroll];
-#pragma unroll
-      for (int u = 0; u < kFlagUnroll; ++u) {
-        const long long i = base + u * kThreads + tid;
-        s[u] = i < end ? __ldcg(p.slot_of_point + i) : -1;
-      }
-#pragma unroll
-      for (int u = 0; u < kFlagUnroll; ++u) {
-        fc[u] = (s[u] >= 0 && (s[u] & kLeaderBit)) ? __ldcg(&p.acc[s[u] & ~kLeaderBit].first_c) : 0u;
-        s[u] = s[u] >= 0 ? (s[u] & ~kLeaderBit) : -1;
-      }
-      unsigned int ball[kFlagUnroll];
-#pragma unroll
-      for (int u = 0; u < kFlagUnroll; ++u) {
-        const long long i = base + u * kThreads + tid;
-        ball[u] = __ballot_sync(0xffffffffu, s[u] >= 0 && fc[u] == ~static_cast<unsigned int>(i));
-        if (lane == 0) s_tile[u][warp] = __popc(ball[u]);
-      }
-      __syncthreads();
-      if (warp == 0) flag_prefix<kFlagUnroll>(&s_tile[0][0], &s_tmp[kWarps], lane);
-      __syncthreads();
-#pragma unroll
-      for (int u = 0; u < kFlagUnroll; ++u)
-        if ((ball[u] >> lane) & 1u)
-          p.firsts[begin + local + s_tile[u][warp] + __popc(ball[u] & lanemask_lt())] = s[u];
-      local += s_tmp[kWarps];
-      __syncthreads();
-    }
+    // A chunk of one block tile (at most kThreads points) takes one step of
+    // one tile (two on 512-thread blocks, so that one lane holds one whole
+    // count); longer chunks take kFlagUnroll tiles a step.
+    const unsigned int local = end - begin <= static_cast<long long>(kThreads)
+                                   ? flag_firsts<(kWarps >= 32 ? 1 : 32 / kWarps)>(p, begin, end, &s_tile[0][0], s_tmp)
+                                   : flag_firsts<kFlagUnroll>(p, begin, end, &s_tile[0][0], s_tmp);
     if (tid == 0) p.counts[cta] = local;
     alive = grid_sync(p.ctl, bar_target + P, &s_flag);
   }
